@@ -1,0 +1,427 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA operator's hot path on one GB300 (or N replicas).
+
+One step = one packed-sequence prefill of 131072 + 65536 + 32768 + 8192
+tokens at H=96, dk=dv=128, bf16 inputs / fp32 state (kda_chunk_fwd), then one
+decode step of 256 sequences at H=96, d=128 with the 1.6 GB fp32 state
+(kda_decode_step).  Inputs are seeded synthetic tensors resident in HBM
+before the timed region; both working sets exceed the 129 MB L2 (29 GB of
+prefill inputs, 1.6 GB of decode state), so no L2 flush is needed.
+
+value      : prefill tokens/s (token positions, all 96 heads each), timed over
+             the prefill launches with CUDA events on the launching stream.
+decode     : state GB/s of the decode step (2 * N*H*dk*dv*4 bytes per step).
+roofline   : the dominant kernel's algorithmic bytes / launch time vs the
+             measured HBM copy bandwidth.
+e2e        : prefill tokens/s through the same API with pinned host buffers:
+             host->device copies of the step's inputs, the call and the
+             device->host read of out and final_state, all inside the timing.
+cpu_baseline / --impl reference : the fp64 CPU oracle on a bounded sample of
+             the same workload, on the host's cores.
+
+Multi-GPU (torchrun): every rank runs an independent replica of the
+workload (the (sequence, head) chains share nothing), no collective on the
+data path; the barrier and a max-over-ranks of the timings are the only
+communication.  value = all ranks' tokens / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gated_delta_rule_11_gb300 import inputs as kin  # noqa: E402
+
+METRIC = "KDA prefill tokens/s (H=96,d=128) + % TC peak; decode step state GB/s vs HBM"
+PREFILL = kin.WORKLOADS["varlen_bf16_H96_237568"]
+DECODE = kin.WORKLOADS["decode_bf16_N256_H96"]
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# Algorithmic work per token and head, d = dk = dv = 128, 16-token tiles:
+# flops 6 d^2 (state products) + 2*16*(3d + 2d) (intra-tile products);
+# bytes: q, k, v, g_raw (4 d bf16) + beta (bf16) + out (d bf16).
+D = 128
+FLOPS_PER_TOKEN_HEAD = 6 * D * D + 2 * 16 * (3 * D + 2 * D)
+BYTES_PER_TOKEN_HEAD = 4 * D * 2 + 2 + D * 2
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(*names):
+    h = hashlib.sha1()
+    for n in names:
+        with open(os.path.join(ROOT, "gated_delta_rule_11_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def recorded_traffic(kernel_key, src_hash):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the kernel source as it is now (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e or e.get("source_sha1") != src_hash:
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu_index = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+def time_region(fn, steps, stream):
+    """CUDA-event time of each call of fn on `stream`, in ms (list)."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for i in range(steps):
+        evs[i][0].record(stream)
+        fn(i)
+        evs[i][1].record(stream)
+    return evs
+
+
+def run_cpu_oracle_sample(seconds_target, nthreads=None):
+    """Time the fp64 oracle on a bounded sample of the prefill workload: the
+    32768-token sequence, successive heads, until about `seconds_target` of
+    wall time.  Returns (tokens/s expressed at H=96, sample description, threads)."""
+    import oracle
+    w = PREFILL
+    T, dk, dv = 32768, w.dk, w.dv
+    nt = oracle.default_threads() if nthreads is None else nthreads
+    per_round = max(1, nt)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(1234)
+    done_heads, elapsed = 0, 0.0
+    while elapsed < seconds_target and done_heads < w.H:
+        nh = min(per_round, w.H - done_heads)
+        sample = kin.make_prefill_inputs(w, device="cpu", seed=w.seed + 100 + done_heads,
+                                         B=1, T=T, seqlens=(), H=nh)
+        args = [sample[n] for n in ("q", "k", "v", "g_raw", "beta")]
+        t0 = time.perf_counter()
+        oracle.kda_oracle_fwd(*args, None, None, nthreads=nt)
+        elapsed += time.perf_counter() - t0
+        done_heads += nh
+    token_heads = done_heads * T
+    rate = token_heads / elapsed / w.H
+    desc = (f"oracle (fp64, C, {nt} threads) on the 32768-token sequence of the packed "
+            f"workload, {done_heads} of 96 heads ({token_heads} token-heads) in {elapsed:.1f} s; "
+            f"tokens/s = token-heads/s / 96")
+    return rate, desc, nt
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world, local)
+
+
+def reduce_max(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_reference(args, rank, world):
+    """The oracle arm: each step runs the fp64 CPU oracle on a bounded sample
+    (16 heads of the 8192-token sequence) of the same workload."""
+    if rank != 0:
+        return 0
+    import oracle
+    w = PREFILL
+    T, nh = 8192, 16
+    sample = kin.make_prefill_inputs(w, device="cpu", seed=w.seed + 77, B=1, T=T, seqlens=(), H=nh)
+    a = [sample[n] for n in ("q", "k", "v", "g_raw", "beta")]
+    nt = oracle.default_threads()
+    for _ in range(args.warmup):
+        oracle.kda_oracle_fwd(*a, None, None, nthreads=nt)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.kda_oracle_fwd(*a, None, None, nthreads=nt)
+    dt = time.perf_counter() - t0
+    tok_per_s = args.steps * T * nh / dt / w.H
+    desc = (f"oracle (fp64, C, {nt} threads): per step 16 of 96 heads of the 8192-token "
+            f"sequence ({T * nh} token-heads); tokens/s = token-heads/s / 96")
+    line = {"impl": "reference", "metric": METRIC, "value": tok_per_s, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "varlen_bf16_H96_237568 (sampled)", "H": 96, "dk": 128,
+                       "dv": 128, "sample": "16 heads x 8192 tokens per step"},
+            "cpu_baseline": {"value": tok_per_s, "unit": "tokens/s", "cores": nt,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": tok_per_s, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, rank, world, local):
+    from gated_delta_rule_11_gb300 import kda
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    kda.load_library()
+    peaks, peak_src = load_peaks()
+
+    # ---- inputs, resident in HBM
+    pw = PREFILL
+    inp = kin.make_prefill_inputs(pw, device=dev, seed=pw.seed + 1000 * rank)
+    q, k, v, g, b = (inp[n] for n in ("q", "k", "v", "g_raw", "beta"))
+    cu = inp["cu_seqlens"]
+    N = len(pw.seqlens)
+    T_total = sum(pw.seqlens)
+    out = torch.empty((1, T_total, pw.H, pw.dv), dtype=torch.bfloat16, device=dev)
+    fin = torch.empty((N, pw.H, pw.dk, pw.dv), dtype=torch.float32, device=dev)
+
+    dw = DECODE
+    S = kin.make_decode_state(dw, device=dev, seed=dw.seed + 1000 * rank)
+    toks = [kin.make_decode_token(dw, i, device=dev, seed=dw.seed + 1000 * rank) for i in range(4)]
+    dout = torch.empty((dw.N, dw.H, dw.dv), dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream(dev)
+
+    def prefill(_i):
+        kda.kda_chunk_fwd(q, k, v, g, b, None, cu, out=out, final_state=fin)
+
+    def decode(i):
+        t = toks[i % len(toks)]
+        kda.kda_decode_step(t["q"], t["k"], t["v"], t["g_raw"], t["beta"], S, out=dout)
+
+    for i in range(args.warmup):
+        prefill(i)
+        decode(i)
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps of (prefill, decode)
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.1)
+    launches0 = kda.launch_count()
+    t_wall0 = time.perf_counter()
+    ev_all0 = torch.cuda.Event(enable_timing=True)
+    ev_all1 = torch.cuda.Event(enable_timing=True)
+    pev, dev_ev = [], []
+    ev_all0.record(stream)
+    for i in range(args.steps):
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        prefill(i)
+        e1.record(stream)
+        decode(i)
+        e2.record(stream)
+        pev.append((e0, e1))
+        dev_ev.append((e1, e2))
+    ev_all1.record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    launches = kda.launch_count() - launches0
+    barrier(world)
+    clocks = sampler.stop()
+
+    prefill_ms = [a.elapsed_time(c) for a, c in pev]
+    decode_ms = [a.elapsed_time(c) for a, c in dev_ev]
+    total_ms = ev_all0.elapsed_time(ev_all1)
+    p_mean = reduce_max(statistics.fmean(prefill_ms), world)
+    d_mean = reduce_max(statistics.fmean(decode_ms), world)
+    step_ms = reduce_max(total_ms / args.steps, world)
+
+    tokens = T_total * world
+    value = tokens / (p_mean * 1e-3)
+    token_heads = T_total * pw.H
+    alg_bytes = token_heads * BYTES_PER_TOKEN_HEAD + N * pw.H * pw.dk * pw.dv * 4
+    alg_flops = token_heads * FLOPS_PER_TOKEN_HEAD
+    p_gbs = alg_bytes / (p_mean * 1e-3) / 1e9
+    tc_tflops = alg_flops / (p_mean * 1e-3) / 1e12
+    dec_bytes = 2 * dw.N * dw.H * dw.dk * dw.dv * 4
+    d_gbs = dec_bytes / (d_mean * 1e-3) / 1e9
+    hbm_peak = float(peaks["hbm_gbs"])
+    tc_peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    prefill_src = source_hash("kda_prefill_simt.cu", "kda_internal.cuh")
+    decode_src = source_hash("kda_decode.cu", "kda_internal.cuh")
+    p_traffic = recorded_traffic("prefill", prefill_src)
+    d_traffic = recorded_traffic("decode", decode_src)
+
+    e2e = None
+    if not args.no_e2e:   # every rank: the timing is reduced over ranks
+        e2e = run_e2e(kda, q, k, v, g, b, cu, out, fin, args.e2e_steps, world, T_total)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, desc, nt = run_cpu_oracle_sample(args.cpu_seconds)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": nt, "kind": "oracle", "sample": desc}
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 (bf16 inputs, fp32 state and arithmetic)", "data": "synthetic",
+        "config": {
+            "workload": "varlen_bf16_H96_237568 prefill + decode_bf16_N256_H96 step",
+            "prefill_seqlens": list(pw.seqlens), "H": pw.H, "dk": pw.dk, "dv": pw.dv,
+            "decode_N": dw.N, "l2": "inputs larger than L2 (29 GB prefill inputs, 1.6 GB decode state); no flush",
+            "value_counts": "prefill launches only (decode reported under 'decode')",
+            "parallelism": f"replicas x{world}",
+        },
+        "prefill_ms": p_mean, "decode_ms": d_mean,
+        "roofline": {"kernel": "prefill_simt_kernel", "bound": "hbm", "achieved": p_gbs,
+                     "peak": hbm_peak, "unit": "GB/s", "frac": p_gbs / hbm_peak,
+                     "traffic": p_traffic, "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": alg_bytes},
+        "tensor": {"achieved_tflops": tc_tflops, "peak_tflops": tc_peak,
+                   "frac": tc_tflops / tc_peak, "algorithmic_flops_per_launch": alg_flops,
+                   "peak_source": peak_src + " (sustained bf16)"},
+        "decode": {"metric": "decode step state GB/s", "value": d_gbs, "unit": "GB/s",
+                   "ms": d_mean, "state_bytes_per_step": dec_bytes,
+                   "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": d_gbs,
+                                "peak": hbm_peak, "unit": "GB/s", "frac": d_gbs / hbm_peak,
+                                "traffic": d_traffic, "peak_source": peak_src}},
+        "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches,
+        "clocks": clocks, "wall_s_timed": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_e2e(kda, q, k, v, g, b, cu, out, fin, steps, world, T_total):
+    """Prefill through the public API from pinned host buffers."""
+    def pinned_copy(t):
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        return h
+
+    hq, hk, hv, hg, hb = (pinned_copy(t) for t in (q, k, v, g, b))
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    hfin = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for d, h in ((q, hq), (k, hk), (v, hv), (g, hg), (b, hb)):
+            d.copy_(h, non_blocking=True)
+        kda.kda_chunk_fwd(q, k, v, g, b, None, cu, out=out, final_state=fin)
+        hout.copy_(out, non_blocking=True)
+        hfin.copy_(fin, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = reduce_max(e0.elapsed_time(e1) / steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb))
+    d2h = hout.numel() * hout.element_size() + hfin.numel() * hfin.element_size()
+    return {"value": T_total * world / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,130 @@
+// Host side of the C ABI declared in include/kda.h: argument validation,
+// kernel selection and launch on the caller's stream.  Nothing here
+// allocates memory or synchronises.
+#include <atomic>
+#include <cstddef>
+#include <cstdint>
+
+#include "kda_internal.cuh"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+std::atomic<unsigned long long> g_launches{0};
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned_to(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool head_dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
+
+void resolve_params(const kda_params *p, float &g_min, const float *&A_log, float &scale) {
+    g_min = -5.0f;
+    A_log = nullptr;
+    scale = 1.0f;
+    if (p) {
+        if (p->g_min != 0.0f) g_min = p->g_min;
+        A_log = p->A_log;
+        if (p->scale != 0.0f) scale = p->scale;
+    }
+}
+
+kda_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return KDA_OK;
+    g_last_cuda_error = static_cast<int>(e);
+    return KDA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+namespace kda {
+void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace kda
+
+extern "C" {
+
+const char *kda_status_str(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_ARG: return "invalid argument (null pointer, negative size or inconsistent N/B)";
+        case KDA_ERR_DTYPE: return "unsupported dtype";
+        case KDA_ERR_SHAPE: return "unsupported head dimension (dk and dv must be 32, 64 or 128)";
+        case KDA_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case KDA_ERR_LAUNCH: return "CUDA launch failed";
+        case KDA_ERR_TIMEOUT: return "a bounded device wait timed out";
+    }
+    return "unknown status";
+}
+
+int kda_last_cuda_error(void) { return g_last_cuda_error; }
+
+int kda_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+unsigned long long kda_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+kda_status kda_chunk_fwd(kda_dtype dt, int B, int T, int H, int dk, int dv,
+                         const void *q, const void *k, const void *v,
+                         const void *g_raw, const void *beta,
+                         const float *init_state,
+                         const int32_t *cu_seqlens, int N,
+                         void *out, float *final_state,
+                         const kda_params *p, kda_stream_t stream) {
+    if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_DTYPE;
+    if (B < 0 || T < 0 || H <= 0 || N < 0) return KDA_ERR_ARG;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return KDA_ERR_SHAPE;
+    if (cu_seqlens) {
+        if (B != 1 || N < 1) return KDA_ERR_ARG;
+    } else if (N != B) {
+        return KDA_ERR_ARG;
+    }
+    const long long total = static_cast<long long>(B) * T;
+    if (total > INT32_MAX || static_cast<long long>(N) * H > INT32_MAX) return KDA_ERR_ARG;
+    if (total > 0 && (!q || !k || !v || !g_raw || !beta || !out)) return KDA_ERR_ARG;
+    const void *ptrs[] = {q, k, v, g_raw, init_state, out, final_state};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return KDA_ERR_ALIGN;
+    if (!aligned_to(beta, dt == KDA_F32 ? 4 : 2) || !aligned_to(cu_seqlens, 4)) return KDA_ERR_ALIGN;
+    if (N == 0 || (total == 0 && !final_state)) return KDA_OK;  // nothing to compute
+
+    kda::PrefillArgs a;
+    a.q = q; a.k = k; a.v = v; a.g = g_raw; a.beta = beta;
+    a.init_state = init_state;
+    a.cu_seqlens = cu_seqlens;
+    a.out = out;
+    a.final_state = final_state;
+    resolve_params(p, a.g_min, a.A_log, a.scale);
+    if (a.A_log && !aligned_to(a.A_log, 4)) return KDA_ERR_ALIGN;
+    a.N = N;
+    a.H = H;
+    a.T_total = static_cast<int>(total);
+    a.T_seq = T;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return from_cuda(kda::launch_prefill_simt(dt, dk, dv, a, s));
+}
+
+kda_status kda_decode_step(kda_dtype dt, int N, int H, int dk, int dv,
+                           const void *q, const void *k, const void *v,
+                           const void *g_raw, const void *beta,
+                           float *state, void *out,
+                           const kda_params *p, kda_stream_t stream) {
+    if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_DTYPE;
+    if (N < 0 || H <= 0) return KDA_ERR_ARG;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return KDA_ERR_SHAPE;
+    if (static_cast<long long>(N) * H > INT32_MAX) return KDA_ERR_ARG;
+    if (N == 0) return KDA_OK;
+    if (!q || !k || !v || !g_raw || !beta || !state || !out) return KDA_ERR_ARG;
+    const void *ptrs[] = {q, k, v, g_raw, state, out};
+    for (const void *ptr : ptrs)
+        if (!aligned16(ptr)) return KDA_ERR_ALIGN;
+    if (!aligned_to(beta, dt == KDA_F32 ? 4 : 2)) return KDA_ERR_ALIGN;
+    kda::DecodeArgs a;
+    a.q = q; a.k = k; a.v = v; a.g = g_raw; a.beta = beta;
+    a.state = state;
+    a.out = out;
+    resolve_params(p, a.g_min, a.A_log, a.scale);
+    if (a.A_log && !aligned_to(a.A_log, 4)) return KDA_ERR_ALIGN;
+    a.N = N;
+    a.H = H;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return from_cuda(kda::launch_decode(dt, dk, dv, a, s));
+}
+
+}  // extern "C"

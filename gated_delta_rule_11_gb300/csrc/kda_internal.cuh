@@ -1,0 +1,76 @@
+// Internal declarations shared by the libkda translation units.
+// Not part of the public ABI (that is include/kda.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// Per-launch arguments of the prefill kernels.  Token-major packed layout:
+// q, k, g_raw [T_total, H, dk]; v, out [T_total, H, dv]; beta [T_total, H];
+// states [N, H, dk, dv] fp32.
+struct PrefillArgs {
+    const void *q, *k, *v, *g, *beta;
+    const float *init_state;
+    const int32_t *cu_seqlens;  // device [N+1] or nullptr (then fixed length T_seq)
+    void *out;
+    float *final_state;
+    const float *A_log;         // device [H] or nullptr
+    int N, H, T_total, T_seq;
+    float g_min, scale;
+};
+
+struct DecodeArgs {
+    const void *q, *k, *v, *g, *beta;
+    float *state;
+    void *out;
+    const float *A_log;
+    int N, H;
+    float g_min, scale;
+};
+
+// Element loads/stores in the caller's dtype, computed in fp32.
+template <typename T> __device__ __forceinline__ float ld_in(const T *p);
+template <> __device__ __forceinline__ float ld_in<float>(const float *p) { return __ldg(p); }
+template <> __device__ __forceinline__ float ld_in<__nv_bfloat16>(const __nv_bfloat16 *p) {
+    return __bfloat162float(__ldg(p));
+}
+template <typename T> __device__ __forceinline__ void st_out(T *p, float x);
+template <> __device__ __forceinline__ void st_out<float>(float *p, float x) { *p = x; }
+template <> __device__ __forceinline__ void st_out<__nv_bfloat16>(__nv_bfloat16 *p, float x) {
+    *p = __float2bfloat16_rn(x);
+}
+
+// Bounded log-decay, "Kimi K3：从三条信息流到完整系统" §下界 log-decay 是一个
+// kernel 设计, eq. (5): g = g_min * sigmoid(e^A z); escale = e^A.
+__device__ __forceinline__ float log_decay(float z, float escale, float g_min) {
+    return g_min / (1.0f + expf(-escale * z));
+}
+
+// Sequence span [bos, eos) of sequence n, clamped into [0, T_total].
+__device__ __forceinline__ void seq_span(const PrefillArgs &a, int n, int &bos, int &eos) {
+    if (a.cu_seqlens) {
+        int b0 = a.cu_seqlens[n], e0 = a.cu_seqlens[n + 1];
+        b0 = min(max(b0, 0), a.T_total);
+        e0 = min(max(e0, b0), a.T_total);
+        bos = b0;
+        eos = e0;
+    } else {
+        bos = n * a.T_seq;
+        eos = bos + a.T_seq;
+    }
+}
+
+// Record n successfully enqueued kernels (backs kda_launch_count).
+void count_launches(unsigned n);
+
+// Launchers (return a cudaError_t from the launch).
+cudaError_t launch_decode(kda_dtype dt, int dk, int dv, const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_prefill_simt(kda_dtype dt, int dk, int dv, const PrefillArgs &a,
+                                cudaStream_t s);
+
+}  // namespace kda

@@ -1,0 +1,202 @@
+"""Thin Python binding of libkda (include/kda.h) over ctypes.
+
+Argument marshalling only: tensors are checked for device, dtype, shape and
+contiguity, their device pointers and the current CUDA stream are passed to
+the C ABI, and a non-OK status raises ``KdaError``.  All arithmetic runs in
+the library's CUDA kernels; there is no fallback.  PyTorch provides device
+memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+KDA_F32, KDA_BF16 = 0, 1
+_STATUS = {0: "KDA_OK", 1: "KDA_ERR_ARG", 2: "KDA_ERR_DTYPE", 3: "KDA_ERR_SHAPE",
+           4: "KDA_ERR_ALIGN", 5: "KDA_ERR_LAUNCH", 6: "KDA_ERR_TIMEOUT"}
+
+_lib = None
+_lock = threading.Lock()
+
+EXPORTED = ("kda_chunk_fwd", "kda_decode_step", "kda_status_str", "kda_last_cuda_error",
+            "kda_version", "kda_launch_count")
+
+
+class KdaError(RuntimeError):
+    def __init__(self, fn, status, detail=""):
+        self.status = status
+        self.status_name = _STATUS.get(status, str(status))
+        super().__init__(f"{fn} returned {self.status_name}: {detail}")
+
+
+class KdaParams(ctypes.Structure):
+    _fields_ = [("g_min", ctypes.c_float), ("A_log", ctypes.c_void_p), ("scale", ctypes.c_float)]
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(build_if_missing: bool = False):
+    """Load libkda.so (raises if it is missing and building is not requested)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(
+                    f"libkda.so not found at {path}: build it first "
+                    "(python -m gated_delta_rule_11_gb300.build)")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        vp, i = ctypes.c_void_p, ctypes.c_int
+        lib.kda_chunk_fwd.restype = i
+        lib.kda_chunk_fwd.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, i, vp, vp,
+                                      ctypes.POINTER(KdaParams), vp]
+        lib.kda_decode_step.restype = i
+        lib.kda_decode_step.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp,
+                                        ctypes.POINTER(KdaParams), vp]
+        lib.kda_status_str.restype = ctypes.c_char_p
+        lib.kda_status_str.argtypes = [i]
+        lib.kda_last_cuda_error.restype = i
+        lib.kda_last_cuda_error.argtypes = []
+        lib.kda_version.restype = i
+        lib.kda_version.argtypes = []
+        lib.kda_launch_count.restype = ctypes.c_ulonglong
+        lib.kda_launch_count.argtypes = []
+        _lib = lib
+        return lib
+
+
+def launch_count() -> int:
+    """Kernels enqueued by libkda in this process so far."""
+    return int(load_library().kda_launch_count())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return KDA_F32
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    raise TypeError(f"KDA inputs must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t, name, shape, dtype, device):
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _params(g_min, A_log, scale):
+    return KdaParams(float(g_min or 0.0), None if A_log is None else A_log.data_ptr(),
+                     float(scale or 0.0))
+
+
+def _stream_handle(device, stream):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _raise(lib, fn, st):
+    detail = lib.kda_status_str(st).decode()
+    if st == 5:
+        detail += f" (cudaError {lib.kda_last_cuda_error()})"
+    raise KdaError(fn, st, detail)
+
+
+def kda_chunk_fwd(q, k, v, g_raw, beta, init_state=None, cu_seqlens=None, *,
+                  out=None, final_state=None, output_final_state: bool = True,
+                  g_min: float = -5.0, A_log=None, scale: float = 1.0, stream=None):
+    """KDA forward over whole sequences (prefill).
+
+    q, k, g_raw [B, T, H, dk]; v [B, T, H, dv]; beta [B, T, H] (all float32 or
+    all bfloat16, on one CUDA device); init_state [N, H, dk, dv] float32 or
+    None; cu_seqlens int32 [N+1] on the device (then B == 1) or None.
+    Returns (out [B, T, H, dv], final_state [N, H, dk, dv] float32 or None).
+    """
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("kda_chunk_fwd runs on CUDA tensors only")
+    dt = q.dtype
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    for name, t, shp in (("q", q, (B, T, H, dk)), ("k", k, (B, T, H, dk)),
+                         ("g_raw", g_raw, (B, T, H, dk)), ("v", v, (B, T, H, dv)),
+                         ("beta", beta, (B, T, H))):
+        _check(t, name, shp, dt, dev)
+    if cu_seqlens is not None:
+        if cu_seqlens.dtype != torch.int32 or cu_seqlens.device != dev or cu_seqlens.dim() != 1:
+            raise ValueError("cu_seqlens must be a 1-D int32 tensor on the inputs' device")
+        if B != 1:
+            raise ValueError("packed sequences (cu_seqlens) require B == 1")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    if init_state is not None:
+        _check(init_state, "init_state", (N, H, dk, dv), torch.float32, dev)
+    if A_log is not None:
+        _check(A_log, "A_log", (H,), torch.float32, dev)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=dt, device=dev)
+    else:
+        _check(out, "out", (B, T, H, dv), dt, dev)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    elif final_state is not None:
+        _check(final_state, "final_state", (N, H, dk, dv), torch.float32, dev)
+    prm = _params(g_min, A_log, scale)
+    st = lib.kda_chunk_fwd(_dtype_code(q), B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v),
+                           _ptr(g_raw), _ptr(beta), _ptr(init_state), _ptr(cu_seqlens), N,
+                           _ptr(out), _ptr(final_state), ctypes.byref(prm),
+                           _stream_handle(dev, stream))
+    if st != 0:
+        _raise(lib, "kda_chunk_fwd", st)
+    return out, final_state
+
+
+def kda_decode_step(q, k, v, g_raw, beta, state, *, out=None, g_min: float = -5.0,
+                    A_log=None, scale: float = 1.0, stream=None):
+    """Advance N sequences by one token; ``state`` [N, H, dk, dv] float32 is
+    updated in place.  q, k, g_raw [N, H, dk]; v [N, H, dv]; beta [N, H].
+    Returns out [N, H, dv]."""
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("kda_decode_step runs on CUDA tensors only")
+    dt = q.dtype
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    for name, t, shp in (("q", q, (N, H, dk)), ("k", k, (N, H, dk)), ("g_raw", g_raw, (N, H, dk)),
+                         ("v", v, (N, H, dv)), ("beta", beta, (N, H))):
+        _check(t, name, shp, dt, dev)
+    _check(state, "state", (N, H, dk, dv), torch.float32, dev)
+    if A_log is not None:
+        _check(A_log, "A_log", (H,), torch.float32, dev)
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=dt, device=dev)
+    else:
+        _check(out, "out", (N, H, dv), dt, dev)
+    prm = _params(g_min, A_log, scale)
+    st = lib.kda_decode_step(_dtype_code(q), N, H, dk, dv, _ptr(q), _ptr(k), _ptr(v),
+                             _ptr(g_raw), _ptr(beta), _ptr(state), _ptr(out),
+                             ctypes.byref(prm), _stream_handle(dev, stream))
+    if st != 0:
+        _raise(lib, "kda_decode_step", st)
+    return out

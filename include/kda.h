@@ -1,0 +1,146 @@
+/*
+ * kda.h -- C ABI of libkda, a GB300 (sm_103a) implementation of the Kimi
+ * Delta Attention (KDA) operator.
+ *
+ * Operation (from "Kimi K3：从三条信息流到完整系统", wineandchord.com):
+ *   §KDA 是带逐通道遗忘的 delta rule, eq. (1), per sequence and head:
+ *       S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *       o_t = scale * S_t^T q_t
+ *     S is dk x dv; Diag(alpha_t) scales the key-channel rows of S; o_t reads
+ *     the state after token t's own write.
+ *   §下界 log-decay 是一个 kernel 设计, eq. (5):
+ *       g_t = g_min * Sigmoid(e^A * z_t),  alpha_t = e^{g_t},  g_min = -5
+ *     where z_t (per key channel) is the caller's gate pre-activation g_raw.
+ *   §从投影到 Chunkwise 的完整接口, eqs. (3)-(4): the chunkwise form that the
+ *     prefill kernels evaluate (16-token tiles, exact in real arithmetic).
+ *
+ * Conventions for every entry point:
+ *   - All tensor arguments are DEVICE pointers owned by the caller; the
+ *     library allocates no device or host memory and keeps no pointer after
+ *     the call returns.
+ *   - Every call is asynchronous on the given stream (0 = legacy default
+ *     stream).  A KDA_OK return means the work was validated and enqueued.
+ *   - Tensors are dense and row-major ("contiguous") in the stated shape.
+ *   - Alignment (KDA_ERR_ALIGN otherwise): q, k, v, g_raw, out and the
+ *     state tensors 16 bytes (they are moved by TMA / vector loads); beta
+ *     and A_log to their element size; cu_seqlens to 4 bytes.
+ *   - Arguments are validated on the host before any launch; a rejected
+ *     call enqueues nothing and leaves every output untouched.  No call
+ *     aborts, traps on the device or throws across this boundary.
+ *   - Outputs must not alias inputs, except decode's state (in place).
+ *   - Head dimensions dk, dv must each be 32, 64 or 128.
+ *   - The query scale defaults to 1 (the pages apply none).
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque stream handle: a cudaStream_t passes through unchanged. */
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_ARG = 1,     /* NULL required pointer, negative size, bad N/B   */
+    KDA_ERR_DTYPE = 2,   /* unknown kda_dtype                                */
+    KDA_ERR_SHAPE = 3,   /* unsupported dk/dv                                */
+    KDA_ERR_ALIGN = 4,   /* pointer not 16-byte aligned                      */
+    KDA_ERR_LAUNCH = 5,  /* CUDA rejected the launch (see kda_last_cuda_error) */
+    KDA_ERR_TIMEOUT = 6  /* reserved: a bounded device wait gave up          */
+} kda_status;
+
+typedef enum {
+    KDA_F32 = 0,         /* q, k, v, g_raw, beta, out in fp32                 */
+    KDA_BF16 = 1         /* q, k, v, g_raw, beta, out in bf16                 */
+} kda_dtype;
+
+/*
+ * Optional parameters.  A zero-initialised struct (or a NULL pointer)
+ * selects the pages' defaults.
+ *   g_min : floor of the log-decay in eq. (5); 0 selects -5.
+ *   A_log : DEVICE pointer to H fp32 values, the per-head log-scale A of
+ *           eq. (5) (the logit is multiplied by e^A); NULL selects A = 0.
+ *   scale : factor applied to o_t; 0 selects 1.
+ */
+typedef struct {
+    float g_min;
+    const float *A_log;
+    float scale;
+} kda_params;
+
+/*
+ * kda_chunk_fwd -- prefill / forward over whole sequences.
+ *
+ * Inputs (dtype dt unless stated):
+ *   q, k   [B, T, H, dk]   queries and keys, used as given (already
+ *                          normalised by the caller's projection chain).
+ *   v      [B, T, H, dv]   values.
+ *   g_raw  [B, T, H, dk]   gate pre-activation z of eq. (5).
+ *   beta   [B, T, H]       write strength, already in (0, 1).
+ *   init_state [N, H, dk, dv] fp32, or NULL for zeros: the state entering
+ *                          each sequence (row = key channel).
+ *   cu_seqlens [N + 1] int32 DEVICE array, or NULL.
+ *          NULL : the B rows are N = B independent sequences of length T.
+ *          set  : B must be 1; the T tokens are N packed sequences, sequence
+ *                 n spanning tokens [cu_seqlens[n], cu_seqlens[n+1]).  The
+ *                 array must start at 0, be non-decreasing and end at T.
+ *                 The kernels clamp each span into [0, T], so a malformed
+ *                 array yields unspecified values but never an
+ *                 out-of-bounds access.  Empty sequences are allowed: their
+ *                 final state equals their initial state.
+ *   N      number of sequences (must equal B when cu_seqlens is NULL).
+ * Outputs:
+ *   out    [B, T, H, dv]   o_t for every token (dtype dt); required if B*T > 0.
+ *   final_state [N, H, dk, dv] fp32, or NULL: the state after each
+ *          sequence's last token.
+ * Numerics: fp32 state and accumulation.  The bf16 path feeds bf16
+ * operands (inputs and a bf16 copy of the state) to the tensor cores; the
+ * fp32 path computes in fp32 throughout.
+ */
+kda_status kda_chunk_fwd(kda_dtype dt, int B, int T, int H, int dk, int dv,
+                         const void *q, const void *k, const void *v,
+                         const void *g_raw, const void *beta,
+                         const float *init_state,
+                         const int32_t *cu_seqlens, int N,
+                         void *out, float *final_state,
+                         const kda_params *p, kda_stream_t stream);
+
+/*
+ * kda_decode_step -- advance N independent sequences by one token each.
+ *
+ * Inputs (dtype dt): q, k, g_raw [N, H, dk]; v [N, H, dv]; beta [N, H].
+ * In/out: state [N, H, dk, dv] fp32, read and overwritten in place with the
+ *         state after this token.
+ * Output: out [N, H, dv] (dtype dt), o = scale * S_new^T q.
+ * Each (sequence, head) state is read once and written once.
+ */
+kda_status kda_decode_step(kda_dtype dt, int N, int H, int dk, int dv,
+                           const void *q, const void *k, const void *v,
+                           const void *g_raw, const void *beta,
+                           float *state, void *out,
+                           const kda_params *p, kda_stream_t stream);
+
+/* Static string for a status code (never NULL). */
+const char *kda_status_str(kda_status s);
+
+/* The CUDA error code (cudaError_t value) behind the last KDA_ERR_LAUNCH
+ * returned on the calling host thread, or 0. */
+int kda_last_cuda_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int kda_version(void);
+
+/* Number of CUDA kernels this library has enqueued in this process so far
+ * (all entry points, all threads).  Lets a caller count launches over a
+ * region of its own code. */
+unsigned long long kda_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

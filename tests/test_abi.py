@@ -1,0 +1,86 @@
+"""The C-ABI library builds, loads and exports what include/kda.h declares;
+host-side validation rejects bad arguments before touching the GPU.
+(No compute call here: these run without a GPU.)"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_delta_rule_11_gb300 import build as kbuild
+from gated_delta_rule_11_gb300 import kda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kda.load_library()
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^[ \t]*(?:[A-Za-z_]\w*[ \t*]+)+(kda_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for fn in ("kda_chunk_fwd", "kda_decode_step", "kda_status_str"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for fn in declared_functions():
+        assert hasattr(lib, fn), f"libkda.so does not export {fn}"
+    assert set(kda.EXPORTED) <= set(declared_functions())
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = lib.kda_status_str(code)
+        assert s and len(s) > 1
+    assert lib.kda_status_str(99) == b"unknown status"
+    assert lib.kda_version() >= 10000
+
+
+def _fwd(lib, dt=1, B=1, T=16, H=1, dk=128, dv=128, ptr=4096, init=None, cu=None, N=1,
+         out=4096, fin=None):
+    p = ctypes.c_void_p(ptr)
+    return lib.kda_chunk_fwd(dt, B, T, H, dk, dv, p, p, p, p, p, init, cu, N,
+                             ctypes.c_void_p(out) if out else None, fin, None, None)
+
+
+def test_validation_rejects_before_launch(lib):
+    # Every case fails validation, so no pointer is dereferenced and no CUDA call is made.
+    assert _fwd(lib, dt=7) == 2                      # dtype
+    assert _fwd(lib, dk=48) == 3                     # head dimension
+    assert _fwd(lib, dv=256) == 3
+    assert _fwd(lib, B=-1) == 1
+    assert _fwd(lib, H=0) == 1
+    assert _fwd(lib, N=2) == 1                       # N must equal B without cu_seqlens
+    assert _fwd(lib, ptr=4100) == 4                  # misaligned
+    assert _fwd(lib, out=0) == 1                     # missing output
+    assert _fwd(lib, B=2, cu=ctypes.c_void_p(4096), N=2) == 1   # packed needs B == 1
+    assert _fwd(lib, B=0, T=16, N=0) == 0            # empty batch: nothing to do
+    p = ctypes.c_void_p(4096)
+    assert lib.kda_decode_step(1, 4, 2, 128, 100, p, p, p, p, p, p, p, None, None) == 3
+    assert lib.kda_decode_step(1, 4, 2, 128, 128, p, p, p, p, p, None, p, None, None) == 1
+    assert lib.kda_decode_step(1, 4, 2, 128, 128, p, p, p, p, ctypes.c_void_p(4097), p, p,
+                               None, None) == 4           # bf16 beta needs 2-byte alignment
+    assert lib.kda_decode_step(1, 4, 2, 128, 128, p, p, p, p, p, ctypes.c_void_p(4104), p,
+                               None, None) == 4           # state needs 16 bytes
+    assert lib.kda_decode_step(1, 0, 2, 128, 128, None, None, None, None, None, None, None,
+                               None, None) == 0
+
+
+def test_python_binding_refuses_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(1, 16, 1, 32)
+    with pytest.raises(ValueError):
+        kda.kda_chunk_fwd(x, x, x, x, torch.zeros(1, 16, 1))
