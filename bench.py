@@ -341,7 +341,9 @@ def run_ours(args, rank, world, local):
     d_gbs = dec_bytes / (d_mean * 1e-3) / 1e9
     hbm_peak = float(peaks["hbm_gbs"])
     tc_peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
-    prefill_src = source_hash("kda_prefill_simt.cu", "kda_internal.cuh")
+    kernel_name = kda.chunk_fwd_kernel(torch.bfloat16, pw.dk, pw.dv)
+    prefill_src = source_hash("kda_prefill_tc.cu" if kernel_name == "prefill_tc_kernel"
+                              else "kda_prefill_simt.cu", "kda_internal.cuh", "kda_sm100.cuh")
     decode_src = source_hash("kda_decode.cu", "kda_internal.cuh")
     p_traffic = recorded_traffic("prefill", prefill_src)
     d_traffic = recorded_traffic("decode", decode_src)
@@ -361,7 +363,9 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32 (bf16 inputs, fp32 state and arithmetic)", "data": "synthetic",
+        "dtype": ("f16 tensor-core operands (bf16 inputs; fp32 state, gates and accumulation)"
+                  if kernel_name == "prefill_tc_kernel" else "f32 (bf16 inputs)"),
+        "data": "synthetic",
         "config": {
             "workload": "varlen_bf16_H96_237568 prefill + decode_bf16_N256_H96 step",
             "prefill_seqlens": list(pw.seqlens), "H": pw.H, "dk": pw.dk, "dv": pw.dv,
@@ -370,7 +374,7 @@ def run_ours(args, rank, world, local):
             "parallelism": f"replicas x{world}",
         },
         "prefill_ms": p_mean, "decode_ms": d_mean,
-        "roofline": {"kernel": "prefill_simt_kernel", "bound": "hbm", "achieved": p_gbs,
+        "roofline": {"kernel": kernel_name, "bound": "hbm", "achieved": p_gbs,
                      "peak": hbm_peak, "unit": "GB/s", "frac": p_gbs / hbm_peak,
                      "traffic": p_traffic, "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": alg_bytes},

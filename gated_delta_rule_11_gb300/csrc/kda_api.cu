@@ -56,9 +56,23 @@ const char *kda_status_str(kda_status s) {
 
 int kda_last_cuda_error(void) { return g_last_cuda_error; }
 
+const char *kda_chunk_fwd_kernel(kda_dtype dt, int dk, int dv) {
+    if ((dt != KDA_F32 && dt != KDA_BF16) || !head_dim_ok(dk) || !head_dim_ok(dv)) return nullptr;
+    return kda::prefill_tc_supported(dt, dk, dv) ? "prefill_tc_kernel" : "prefill_simt_kernel";
+}
+
 int kda_version(void) { return 1 * 10000 + 0 * 100 + 0; }
 
 unsigned long long kda_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+kda_status kda_check_device_status(void) {
+    const cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        g_last_cuda_error = static_cast<int>(e);
+        return KDA_ERR_LAUNCH;
+    }
+    return kda::take_tc_timeouts() ? KDA_ERR_TIMEOUT : KDA_OK;
+}
 
 kda_status kda_chunk_fwd(kda_dtype dt, int B, int T, int H, int dk, int dv,
                          const void *q, const void *k, const void *v,
@@ -97,6 +111,8 @@ kda_status kda_chunk_fwd(kda_dtype dt, int B, int T, int H, int dk, int dv,
     a.T_total = static_cast<int>(total);
     a.T_seq = T;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (kda::prefill_tc_supported(dt, dk, dv) && a.T_total > 0)
+        return from_cuda(kda::launch_prefill_tc(a, s));
     return from_cuda(kda::launch_prefill_simt(dt, dk, dv, a, s));
 }
 

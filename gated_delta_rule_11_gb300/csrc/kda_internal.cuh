@@ -51,6 +51,12 @@ __device__ __forceinline__ float log_decay(float z, float escale, float g_min) {
     return g_min / (1.0f + expf(-escale * z));
 }
 
+// The same gate with hardware exponential and reciprocal (relative error
+// ~1e-6, far below the tensor-core paths' operand rounding).
+__device__ __forceinline__ float log_decay_fast(float z, float escale, float g_min) {
+    return g_min * __frcp_rn(1.0f + __expf(-escale * z));
+}
+
 // Sequence span [bos, eos) of sequence n, clamped into [0, T_total].
 __device__ __forceinline__ void seq_span(const PrefillArgs &a, int n, int &bos, int &eos) {
     if (a.cu_seqlens) {
@@ -72,5 +78,11 @@ void count_launches(unsigned n);
 cudaError_t launch_decode(kda_dtype dt, int dk, int dv, const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_prefill_simt(kda_dtype dt, int dk, int dv, const PrefillArgs &a,
                                 cudaStream_t s);
+
+// Tensor-core prefill (bf16, dk = dv = 128).
+bool prefill_tc_supported(kda_dtype dt, int dk, int dv);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
+// Number of bounded device waits that gave up since the last call (syncs the device).
+unsigned int take_tc_timeouts();
 
 }  // namespace kda

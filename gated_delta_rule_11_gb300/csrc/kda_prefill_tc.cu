@@ -1,0 +1,519 @@
+// Chunked KDA prefill on the 5th-generation tensor cores (tcgen05 + TMEM,
+// TMA-fed): bf16 inputs, fp32 state, dk = dv = 128.
+//
+// Method ("Kimi K3：从三条信息流到完整系统"): the recurrence of §KDA 是带逐通道
+// 遗忘的 delta rule, eq. (1), evaluated in the chunkwise form of
+// §从投影到 Chunkwise 的完整接口, eqs. (3)-(4), over 16-token tiles -- the
+// tile whose cumulative log-decay §下界 log-decay 是一个 kernel 设计 bounds to
+// (-80, 0), so e^{-b} stays finite and the in-tile products are dense
+// matmuls.  With b_r the in-tile inclusive cumsum of g, S_0 the state
+// entering the tile, and the UT transform written out:
+//   L  = StrictTril[(K e^b)(K e^-b)^T],   A = Tril[(Q e^b)(K e^-b)^T]
+//   T  = (I + Diag(beta) L)^-1,  U = T Diag(beta) V,  W = T Diag(beta) (K e^b)
+//   Vt = U - W S_0
+//   O  = scale * ((Q e^b) S_0 + A Vt)
+//   S  = Diag(e^{b_C}) S_0 + (K e^{b_C - b})^T Vt
+//
+// Precision.  Vt is the delta-rule residual (about |v|, while S is about
+// 0.1-0.5), and rounding it, or A, to bf16 alone costs ~2e-2 of the output
+// RMS.  So the tensor-core operands are fp16 (11-bit significand; every one
+// of S, W, Q e^b, Vt, A, K e^{b_C-b} is bounded well inside fp16's range),
+// L and A come from tf32 mma.sync on fp32 operands (K e^-b reaches e^80, out
+// of fp16 range), and U, W, T, the gates and the state master are fp32.
+//
+// Every tensor-core product is computed transposed so that its M side is a
+// 128-wide head dimension (tcgen05 M = 128, TMEM lane j = value channel j):
+//   (e) D[:, 0:32]   = S^T [-W ; Q e^b]^T                M128 N32  K128
+//       -> D[:, 0:16] = -(W S_0)^T, D[:, 16:32] = ((Q e^b) S_0)^T
+//   (g) D[:, 16:32] += Vt^T A^T                          M128 N16  K16
+//       -> D[:, 16:32] = O^T / scale
+//   (h) D[:, 32:160] = Vt^T (K e^{b_C - b})              M128 N128 K16
+//       -> the state increment, transposed
+//
+// CTA roles (one CTA per (sequence, head) chain, 320 threads):
+//   warps 0-3  chain     : thread j owns column j of the fp32 state in
+//                          registers; per tile it forms Vt^T = U^T + D[:,0:16]
+//                          as the fp16 operand of (g)/(h), stores O, applies
+//                          S = Diag(e^{b_C}) S + increment, and writes the fp16
+//                          copy of S^T that the next tile's (e) reads.
+//   warps 4-7  producer  : thread c owns key channel c: gate (eq. 5),
+//                          cumulative decay, decay-scaled operands, L and A
+//                          (one 16x8 block per warp, mma.sync tf32), the
+//                          triangular solve (warp 4), W and U.
+//   warp 8     TMA       : loads the q, k, g_raw, v tiles (16 tokens each)
+//                          into a 3-stage ring.
+//   warp 9     MMA       : issues the tcgen05 products and commits.
+// The chain is serial per tile; the producer and TMA run up to 3 tiles ahead.
+// Tokens past a sequence's end are masked in the producer (k = q = 0, g = 0,
+// beta = 0), which makes U, W, A and the increment vanish for them.
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include "kda_internal.cuh"
+#include "kda_sm100.cuh"
+
+namespace kda {
+
+__device__ unsigned int g_tc_timeouts = 0;
+
+namespace {
+using namespace sm100;
+
+constexpr int D = 128;           // dk = dv
+constexpr int C = 16;            // tile tokens
+constexpr int NS = 3;            // ring stages
+constexpr int NTHREADS = 320;
+constexpr int TMEM_COLS = 256;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits: 1 s (legitimate ones take microseconds)
+constexpr int PADF = 132;        // fp32 row stride of the mma.sync operand tiles (conflict-free fragments)
+
+// ---- shared memory map (bytes from a 1024-aligned base); stage s at s * STAGE_BYTES
+constexpr int ST_Q = 0;          // [16][128] bf16 (TMA, unswizzled)
+constexpr int ST_K = 4096;
+constexpr int ST_Z = 8192;
+constexpr int ST_V = 12288;
+constexpr int ST_WQ = 16384;     // B of (e): fp16 K-major SW128, 32 rows x 128 (rows 0-15 -W, 16-31 Q e^b)
+constexpr int ST_KD = 24576;     // B of (h): fp16 MN-major SW128, mn = c, k = s
+constexpr int ST_AT = 28672;     // B of (g): fp16 K-major none, 16 rows x 16
+constexpr int ST_U = 29696;      // fp32 [16][128] U
+constexpr int ST_GC = 37888;     // fp32 [128] e^{b_C}
+constexpr int ST_BETA = 38400;   // fp32 [16]
+constexpr int STAGE_BYTES = 38912;
+constexpr int OFF_ST = NS * STAGE_BYTES;          // S^T fp16, K-major SW128, 128 x 128
+constexpr int OFF_VT = OFF_ST + 32768;            // Vt^T fp16, K-major none, 128 x 16
+constexpr int OFF_KGM = OFF_VT + 4096;            // fp32 [16][PADF]: K e^b   (tf32-rounded)
+constexpr int OFF_QGM = OFF_KGM + C * PADF * 4;   // fp32 [16][PADF]: Q e^b   (tf32-rounded)
+constexpr int OFF_KIM = OFF_QGM + C * PADF * 4;   // fp32 [16][PADF]: K e^-b  (tf32-rounded)
+constexpr int OFF_LS = OFF_KIM + C * PADF * 4;    // fp32 [16][17]: L
+constexpr int OFF_TBF = OFF_LS + C * 17 * 4;      // fp32 [16][16]: T Diag(beta)
+constexpr int OFF_BAR = (OFF_TBF + C * C * 4 + 63) & ~63;
+enum { B_RAW = 0, B_FULL = NS, B_EMPTY = 2 * NS, B_VT = 3 * NS, B_VTS, B_UPD, B_SRDY, NUM_BARS };
+constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
+constexpr int OFF_FLAG = OFF_SLOT + 4;
+constexpr int SMEM_USED = OFF_FLAG + 4;
+constexpr int SMEM_BYTES = SMEM_USED + 1024;      // + alignment slack
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+static_assert(STAGE_BYTES % 1024 == 0 && ST_WQ % 1024 == 0 && ST_KD % 1024 == 0 && OFF_ST % 1024 == 0,
+              "128B-swizzled operands need 1024-byte alignment");
+constexpr uint32_t TX_BYTES = 4 * C * D * 2;
+
+__device__ __forceinline__ float bf16_at(const uint8_t *p) {
+    return __bfloat162float(__ushort_as_bfloat16(*reinterpret_cast<const uint16_t *>(p)));
+}
+__device__ __forceinline__ void st_h(uint8_t *p, float x) {
+    *reinterpret_cast<uint16_t *>(p) = __half_as_ushort(__float2half_rn(x));
+}
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+__device__ __forceinline__ float to_tf32(float x) {
+    uint32_t u;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(u) : "f"(x));
+    return __uint_as_float(u);
+}
+// D (16x8 fp32) += A (16x8 tf32, row) * B (8x8 tf32, col)
+__device__ __forceinline__ void mma_1688_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void note_timeout(volatile int *flag) {
+    *flag = 1;
+    atomicAdd(&g_tc_timeouts, 1u);
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_v,
+                  PrefillArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + OFF_BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + OFF_SLOT);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base + OFF_FLAG);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int chain = blockIdx.x;
+    const int n = chain / a.H, h = chain % a.H;
+    int bos, eos;
+    seq_span(a, n, bos, eos);
+    const int ntiles = (eos - bos + C - 1) / C;
+    const size_t state_off = static_cast<size_t>(chain) * D * D;
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&bars[B_RAW + s], 1);
+            mbar_init(&bars[B_FULL + s], 128);
+            mbar_init(&bars[B_EMPTY + s], 2);
+        }
+        mbar_init(&bars[B_VT], 1);
+        mbar_init(&bars[B_VTS], 128);
+        mbar_init(&bars[B_UPD], 1);
+        mbar_init(&bars[B_SRDY], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, TMEM_COLS);
+    if (warp == 8 && lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_z);
+        prefetch_tmap(&tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 8) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0) {
+            for (int t = 0; t < ntiles; ++t) {
+                const int s = t % NS;
+                if (t >= NS && !mbar_wait(&bars[B_EMPTY + s], ((t / NS) - 1) & 1, kWaitLimitNs)) {
+                    note_timeout(abort_flag);
+                    break;
+                }
+                if (*abort_flag) break;
+                uint8_t *st = base + s * STAGE_BYTES;
+                const int tok = bos + t * C;
+                mbar_arrive_expect_tx(&bars[B_RAW + s], TX_BYTES);
+                tma_load_3d(st + ST_Q, &tm_q, &bars[B_RAW + s], 0, h, tok);
+                tma_load_3d(st + ST_K, &tm_k, &bars[B_RAW + s], 0, h, tok);
+                tma_load_3d(st + ST_Z, &tm_z, &bars[B_RAW + s], 0, h, tok);
+                tma_load_3d(st + ST_V, &tm_v, &bars[B_RAW + s], 0, h, tok);
+            }
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            constexpr uint32_t id_e = idesc_f16kind(kTypeF16, 128, 32, 0, 0);
+            constexpr uint32_t id_g = idesc_f16kind(kTypeF16, 128, 16, 0, 0);
+            constexpr uint32_t id_h = idesc_f16kind(kTypeF16, 128, 128, 0, 1);
+            const uint32_t sb = smem_u32(base);
+            const uint64_t d_vt = smem_desc(sb + OFF_VT, 128, 256, kLayoutNone);
+            for (int t = 0; t < ntiles; ++t) {
+                const int s = t % NS;
+                const uint32_t st = sb + s * STAGE_BYTES;
+                if (!mbar_wait(&bars[B_FULL + s], (t / NS) & 1, kWaitLimitNs) ||
+                    !mbar_wait(&bars[B_SRDY], t & 1, kWaitLimitNs)) {
+                    note_timeout(abort_flag);
+                    break;
+                }
+                if (*abort_flag) break;
+                tc_fence_after();
+                // (e) D[:,0:32] = S^T [-W ; Q e^b]^T, K = 128 in steps of 16
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int k = kk * 16;
+                    const uint32_t a_off = OFF_ST + (k >> 6) * (128 * 128) + (k & 63) * 2;
+                    const uint32_t b_off = ST_WQ + (k >> 6) * (32 * 128) + (k & 63) * 2;
+                    mma_f16kind(tmem, smem_desc(sb + a_off, 16, 1024, kLayoutSW128),
+                                smem_desc(st + b_off, 16, 1024, kLayoutSW128), id_e, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bars[B_VT]);
+                if (!mbar_wait(&bars[B_VTS], t & 1, kWaitLimitNs)) {
+                    note_timeout(abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                // (g) D[:,16:32] += Vt^T A^T
+                mma_f16kind(tmem + 16, d_vt, smem_desc(st + ST_AT, 128, 256, kLayoutNone), id_g, 1);
+                // (h) D[:,32:160] = Vt^T (K e^{b_C - b})
+                mma_f16kind(tmem + 32, d_vt, smem_desc(st + ST_KD, 2048, 1024, kLayoutSW128), id_h, 0);
+                mma_commit(&bars[B_UPD]);
+                mma_commit(&bars[B_EMPTY + s]);
+            }
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ producer
+        const int c = tid - 128;
+        const int pw = warp - 4;
+        const float escale = a.A_log ? expf(__ldg(a.A_log + h)) : 1.0f;
+        const __nv_bfloat16 *gbeta = static_cast<const __nv_bfloat16 *>(a.beta);
+        float *kgm = reinterpret_cast<float *>(base + OFF_KGM);
+        float *qgm = reinterpret_cast<float *>(base + OFF_QGM);
+        float *kim = reinterpret_cast<float *>(base + OFF_KIM);
+        float *ls = reinterpret_cast<float *>(base + OFF_LS);
+        float *tbf = reinterpret_cast<float *>(base + OFF_TBF);
+        // beta is a strided gather (one value per token): load it a tile ahead
+        // so its latency hides behind a tile of work.
+        auto load_beta = [&](int tt) {
+            const int tok = bos + tt * C + c;
+            return (c < C && tt < ntiles && tok < eos)
+                       ? __bfloat162float(gbeta[static_cast<size_t>(tok) * a.H + h]) : 0.f;
+        };
+        float bt_next = load_beta(0);
+        for (int t = 0; t < ntiles; ++t) {
+            const int s = t % NS;
+            uint8_t *st = base + s * STAGE_BYTES;
+            const int t0 = bos + t * C;
+            const int nv = min(C, eos - t0);
+            const float bt = bt_next;
+            bt_next = load_beta(t + 1);
+            if (!mbar_wait(&bars[B_RAW + s], (t / NS) & 1, kWaitLimitNs)) note_timeout(abort_flag);
+
+            float kr[C], qr[C], b[C];
+            float run = 0.f;
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                const float z = bf16_at(st + ST_Z + r * 256 + c * 2);
+                kr[r] = bf16_at(st + ST_K + r * 256 + c * 2);
+                qr[r] = bf16_at(st + ST_Q + r * 256 + c * 2);
+                if (r < nv) {
+                    run += log_decay_fast(z, escale, a.g_min);
+                } else {
+                    kr[r] = 0.f;
+                    qr[r] = 0.f;
+                }
+                b[r] = run;
+            }
+            const float gC = expf(run);
+            reinterpret_cast<float *>(st + ST_GC)[c] = gC;
+            if (c < C) reinterpret_cast<float *>(st + ST_BETA)[c] = bt;
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                const float e = __expf(b[r]);
+                const float ei = __frcp_rn(e);
+                const float kg = kr[r] * e;
+                const float qg = qr[r] * e;
+                st_h(st + ST_WQ + off_kmajor_sw128(16 + r, c, 32), qg);
+                qgm[r * PADF + c] = to_tf32(qg);
+                kgm[r * PADF + c] = to_tf32(kg);
+                kim[r * PADF + c] = to_tf32(kr[r] * ei);
+                st_h(st + ST_KD + off_mnmajor_sw128(c, r, C), kr[r] * (gC * ei));
+                b[r] = kg;  // keep K e^b (fp32) for W
+            }
+            if (named_bar_or(1, 128, *abort_flag != 0)) break;   // uniform across the warpgroup
+
+            {
+                // one 16x8 block per warp: pw 0/1 -> L columns 0-7/8-15, pw 2/3 -> A
+                const int g = lane >> 2, tq = lane & 3;
+                const float *lhs = pw < 2 ? kgm : qgm;
+                const int n0 = (pw & 1) * 8;
+                float d4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int k0 = 0; k0 < D; k0 += 8) {
+                    const uint32_t a0 = __float_as_uint(lhs[g * PADF + k0 + tq]);
+                    const uint32_t a1 = __float_as_uint(lhs[(g + 8) * PADF + k0 + tq]);
+                    const uint32_t a2 = __float_as_uint(lhs[g * PADF + k0 + tq + 4]);
+                    const uint32_t a3 = __float_as_uint(lhs[(g + 8) * PADF + k0 + tq + 4]);
+                    const uint32_t b0 = __float_as_uint(kim[(n0 + g) * PADF + k0 + tq]);
+                    const uint32_t b1 = __float_as_uint(kim[(n0 + g) * PADF + k0 + tq + 4]);
+                    mma_1688_tf32(d4, a0, a1, a2, a3, b0, b1);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int row = g + (e >> 1) * 8;
+                    const int col = n0 + 2 * tq + (e & 1);
+                    if (pw < 2)
+                        ls[row * 17 + col] = col < row ? d4[e] : 0.f;
+                    else
+                        st_h(st + ST_AT + off_kmajor_none(row, col, C), col <= row ? d4[e] : 0.f);
+                }
+            }
+            named_bar_sync(1, 128);
+            if (pw == 0 && lane < C) {
+                // T = (I + Diag(beta) L)^-1 by forward substitution; lane s owns column s.
+                const float *betas = reinterpret_cast<const float *>(st + ST_BETA);
+                float tcol[C];
+#pragma unroll
+                for (int r = 0; r < C; ++r) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int i = 0; i < r; ++i) acc += ls[r * 17 + i] * tcol[i];
+                    tcol[r] = (r == lane ? 1.f : 0.f) - betas[r] * acc;
+                }
+                const float bs = betas[lane];
+#pragma unroll
+                for (int r = 0; r < C; ++r) tbf[r * C + lane] = tcol[r] * bs;
+            }
+            named_bar_sync(1, 128);
+            // W = T Diag(beta) (K e^b) -> rows 0..15 of the (e) B operand hold -W;
+            // U = T Diag(beta) V (fp32) for the chain.
+            float *u = reinterpret_cast<float *>(st + ST_U);
+            float vc[C];
+#pragma unroll
+            for (int r = 0; r < C; ++r) vc[r] = bf16_at(st + ST_V + r * 256 + c * 2);
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                float tb[C];
+#pragma unroll
+                for (int q4 = 0; q4 < C / 4; ++q4) {
+                    const float4 t4 = *reinterpret_cast<const float4 *>(tbf + r * C + q4 * 4);
+                    tb[q4 * 4 + 0] = t4.x;
+                    tb[q4 * 4 + 1] = t4.y;
+                    tb[q4 * 4 + 2] = t4.z;
+                    tb[q4 * 4 + 3] = t4.w;
+                }
+                float w = 0.f, uu = 0.f;
+#pragma unroll
+                for (int s2 = 0; s2 <= r; ++s2) {
+                    w = fmaf(tb[s2], b[s2], w);
+                    uu = fmaf(tb[s2], vc[s2], uu);
+                }
+                st_h(st + ST_WQ + off_kmajor_sw128(r, c, 32), -w);
+                u[r * D + c] = uu;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars[B_FULL + s]);
+        }
+    } else {
+        // ------------------------------------------------------------ chain
+        const int j = tid;
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        float S[D];
+#pragma unroll
+        for (int cc = 0; cc < D; ++cc)
+            S[cc] = a.init_state ? a.init_state[state_off + static_cast<size_t>(cc) * D + j] : 0.f;
+        uint8_t *sT = base + OFF_ST;
+        auto write_sT = [&]() {
+#pragma unroll
+            for (int q8 = 0; q8 < D / 8; ++q8) {
+                uint4 v;
+                v.x = pack_h2(S[q8 * 8 + 0], S[q8 * 8 + 1]);
+                v.y = pack_h2(S[q8 * 8 + 2], S[q8 * 8 + 3]);
+                v.z = pack_h2(S[q8 * 8 + 4], S[q8 * 8 + 5]);
+                v.w = pack_h2(S[q8 * 8 + 6], S[q8 * 8 + 7]);
+                *reinterpret_cast<uint4 *>(sT + off_kmajor_sw128(j, q8 * 8, D)) = v;
+            }
+        };
+        write_sT();
+        fence_proxy_async_smem();
+        named_bar_sync(2, 128);
+        if (tid == 0) mbar_arrive(&bars[B_SRDY]);
+
+        __nv_bfloat16 *gout = static_cast<__nv_bfloat16 *>(a.out);
+        uint8_t *vt = base + OFF_VT;
+        for (int t = 0; t < ntiles; ++t) {
+            const int s = t % NS;
+            const uint8_t *st = base + s * STAGE_BYTES;
+            const int t0 = bos + t * C;
+            const int nv = min(C, eos - t0);
+            if (!mbar_wait(&bars[B_VT], t & 1, kWaitLimitNs)) note_timeout(abort_flag);
+            tc_fence_after();
+            {
+                float v[16];
+                tmem_ld16(tmem + lane_base, v);
+                const float *u = reinterpret_cast<const float *>(st + ST_U);
+                float uj[16];
+#pragma unroll
+                for (int r = 0; r < C; ++r) uj[r] = u[r * D + j];
+                tmem_ld_wait();
+                uint4 lo, hi;
+                lo.x = pack_h2(uj[0] + v[0], uj[1] + v[1]);
+                lo.y = pack_h2(uj[2] + v[2], uj[3] + v[3]);
+                lo.z = pack_h2(uj[4] + v[4], uj[5] + v[5]);
+                lo.w = pack_h2(uj[6] + v[6], uj[7] + v[7]);
+                hi.x = pack_h2(uj[8] + v[8], uj[9] + v[9]);
+                hi.y = pack_h2(uj[10] + v[10], uj[11] + v[11]);
+                hi.z = pack_h2(uj[12] + v[12], uj[13] + v[13]);
+                hi.w = pack_h2(uj[14] + v[14], uj[15] + v[15]);
+                *reinterpret_cast<uint4 *>(vt + off_kmajor_none(j, 0, C)) = lo;
+                *reinterpret_cast<uint4 *>(vt + off_kmajor_none(j, 8, C)) = hi;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bars[B_VTS]);
+            if (!mbar_wait(&bars[B_UPD], t & 1, kWaitLimitNs)) note_timeout(abort_flag);
+            tc_fence_after();
+            {
+                float o[16];
+                tmem_ld16(tmem + lane_base + 16, o);
+                tmem_ld_wait();
+                __nv_bfloat16 *op = gout + static_cast<size_t>(t0) * a.H * D + static_cast<size_t>(h) * D + j;
+#pragma unroll
+                for (int r = 0; r < C; ++r)
+                    if (r < nv) op[static_cast<size_t>(r) * a.H * D] = __float2bfloat16_rn(a.scale * o[r]);
+            }
+            const float *gc = reinterpret_cast<const float *>(st + ST_GC);
+#pragma unroll
+            for (int cb = 0; cb < D / 16; ++cb) {
+                float inc[16];
+                tmem_ld16(tmem + lane_base + 32 + cb * 16, inc);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) S[cb * 16 + i] = fmaf(gc[cb * 16 + i], S[cb * 16 + i], inc[i]);
+            }
+            write_sT();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            if (named_bar_or(2, 128, *abort_flag != 0)) break;   // uniform across the warpgroup
+            if (tid == 0) {
+                mbar_arrive(&bars[B_SRDY]);
+                mbar_arrive(&bars[B_EMPTY + s]);
+            }
+        }
+        if (a.final_state && !*abort_flag) {
+#pragma unroll
+            for (int cc = 0; cc < D; ++cc) a.final_state[state_off + static_cast<size_t>(cc) * D + j] = S[cc];
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// [T_total, H, 128] bf16 viewed as a 3-D tensor (d, head, token).
+bool make_map(CUtensorMap *m, const void *ptr, int H, int T_total, int box_d, bool swizzle128) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(T_total)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_d), 1, static_cast<cuuint32_t>(C)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool prefill_tc_supported(kda_dtype dt, int dk, int dv) { return dt == KDA_BF16 && dk == D && dv == D; }
+
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
+    CUtensorMap tq, tk, tz, tv;
+    if (!make_map(&tq, a.q, a.H, a.T_total, D, false) || !make_map(&tk, a.k, a.H, a.T_total, D, false) ||
+        !make_map(&tz, a.g, a.H, a.T_total, D, false) || !make_map(&tv, a.v, a.H, a.T_total, D, false))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(static_cast<unsigned>(a.N) * static_cast<unsigned>(a.H));
+    prefill_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, s>>>(tq, tk, tz, tv, a);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
+
+unsigned int take_tc_timeouts() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_tc_timeouts, sizeof(v)) != cudaSuccess) return 0;
+    cudaMemcpyToSymbol(g_tc_timeouts, &zero, sizeof(zero));
+    return v;
+}
+
+}  // namespace kda

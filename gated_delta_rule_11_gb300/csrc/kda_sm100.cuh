@@ -1,0 +1,199 @@
+// Thin inline-PTX wrappers for the sm_100-family features the tensor-core
+// prefill uses: mbarriers (every wait bounded), TMA tiled loads, tcgen05
+// tensor-memory allocation, MMA, commit and loads, and the shared-memory
+// matrix / instruction descriptors.  Library-internal.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+namespace kda {
+namespace sm100 {
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: gives up after `limit_ns` of wall time and returns false.
+// The caller records the failure and winds the kernel down.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// ---------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------- fences
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Barrier over `nthreads` threads that also returns the OR of `pred` over them,
+// so every participant takes the same branch afterwards.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n"
+        " selp.u32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
+// ---------------------------------------------------------------- TMEM
+// Executed by one full warp.  Writes the allocated base address to *slot.
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem], 16-bit inputs, fp32 accumulator.  One thread.
+__device__ __forceinline__ void mma_f16kind(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on *bar once every tcgen05 operation issued so far by this thread is complete.
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns: thread i of the warp gets lane
+// (warp's lane quarter base + i), columns [col, col + 16).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------- descriptors
+// Shared-memory matrix descriptor (tcgen05): start address, leading and
+// stride byte offsets (all >> 4), fixed 0b001 at bits 46-48, layout at 61-63.
+//   K-major, 128B swizzle : SBO = stride between 8-row groups (1024 for dense
+//                           atoms); LBO unused.  Advance K within a 64-element
+//                           swizzle row by adding bytes to the start address.
+//   MN-major, 128B swizzle: LBO = stride between 64-element MN chunks,
+//                           SBO = stride between 8-row K groups.
+//   no swizzle (K-major)  : LBO = stride between 8x8 core matrices along K,
+//                           SBO = stride between 8-row groups along M/N.
+enum : uint32_t { kLayoutNone = 0, kLayoutSW128 = 2 };
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(layout & 7u) << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 D (bits 4-5 = 1), A and B type at
+// bits 7-9 / 10-12 (F16 = 0, BF16 = 1; both operands of one MMA share a
+// type), K-major (0) or MN-major (1) operands at bits 15 / 16, N >> 3 at
+// bit 17, M >> 4 at bit 24.
+enum : uint32_t { kTypeF16 = 0, kTypeBF16 = 1 };
+__host__ __device__ constexpr uint32_t idesc_f16kind(uint32_t ab_type, int M, int N, int a_mn_major,
+                                                     int b_mn_major) {
+    return (1u << 4) | (ab_type << 7) | (ab_type << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |
+           (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Byte offset of element (row, k) of a 16-bit operand in the K-major 128B-swizzled
+// layout with R rows: 64-element K blocks of R*128 bytes, 8-row atoms of 1024 B.
+__host__ __device__ __forceinline__ uint32_t off_kmajor_sw128(int row, int k, int R) {
+    const uint32_t inrow = static_cast<uint32_t>((k & 63) * 2);
+    const uint32_t chunk = ((inrow >> 4) ^ static_cast<uint32_t>(row & 7));
+    return static_cast<uint32_t>((k >> 6) * (R * 128) + (row >> 3) * 1024 + (row & 7) * 128) + (chunk << 4) +
+           (inrow & 15u);
+}
+// Element (mn, k) of a 16-bit operand in the MN-major 128B-swizzled layout with
+// K extent Kx: 64-element MN chunks of (Kx/8)*1024 bytes, 8-row K atoms.
+__host__ __device__ __forceinline__ uint32_t off_mnmajor_sw128(int mn, int k, int Kx) {
+    const uint32_t inrow = static_cast<uint32_t>((mn & 63) * 2);
+    const uint32_t chunk = ((inrow >> 4) ^ static_cast<uint32_t>(k & 7));
+    return static_cast<uint32_t>((mn >> 6) * ((Kx >> 3) * 1024) + (k >> 3) * 1024 + (k & 7) * 128) +
+           (chunk << 4) + (inrow & 15u);
+}
+// Element (row, k) of a 16-bit operand in the K-major unswizzled layout with K
+// extent Kx: 8x8 core matrices of 128 B, LBO = 128 (along K), SBO = Kx*16.
+__host__ __device__ __forceinline__ uint32_t off_kmajor_none(int row, int k, int Kx) {
+    return static_cast<uint32_t>((row >> 3) * (Kx * 16) + (k >> 3) * 128 + (row & 7) * 16 + (k & 7) * 2);
+}
+
+}  // namespace sm100
+}  // namespace kda

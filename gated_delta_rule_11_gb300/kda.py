@@ -24,7 +24,7 @@ _lib = None
 _lock = threading.Lock()
 
 EXPORTED = ("kda_chunk_fwd", "kda_decode_step", "kda_status_str", "kda_last_cuda_error",
-            "kda_version", "kda_launch_count")
+            "kda_version", "kda_launch_count", "kda_check_device_status", "kda_chunk_fwd_kernel")
 
 
 class KdaError(RuntimeError):
@@ -71,6 +71,10 @@ def load_library(build_if_missing: bool = False):
         lib.kda_version.argtypes = []
         lib.kda_launch_count.restype = ctypes.c_ulonglong
         lib.kda_launch_count.argtypes = []
+        lib.kda_check_device_status.restype = i
+        lib.kda_check_device_status.argtypes = []
+        lib.kda_chunk_fwd_kernel.restype = ctypes.c_char_p
+        lib.kda_chunk_fwd_kernel.argtypes = [i, i, i]
         _lib = lib
         return lib
 
@@ -78,6 +82,21 @@ def load_library(build_if_missing: bool = False):
 def launch_count() -> int:
     """Kernels enqueued by libkda in this process so far."""
     return int(load_library().kda_launch_count())
+
+
+def chunk_fwd_kernel(dtype: torch.dtype, dk: int, dv: int):
+    """Name of the kernel kda_chunk_fwd uses for this dtype and head size."""
+    code = KDA_F32 if dtype == torch.float32 else KDA_BF16
+    r = load_library().kda_chunk_fwd_kernel(code, dk, dv)
+    return None if r is None else r.decode()
+
+
+def check_device_status() -> None:
+    """Synchronise and raise KdaError if a kernel gave up a bounded wait."""
+    lib = load_library()
+    st = lib.kda_check_device_status()
+    if st != 0:
+        _raise(lib, "kda_check_device_status", st)
 
 
 def _dtype_code(t: torch.Tensor) -> int:

@@ -124,6 +124,12 @@ kda_status kda_decode_step(kda_dtype dt, int N, int H, int dk, int dv,
                            float *state, void *out,
                            const kda_params *p, kda_stream_t stream);
 
+/* Name of the kernel kda_chunk_fwd launches for this dtype and head size
+ * ("prefill_tc_kernel": tcgen05 tensor cores, bf16 with dk = dv = 128;
+ * "prefill_simt_kernel": fp32 CUDA cores, every other supported case), or
+ * NULL for an unsupported combination. */
+const char *kda_chunk_fwd_kernel(kda_dtype dt, int dk, int dv);
+
 /* Static string for a status code (never NULL). */
 const char *kda_status_str(kda_status s);
 
@@ -133,6 +139,14 @@ int kda_last_cuda_error(void);
 
 /* Library version as major*10000 + minor*100 + patch. */
 int kda_version(void);
+
+/* Synchronises the current device, then reports whether any kernel of this
+ * library gave up a bounded wait since the previous call (KDA_ERR_TIMEOUT;
+ * the outputs of that launch are then unspecified) or the device reported an
+ * error (KDA_ERR_LAUNCH).  Clears the timeout record.  The tensor-core
+ * prefill bounds each of its internal waits at a few seconds and exits
+ * instead of hanging. */
+kda_status kda_check_device_status(void);
 
 /* Number of CUDA kernels this library has enqueued in this process so far
  * (all entry points, all threads).  Lets a caller count launches over a

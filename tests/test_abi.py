@@ -79,6 +79,14 @@ def test_validation_rejects_before_launch(lib):
                                None, None) == 0
 
 
+def test_kernel_selection(lib):
+    import torch
+    assert kda.chunk_fwd_kernel(torch.bfloat16, 128, 128) == "prefill_tc_kernel"
+    assert kda.chunk_fwd_kernel(torch.float32, 128, 128) == "prefill_simt_kernel"
+    assert kda.chunk_fwd_kernel(torch.bfloat16, 64, 128) == "prefill_simt_kernel"
+    assert lib.kda_chunk_fwd_kernel(1, 48, 128) is None
+
+
 def test_python_binding_refuses_cpu_tensors(lib):
     import torch
     x = torch.zeros(1, 16, 1, 32)
