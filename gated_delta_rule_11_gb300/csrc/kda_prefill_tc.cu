@@ -30,19 +30,22 @@
 //   (h) D[:, 32:160] = Vt^T (K e^{b_C - b})              M128 N128 K16
 //       -> the state increment, transposed
 //
-// CTA roles (one CTA per (sequence, head) chain, 320 threads):
-//   warps 0-3  chain     : thread j owns column j of the fp32 state in
-//                          registers; per tile it forms Vt^T = U^T + D[:,0:16]
-//                          as the fp16 operand of (g)/(h), stores O, applies
-//                          S = Diag(e^{b_C}) S + increment, and writes the fp16
-//                          copy of S^T that the next tile's (e) reads.
-//   warps 4-7  producer  : thread c owns key channel c: gate (eq. 5),
-//                          cumulative decay, decay-scaled operands, L and A
-//                          (one 16x8 block per warp, mma.sync tf32), the
-//                          triangular solve (warp 4), W and U.
-//   warp 8     TMA       : loads the q, k, g_raw, v tiles (16 tokens each)
+// CTA roles (one CTA per (sequence, head) chain, 448 threads):
+//   warps 0-7  chain     : two warpgroups; thread (j, half) owns rows
+//                          [64 half, 64 half + 64) of column j of the fp32
+//                          state in registers.  Per tile they form
+//                          Vt^T = U^T + D[:,0:16] as the fp16 operand of
+//                          (g)/(h), store O, apply S = Diag(e^{b_C}) S +
+//                          increment and write the fp16 copy of S^T that the
+//                          next tile's (e) reads.
+//   warps 8-11 producer  : thread c owns key channel c: gate (eq. 5) and
+//                          in-tile decays as running products of the
+//                          retentions, decay-scaled operands, L and A (one
+//                          16x8 block per warp), the triangular solve
+//                          (warp 8), W and U (tf32 mma.sync).
+//   warp 12    TMA       : loads the q, k, g_raw, v tiles (16 tokens each)
 //                          into a 3-stage ring.
-//   warp 9     MMA       : issues the tcgen05 products and commits.
+//   warp 13    MMA       : issues the tcgen05 products and commits.
 // The chain is serial per tile; the producer and TMA run up to 3 tiles ahead.
 // Tokens past a sequence's end are masked in the producer (k = q = 0, g = 0,
 // beta = 0), which makes U, W, A and the increment vanish for them.
@@ -62,7 +65,9 @@ using namespace sm100;
 constexpr int D = 128;           // dk = dv
 constexpr int C = 16;            // tile tokens
 constexpr int NS = 3;            // ring stages
-constexpr int NTHREADS = 320;
+constexpr int NTHREADS = 448;
+constexpr int NCHAIN = 256;        // chain threads (two warpgroups)
+constexpr int TBS = 20;            // row stride of the fp32 T Diag(beta) tile (conflict-free fragments)
 constexpr int TMEM_COLS = 256;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits: 1 s (legitimate ones take microseconds)
 constexpr int PADF = 132;        // fp32 row stride of the mma.sync operand tiles (conflict-free fragments)
@@ -85,8 +90,8 @@ constexpr int OFF_KGM = OFF_VT + 4096;            // fp32 [16][PADF]: K e^b   (t
 constexpr int OFF_QGM = OFF_KGM + C * PADF * 4;   // fp32 [16][PADF]: Q e^b   (tf32-rounded)
 constexpr int OFF_KIM = OFF_QGM + C * PADF * 4;   // fp32 [16][PADF]: K e^-b  (tf32-rounded)
 constexpr int OFF_LS = OFF_KIM + C * PADF * 4;    // fp32 [16][17]: L
-constexpr int OFF_TBF = OFF_LS + C * 17 * 4;      // fp32 [16][16]: T Diag(beta)
-constexpr int OFF_BAR = (OFF_TBF + C * C * 4 + 63) & ~63;
+constexpr int OFF_TBF = OFF_LS + C * 17 * 4;      // fp32 [16][TBS]: T Diag(beta) (tf32-rounded)
+constexpr int OFF_BAR = (OFF_TBF + C * TBS * 4 + 63) & ~63;
 enum { B_RAW = 0, B_FULL = NS, B_EMPTY = 2 * NS, B_VT = 3 * NS, B_VTS, B_UPD, B_SRDY, NUM_BARS };
 constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_FLAG = OFF_SLOT + 4;
@@ -106,6 +111,18 @@ __device__ __forceinline__ void st_h(uint8_t *p, float x) {
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&h);
+}
+constexpr float kLog2e = 1.4426950408889634f;
+// Single-instruction MUFU approximations (rel. error ~2^-22 and 1 ulp).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 __device__ __forceinline__ float to_tf32(float x) {
     uint32_t u;
@@ -152,14 +169,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             mbar_init(&bars[B_EMPTY + s], 2);
         }
         mbar_init(&bars[B_VT], 1);
-        mbar_init(&bars[B_VTS], 128);
+        mbar_init(&bars[B_VTS], NCHAIN);
         mbar_init(&bars[B_UPD], 1);
         mbar_init(&bars[B_SRDY], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tmem_slot, TMEM_COLS);
-    if (warp == 8 && lane == 0) {
+    if (warp == 12 && lane == 0) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_z);
@@ -170,7 +187,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 8) {
+    if (warp == 12) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
             for (int t = 0; t < ntiles; ++t) {
@@ -189,7 +206,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tma_load_3d(st + ST_V, &tm_v, &bars[B_RAW + s], 0, h, tok);
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == 13) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
             constexpr uint32_t id_e = idesc_f16kind(kTypeF16, 128, 32, 0, 0);
@@ -230,10 +247,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 mma_commit(&bars[B_EMPTY + s]);
             }
         }
-    } else if (warp >= 4) {
+    } else if (warp >= 8) {
         // ------------------------------------------------------------ producer
-        const int c = tid - 128;
-        const int pw = warp - 4;
+        const int c = tid - NCHAIN;
+        const int pw = warp - 8;
         const float escale = a.A_log ? expf(__ldg(a.A_log + h)) : 1.0f;
         const __nv_bfloat16 *gbeta = static_cast<const __nv_bfloat16 *>(a.beta);
         float *kgm = reinterpret_cast<float *>(base + OFF_KGM);
@@ -258,36 +275,46 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             bt_next = load_beta(t + 1);
             if (!mbar_wait(&bars[B_RAW + s], (t / NS) & 1, kWaitLimitNs)) note_timeout(abort_flag);
 
-            float kr[C], qr[C], b[C];
-            float run = 0.f;
+            // Gate and decays in log2 units, branch-free: g2 = g / ln 2, the
+            // retention a_r = 2^{g2_r}; prefix products give e^{b_r}, suffix
+            // products e^{b_C - b_r}, and e^{-b_r} = e^{b_C - b_r} / e^{b_C}.
+            float kr[C], qr[C], pre[C], suf[C];
 #pragma unroll
             for (int r = 0; r < C; ++r) {
+                const float m = r < nv ? 1.f : 0.f;
                 const float z = bf16_at(st + ST_Z + r * 256 + c * 2);
-                kr[r] = bf16_at(st + ST_K + r * 256 + c * 2);
-                qr[r] = bf16_at(st + ST_Q + r * 256 + c * 2);
-                if (r < nv) {
-                    run += log_decay_fast(z, escale, a.g_min);
-                } else {
-                    kr[r] = 0.f;
-                    qr[r] = 0.f;
-                }
-                b[r] = run;
+                kr[r] = m * bf16_at(st + ST_K + r * 256 + c * 2);
+                qr[r] = m * bf16_at(st + ST_Q + r * 256 + c * 2);
+                const float sig = rcp_approx(1.f + ex2_approx(-kLog2e * escale * z));
+                suf[r] = ex2_approx(m * (kLog2e * a.g_min) * sig);      // retention a_r (1 past the end)
             }
-            const float gC = expf(run);
+            float run = 1.f;
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                run *= suf[r];
+                pre[r] = run;                                          // e^{b_r}
+            }
+            const float gC = run;                                      // e^{b_C}
+            run = 1.f;
+#pragma unroll
+            for (int r = C - 1; r >= 0; --r) {
+                const float a_r = suf[r];
+                suf[r] = run;                                          // e^{b_C - b_r}
+                run *= a_r;
+            }
+            const float inv_gC = rcp_approx(gC);
             reinterpret_cast<float *>(st + ST_GC)[c] = gC;
             if (c < C) reinterpret_cast<float *>(st + ST_BETA)[c] = bt;
 #pragma unroll
             for (int r = 0; r < C; ++r) {
-                const float e = __expf(b[r]);
-                const float ei = __frcp_rn(e);
-                const float kg = kr[r] * e;
-                const float qg = qr[r] * e;
+                const float kg = kr[r] * pre[r];
+                const float qg = qr[r] * pre[r];
+                const float kd = kr[r] * suf[r];
                 st_h(st + ST_WQ + off_kmajor_sw128(16 + r, c, 32), qg);
+                st_h(st + ST_KD + off_mnmajor_sw128(c, r, C), kd);
                 qgm[r * PADF + c] = to_tf32(qg);
                 kgm[r * PADF + c] = to_tf32(kg);
-                kim[r * PADF + c] = to_tf32(kr[r] * ei);
-                st_h(st + ST_KD + off_mnmajor_sw128(c, r, C), kr[r] * (gC * ei));
-                b[r] = kg;  // keep K e^b (fp32) for W
+                kim[r * PADF + c] = to_tf32(kd * inv_gC);
             }
             if (named_bar_or(1, 128, *abort_flag != 0)) break;   // uniform across the warpgroup
 
@@ -331,61 +358,76 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
                 const float bs = betas[lane];
 #pragma unroll
-                for (int r = 0; r < C; ++r) tbf[r * C + lane] = tcol[r] * bs;
+                for (int r = 0; r < C; ++r) tbf[r * TBS + lane] = to_tf32(tcol[r] * bs);
             }
             named_bar_sync(1, 128);
             // W = T Diag(beta) (K e^b) -> rows 0..15 of the (e) B operand hold -W;
-            // U = T Diag(beta) V (fp32) for the chain.
-            float *u = reinterpret_cast<float *>(st + ST_U);
-            float vc[C];
+            // U = T Diag(beta) V (fp32) for the chain.  16 x 16 x 128 each, tf32
+            // mma.sync; warp pw covers channels [32 pw, 32 pw + 32).
+            {
+                const int g = lane >> 2, tq = lane & 3;
+                uint32_t ta[2][4];
 #pragma unroll
-            for (int r = 0; r < C; ++r) vc[r] = bf16_at(st + ST_V + r * 256 + c * 2);
-#pragma unroll
-            for (int r = 0; r < C; ++r) {
-                float tb[C];
-#pragma unroll
-                for (int q4 = 0; q4 < C / 4; ++q4) {
-                    const float4 t4 = *reinterpret_cast<const float4 *>(tbf + r * C + q4 * 4);
-                    tb[q4 * 4 + 0] = t4.x;
-                    tb[q4 * 4 + 1] = t4.y;
-                    tb[q4 * 4 + 2] = t4.z;
-                    tb[q4 * 4 + 3] = t4.w;
+                for (int ks = 0; ks < 2; ++ks) {
+                    const int k0 = ks * 8;
+                    ta[ks][0] = __float_as_uint(tbf[g * TBS + k0 + tq]);
+                    ta[ks][1] = __float_as_uint(tbf[(g + 8) * TBS + k0 + tq]);
+                    ta[ks][2] = __float_as_uint(tbf[g * TBS + k0 + tq + 4]);
+                    ta[ks][3] = __float_as_uint(tbf[(g + 8) * TBS + k0 + tq + 4]);
                 }
-                float w = 0.f, uu = 0.f;
+                float *u = reinterpret_cast<float *>(st + ST_U);
 #pragma unroll
-                for (int s2 = 0; s2 <= r; ++s2) {
-                    w = fmaf(tb[s2], b[s2], w);
-                    uu = fmaf(tb[s2], vc[s2], uu);
+                for (int nb = 0; nb < 4; ++nb) {
+                    const int cn = pw * 32 + nb * 8 + g;          // B-fragment column (channel)
+                    float dw[4] = {0.f, 0.f, 0.f, 0.f}, du[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        const int s0 = ks * 8 + tq;
+                        const uint32_t bw0 = __float_as_uint(kgm[s0 * PADF + cn]);
+                        const uint32_t bw1 = __float_as_uint(kgm[(s0 + 4) * PADF + cn]);
+                        const uint32_t bu0 = __float_as_uint(bf16_at(st + ST_V + s0 * 256 + cn * 2));
+                        const uint32_t bu1 = __float_as_uint(bf16_at(st + ST_V + (s0 + 4) * 256 + cn * 2));
+                        mma_1688_tf32(dw, ta[ks][0], ta[ks][1], ta[ks][2], ta[ks][3], bw0, bw1);
+                        mma_1688_tf32(du, ta[ks][0], ta[ks][1], ta[ks][2], ta[ks][3], bu0, bu1);
+                    }
+                    const int c0 = pw * 32 + nb * 8 + 2 * tq;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int row = g + (e >> 1) * 8;
+                        st_h(st + ST_WQ + off_kmajor_sw128(row, c0 + (e & 1), 32), -dw[e]);
+                    }
+                    *reinterpret_cast<float2 *>(u + g * D + c0) = make_float2(du[0], du[1]);
+                    *reinterpret_cast<float2 *>(u + (g + 8) * D + c0) = make_float2(du[2], du[3]);
                 }
-                st_h(st + ST_WQ + off_kmajor_sw128(r, c, 32), -w);
-                u[r * D + c] = uu;
             }
             fence_proxy_async_smem();
             mbar_arrive(&bars[B_FULL + s]);
         }
     } else {
         // ------------------------------------------------------------ chain
-        const int j = tid;
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        float S[D];
+        const int j = tid & 127;           // value channel = TMEM lane
+        const int hf = tid >> 7;           // which half of the key rows / tile columns
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        constexpr int HR = D / 2;          // state rows per thread
+        float S[HR];
 #pragma unroll
-        for (int cc = 0; cc < D; ++cc)
-            S[cc] = a.init_state ? a.init_state[state_off + static_cast<size_t>(cc) * D + j] : 0.f;
+        for (int cc = 0; cc < HR; ++cc)
+            S[cc] = a.init_state ? a.init_state[state_off + static_cast<size_t>(hf * HR + cc) * D + j] : 0.f;
         uint8_t *sT = base + OFF_ST;
         auto write_sT = [&]() {
 #pragma unroll
-            for (int q8 = 0; q8 < D / 8; ++q8) {
+            for (int q8 = 0; q8 < HR / 8; ++q8) {
                 uint4 v;
                 v.x = pack_h2(S[q8 * 8 + 0], S[q8 * 8 + 1]);
                 v.y = pack_h2(S[q8 * 8 + 2], S[q8 * 8 + 3]);
                 v.z = pack_h2(S[q8 * 8 + 4], S[q8 * 8 + 5]);
                 v.w = pack_h2(S[q8 * 8 + 6], S[q8 * 8 + 7]);
-                *reinterpret_cast<uint4 *>(sT + off_kmajor_sw128(j, q8 * 8, D)) = v;
+                *reinterpret_cast<uint4 *>(sT + off_kmajor_sw128(j, hf * HR + q8 * 8, D)) = v;
             }
         };
         write_sT();
         fence_proxy_async_smem();
-        named_bar_sync(2, 128);
+        named_bar_sync(2, NCHAIN);
         if (tid == 0) mbar_arrive(&bars[B_SRDY]);
 
         __nv_bfloat16 *gout = static_cast<__nv_bfloat16 *>(a.out);
@@ -398,24 +440,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (!mbar_wait(&bars[B_VT], t & 1, kWaitLimitNs)) note_timeout(abort_flag);
             tc_fence_after();
             {
-                float v[16];
-                tmem_ld16(tmem + lane_base, v);
+                // tile columns [8 hf, 8 hf + 8) of Vt^T = U^T - (W S)^T
+                float v[8];
+                tmem_ld8(tmem + lane_base + 8 * hf, v);
                 const float *u = reinterpret_cast<const float *>(st + ST_U);
-                float uj[16];
+                float uj[8];
 #pragma unroll
-                for (int r = 0; r < C; ++r) uj[r] = u[r * D + j];
+                for (int r = 0; r < 8; ++r) uj[r] = u[(8 * hf + r) * D + j];
                 tmem_ld_wait();
-                uint4 lo, hi;
-                lo.x = pack_h2(uj[0] + v[0], uj[1] + v[1]);
-                lo.y = pack_h2(uj[2] + v[2], uj[3] + v[3]);
-                lo.z = pack_h2(uj[4] + v[4], uj[5] + v[5]);
-                lo.w = pack_h2(uj[6] + v[6], uj[7] + v[7]);
-                hi.x = pack_h2(uj[8] + v[8], uj[9] + v[9]);
-                hi.y = pack_h2(uj[10] + v[10], uj[11] + v[11]);
-                hi.z = pack_h2(uj[12] + v[12], uj[13] + v[13]);
-                hi.w = pack_h2(uj[14] + v[14], uj[15] + v[15]);
-                *reinterpret_cast<uint4 *>(vt + off_kmajor_none(j, 0, C)) = lo;
-                *reinterpret_cast<uint4 *>(vt + off_kmajor_none(j, 8, C)) = hi;
+                uint4 p;
+                p.x = pack_h2(uj[0] + v[0], uj[1] + v[1]);
+                p.y = pack_h2(uj[2] + v[2], uj[3] + v[3]);
+                p.z = pack_h2(uj[4] + v[4], uj[5] + v[5]);
+                p.w = pack_h2(uj[6] + v[6], uj[7] + v[7]);
+                *reinterpret_cast<uint4 *>(vt + off_kmajor_none(j, 8 * hf, C)) = p;
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -423,19 +461,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (!mbar_wait(&bars[B_UPD], t & 1, kWaitLimitNs)) note_timeout(abort_flag);
             tc_fence_after();
             {
-                float o[16];
-                tmem_ld16(tmem + lane_base + 16, o);
+                float o[8];
+                tmem_ld8(tmem + lane_base + 16 + 8 * hf, o);
                 tmem_ld_wait();
-                __nv_bfloat16 *op = gout + static_cast<size_t>(t0) * a.H * D + static_cast<size_t>(h) * D + j;
+                __nv_bfloat16 *op = gout + static_cast<size_t>(t0 + 8 * hf) * a.H * D + static_cast<size_t>(h) * D + j;
 #pragma unroll
-                for (int r = 0; r < C; ++r)
-                    if (r < nv) op[static_cast<size_t>(r) * a.H * D] = __float2bfloat16_rn(a.scale * o[r]);
+                for (int r = 0; r < 8; ++r)
+                    if (8 * hf + r < nv) op[static_cast<size_t>(r) * a.H * D] = __float2bfloat16_rn(a.scale * o[r]);
             }
-            const float *gc = reinterpret_cast<const float *>(st + ST_GC);
+            const float *gc = reinterpret_cast<const float *>(st + ST_GC) + hf * HR;
 #pragma unroll
-            for (int cb = 0; cb < D / 16; ++cb) {
+            for (int cb = 0; cb < HR / 16; ++cb) {
                 float inc[16];
-                tmem_ld16(tmem + lane_base + 32 + cb * 16, inc);
+                tmem_ld16(tmem + lane_base + 32 + hf * HR + cb * 16, inc);
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 16; ++i) S[cb * 16 + i] = fmaf(gc[cb * 16 + i], S[cb * 16 + i], inc[i]);
@@ -443,7 +481,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             write_sT();
             fence_proxy_async_smem();
             tc_fence_before();
-            if (named_bar_or(2, 128, *abort_flag != 0)) break;   // uniform across the warpgroup
+            if (named_bar_or(2, NCHAIN, *abort_flag != 0)) break;   // uniform across the chain
             if (tid == 0) {
                 mbar_arrive(&bars[B_SRDY]);
                 mbar_arrive(&bars[B_EMPTY + s]);
@@ -451,7 +489,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         if (a.final_state && !*abort_flag) {
 #pragma unroll
-            for (int cc = 0; cc < D; ++cc) a.final_state[state_off + static_cast<size_t>(cc) * D + j] = S[cc];
+            for (int cc = 0; cc < HR; ++cc)
+                a.final_state[state_off + static_cast<size_t>(hf * HR + cc) * D + j] = S[cc];
         }
     }
 
