@@ -66,6 +66,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+                    help="run one leg only (for profiling captures; the JSON line needs 'all')")
+    ap.add_argument("--prefill-workload", default="varlen_bf16_H96_237568",
+                    choices=[k for k, w in kin.WORKLOADS.items() if w.kind == "prefill" and w.dtype == "bf16"],
+                    help="prefill workload (profiling captures use the smaller layer-shaped one)")
     return ap.parse_args()
 
 
@@ -256,6 +261,34 @@ def run_reference(args, rank, world):
     return 0
 
 
+def run_single_leg(args, kda, dev):
+    """--only prefill|decode: warm-up then timed launches of one kernel, for
+    profiler captures; prints per-launch CUDA-event times, no JSON line."""
+    if args.only == "prefill":
+        w = kin.WORKLOADS[args.prefill_workload]
+        inp = kin.make_prefill_inputs(w, device=dev)
+        a = [inp[n] for n in ("q", "k", "v", "g_raw", "beta")]
+        out, fin = kda.kda_chunk_fwd(*a, inp["init_state"], inp["cu_seqlens"])
+        fn = lambda i: kda.kda_chunk_fwd(*a, inp["init_state"], inp["cu_seqlens"], out=out, final_state=fin)
+    else:
+        w = DECODE
+        S = kin.make_decode_state(w, device=dev)
+        t = kin.make_decode_token(w, 0, device=dev)
+        fn = lambda i: kda.kda_decode_step(t["q"], t["k"], t["v"], t["g_raw"], t["beta"], S)
+    for i in range(args.warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn(i)
+        e1.record()
+        torch.cuda.synchronize()
+        print(f"{args.only} {w.name}: {e0.elapsed_time(e1):.3f} ms", flush=True)
+    kda.check_device_status()
+    return 0
+
+
 def run_ours(args, rank, world, local):
     from gated_delta_rule_11_gb300 import kda
     if not torch.cuda.is_available():
@@ -263,16 +296,18 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     kda.load_library()
+    if args.only != "all":
+        return run_single_leg(args, kda, dev)
     peaks, peak_src = load_peaks()
 
     # ---- inputs, resident in HBM
-    pw = PREFILL
+    pw = kin.WORKLOADS[args.prefill_workload]
     inp = kin.make_prefill_inputs(pw, device=dev, seed=pw.seed + 1000 * rank)
     q, k, v, g, b = (inp[n] for n in ("q", "k", "v", "g_raw", "beta"))
     cu = inp["cu_seqlens"]
-    N = len(pw.seqlens)
-    T_total = sum(pw.seqlens)
-    out = torch.empty((1, T_total, pw.H, pw.dv), dtype=torch.bfloat16, device=dev)
+    N = pw.n_seqs
+    T_total = pw.total_tokens
+    out = torch.empty_like(v)
     fin = torch.empty((N, pw.H, pw.dk, pw.dv), dtype=torch.float32, device=dev)
 
     dw = DECODE
@@ -367,8 +402,8 @@ def run_ours(args, rank, world, local):
                   if kernel_name == "prefill_tc_kernel" else "f32 (bf16 inputs)"),
         "data": "synthetic",
         "config": {
-            "workload": "varlen_bf16_H96_237568 prefill + decode_bf16_N256_H96 step",
-            "prefill_seqlens": list(pw.seqlens), "H": pw.H, "dk": pw.dk, "dv": pw.dv,
+            "workload": f"{pw.name} prefill + decode_bf16_N256_H96 step",
+            "prefill_seqlens": list(pw.seqlens) or [pw.T] * pw.B, "H": pw.H, "dk": pw.dk, "dv": pw.dv,
             "decode_N": dw.N, "l2": "inputs larger than L2 (29 GB prefill inputs, 1.6 GB decode state); no flush",
             "value_counts": "prefill launches only (decode reported under 'decode')",
             "parallelism": f"replicas x{world}",

@@ -23,29 +23,38 @@
 //
 // Every tensor-core product is computed transposed so that its M side is a
 // 128-wide head dimension (tcgen05 M = 128, TMEM lane j = value channel j):
-//   (e) D[:, 0:32]   = S^T [-W ; Q e^b]^T                M128 N32  K128
-//       -> D[:, 0:16] = -(W S_0)^T, D[:, 16:32] = ((Q e^b) S_0)^T
-//   (g) D[:, 16:32] += Vt^T A^T                          M128 N16  K16
-//       -> D[:, 16:32] = O^T / scale
-//   (h) D[:, 32:160] = Vt^T (K e^{b_C - b})              M128 N128 K16
+// The chain writes the two operands it produces (the fp16 copy of S^T and
+// Vt^T) straight into tensor memory, where the MMAs read them as A.  (e) is
+// split over 4 independent accumulators (K slices 16 p .. mod 64) that the
+// chain sums, so the 8 instructions do not serialise on one accumulator.
+//   (e) E[:, 0:32]   = S^T [-W ; Q e^b]^T                M128 N32  K128
+//       -> E[:, 0:16] = -(W S_0)^T, E[:, 16:32] = ((Q e^b) S_0)^T
+//   (g) E[:, 16:32] += Vt^T A^T                          M128 N16  K16
+//       -> E[:, 16:32] = O^T / scale
+//   (h) H[:, 0:128]  = Vt^T (K e^{b_C - b})              M128 N128 K16
 //       -> the state increment, transposed
+// E is double-buffered in TMEM (tile parity), so tile t's O is read out
+// while tile t+1's (g)/(h) run, off the serial path; full tiles of O are
+// staged in shared memory and written with one TMA store.
 //
-// CTA roles (one CTA per (sequence, head) chain, 448 threads):
+// CTA roles (one CTA per (sequence, head) chain, 512 threads):
 //   warps 0-7  chain     : two warpgroups; thread (j, half) owns rows
 //                          [64 half, 64 half + 64) of column j of the fp32
 //                          state in registers.  Per tile they form
 //                          Vt^T = U^T + D[:,0:16] as the fp16 operand of
 //                          (g)/(h), store O, apply S = Diag(e^{b_C}) S +
-//                          increment and write the fp16 copy of S^T that the
-//                          next tile's (e) reads.
-//   warps 8-11 producer  : thread c owns key channel c: gate (eq. 5) and
+//                          increment and write the fp16 copy of S^T (into
+//                          TMEM) that the next tile's (e) reads.  One elected chain thread
+//                          issues the tcgen05 products and commits them, and
+//                          the TMA loads of the q, k, g_raw, v tiles (16
+//                          tokens each) into a 3-stage ring, refilling a
+//                          stage as soon as the chain has finished with it.
+//   warps 8-15 producer  : two warpgroups taking alternate tiles, each with
+//                          its own scratch; thread c owns key channel c: gate (eq. 5) and
 //                          in-tile decays as running products of the
 //                          retentions, decay-scaled operands, L and A (one
 //                          16x8 block per warp), the triangular solve
-//                          (warp 8), W and U (tf32 mma.sync).
-//   warp 12    TMA       : loads the q, k, g_raw, v tiles (16 tokens each)
-//                          into a 3-stage ring.
-//   warp 13    MMA       : issues the tcgen05 products and commits.
+//                          (first warp), W and U (tf32 mma.sync).
 // The chain is serial per tile; the producer and TMA run up to 3 tiles ahead.
 // Tokens past a sequence's end are masked in the producer (k = q = 0, g = 0,
 // beta = 0), which makes U, W, A and the increment vanish for them.
@@ -65,10 +74,11 @@ using namespace sm100;
 constexpr int D = 128;           // dk = dv
 constexpr int C = 16;            // tile tokens
 constexpr int NS = 3;            // ring stages
-constexpr int NTHREADS = 448;
+constexpr int NTHREADS = 512;
+constexpr int NPROD = 2;           // producer warpgroups
 constexpr int NCHAIN = 256;        // chain threads (two warpgroups)
 constexpr int TBS = 20;            // row stride of the fp32 T Diag(beta) tile (conflict-free fragments)
-constexpr int TMEM_COLS = 256;
+constexpr int TMEM_COLS = 512;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits: 1 s (legitimate ones take microseconds)
 constexpr int PADF = 132;        // fp32 row stride of the mma.sync operand tiles (conflict-free fragments)
 
@@ -84,21 +94,29 @@ constexpr int ST_U = 29696;      // fp32 [16][128] U
 constexpr int ST_GC = 37888;     // fp32 [128] e^{b_C}
 constexpr int ST_BETA = 38400;   // fp32 [16]
 constexpr int STAGE_BYTES = 38912;
-constexpr int OFF_ST = NS * STAGE_BYTES;          // S^T fp16, K-major SW128, 128 x 128
-constexpr int OFF_VT = OFF_ST + 32768;            // Vt^T fp16, K-major none, 128 x 16
-constexpr int OFF_KGM = OFF_VT + 4096;            // fp32 [16][PADF]: K e^b   (tf32-rounded)
-constexpr int OFF_QGM = OFF_KGM + C * PADF * 4;   // fp32 [16][PADF]: Q e^b   (tf32-rounded)
-constexpr int OFF_KIM = OFF_QGM + C * PADF * 4;   // fp32 [16][PADF]: K e^-b  (tf32-rounded)
-constexpr int OFF_LS = OFF_KIM + C * PADF * 4;    // fp32 [16][17]: L
-constexpr int OFF_TBF = OFF_LS + C * 17 * 4;      // fp32 [16][TBS]: T Diag(beta) (tf32-rounded)
-constexpr int OFF_BAR = (OFF_TBF + C * TBS * 4 + 63) & ~63;
-enum { B_RAW = 0, B_FULL = NS, B_EMPTY = 2 * NS, B_VT = 3 * NS, B_VTS, B_UPD, B_SRDY, NUM_BARS };
+constexpr int OFF_OST = NS * STAGE_BYTES;         // two bf16 [16][128] O staging tiles (TMA store)
+constexpr int OFF_VT = OFF_OST + 2 * C * D * 2;
+constexpr int OFF_SCR = OFF_VT;                   // per-producer scratch, SCR_BYTES each:
+constexpr int SC_KGM = 0;                         //   fp32 [16][PADF]: K e^b   (tf32-rounded)
+constexpr int SC_QGM = C * PADF * 4;              //   fp32 [16][PADF]: Q e^b   (tf32-rounded)
+constexpr int SC_KIM = 2 * C * PADF * 4;          //   fp32 [16][PADF]: K e^-b  (tf32-rounded)
+constexpr int SC_LS = 3 * C * PADF * 4;           //   fp32 [16][17]: L
+constexpr int SC_TBF = SC_LS + C * 17 * 4;        //   fp32 [16][TBS]: T Diag(beta) (tf32-rounded)
+constexpr int SCR_BYTES = (SC_TBF + C * TBS * 4 + 127) & ~127;
+constexpr int OFF_BAR = (OFF_SCR + NPROD * SCR_BYTES + 63) & ~63;
+enum { B_RAW = 0, B_FULL = NS, B_VT = 2 * NS, B_UPD, NUM_BARS };
+constexpr int NACC = 4;          // independent accumulators of (e)
+constexpr uint32_t TM_E = 0;     // two E buffers of NACC x 32 columns
+constexpr uint32_t TM_H = 256;   // 128-column H
+constexpr uint32_t TM_ST = 384;  // S^T fp16, 128 K values packed in 64 columns
+constexpr uint32_t TM_VT = 448;  // Vt^T fp16, 16 K values packed in 8 columns
+constexpr uint32_t E_BUF = NACC * 32;
 constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_FLAG = OFF_SLOT + 4;
 constexpr int SMEM_USED = OFF_FLAG + 4;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;      // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-static_assert(STAGE_BYTES % 1024 == 0 && ST_WQ % 1024 == 0 && ST_KD % 1024 == 0 && OFF_ST % 1024 == 0,
+static_assert(STAGE_BYTES % 1024 == 0 && ST_WQ % 1024 == 0 && ST_KD % 1024 == 0,
               "128B-swizzled operands need 1024-byte alignment");
 constexpr uint32_t TX_BYTES = 4 * C * D * 2;
 
@@ -147,7 +165,7 @@ __device__ __forceinline__ void note_timeout(volatile int *flag) {
 __global__ void __launch_bounds__(NTHREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_v,
-                  PrefillArgs a) {
+                  const __grid_constant__ CUtensorMap tm_o, PrefillArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + OFF_BAR);
@@ -166,98 +184,39 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int s = 0; s < NS; ++s) {
             mbar_init(&bars[B_RAW + s], 1);
             mbar_init(&bars[B_FULL + s], 128);
-            mbar_init(&bars[B_EMPTY + s], 2);
         }
         mbar_init(&bars[B_VT], 1);
-        mbar_init(&bars[B_VTS], NCHAIN);
         mbar_init(&bars[B_UPD], 1);
-        mbar_init(&bars[B_SRDY], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tmem_slot, TMEM_COLS);
-    if (warp == 12 && lane == 0) {
+    if (tid == 0) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_z);
         prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_o);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 12) {
-        // ------------------------------------------------------------ TMA
-        if (lane == 0) {
-            for (int t = 0; t < ntiles; ++t) {
-                const int s = t % NS;
-                if (t >= NS && !mbar_wait(&bars[B_EMPTY + s], ((t / NS) - 1) & 1, kWaitLimitNs)) {
-                    note_timeout(abort_flag);
-                    break;
-                }
-                if (*abort_flag) break;
-                uint8_t *st = base + s * STAGE_BYTES;
-                const int tok = bos + t * C;
-                mbar_arrive_expect_tx(&bars[B_RAW + s], TX_BYTES);
-                tma_load_3d(st + ST_Q, &tm_q, &bars[B_RAW + s], 0, h, tok);
-                tma_load_3d(st + ST_K, &tm_k, &bars[B_RAW + s], 0, h, tok);
-                tma_load_3d(st + ST_Z, &tm_z, &bars[B_RAW + s], 0, h, tok);
-                tma_load_3d(st + ST_V, &tm_v, &bars[B_RAW + s], 0, h, tok);
-            }
-        }
-    } else if (warp == 13) {
-        // ------------------------------------------------------------ MMA issue
-        if (lane == 0) {
-            constexpr uint32_t id_e = idesc_f16kind(kTypeF16, 128, 32, 0, 0);
-            constexpr uint32_t id_g = idesc_f16kind(kTypeF16, 128, 16, 0, 0);
-            constexpr uint32_t id_h = idesc_f16kind(kTypeF16, 128, 128, 0, 1);
-            const uint32_t sb = smem_u32(base);
-            const uint64_t d_vt = smem_desc(sb + OFF_VT, 128, 256, kLayoutNone);
-            for (int t = 0; t < ntiles; ++t) {
-                const int s = t % NS;
-                const uint32_t st = sb + s * STAGE_BYTES;
-                if (!mbar_wait(&bars[B_FULL + s], (t / NS) & 1, kWaitLimitNs) ||
-                    !mbar_wait(&bars[B_SRDY], t & 1, kWaitLimitNs)) {
-                    note_timeout(abort_flag);
-                    break;
-                }
-                if (*abort_flag) break;
-                tc_fence_after();
-                // (e) D[:,0:32] = S^T [-W ; Q e^b]^T, K = 128 in steps of 16
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const int k = kk * 16;
-                    const uint32_t a_off = OFF_ST + (k >> 6) * (128 * 128) + (k & 63) * 2;
-                    const uint32_t b_off = ST_WQ + (k >> 6) * (32 * 128) + (k & 63) * 2;
-                    mma_f16kind(tmem, smem_desc(sb + a_off, 16, 1024, kLayoutSW128),
-                                smem_desc(st + b_off, 16, 1024, kLayoutSW128), id_e, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(&bars[B_VT]);
-                if (!mbar_wait(&bars[B_VTS], t & 1, kWaitLimitNs)) {
-                    note_timeout(abort_flag);
-                    break;
-                }
-                tc_fence_after();
-                // (g) D[:,16:32] += Vt^T A^T
-                mma_f16kind(tmem + 16, d_vt, smem_desc(st + ST_AT, 128, 256, kLayoutNone), id_g, 1);
-                // (h) D[:,32:160] = Vt^T (K e^{b_C - b})
-                mma_f16kind(tmem + 32, d_vt, smem_desc(st + ST_KD, 2048, 1024, kLayoutSW128), id_h, 0);
-                mma_commit(&bars[B_UPD]);
-                mma_commit(&bars[B_EMPTY + s]);
-            }
-        }
-    } else if (warp >= 8) {
-        // ------------------------------------------------------------ producer
-        const int c = tid - NCHAIN;
-        const int pw = warp - 8;
+    if (warp >= 8) {
+        // ------------------------------------------------------------ producers
+        const int pg = (warp - 8) >> 2;     // producer warpgroup: tiles t = pg (mod 2)
+        const int c = tid - NCHAIN - 128 * pg;
+        const int pw = (warp - 8) & 3;
+        const uint32_t pbar = 1 + 2 * pg;   // its named barrier (chain uses 2)
         const float escale = a.A_log ? expf(__ldg(a.A_log + h)) : 1.0f;
         const __nv_bfloat16 *gbeta = static_cast<const __nv_bfloat16 *>(a.beta);
-        float *kgm = reinterpret_cast<float *>(base + OFF_KGM);
-        float *qgm = reinterpret_cast<float *>(base + OFF_QGM);
-        float *kim = reinterpret_cast<float *>(base + OFF_KIM);
-        float *ls = reinterpret_cast<float *>(base + OFF_LS);
-        float *tbf = reinterpret_cast<float *>(base + OFF_TBF);
+        uint8_t *scr = base + OFF_SCR + pg * SCR_BYTES;
+        float *kgm = reinterpret_cast<float *>(scr + SC_KGM);
+        float *qgm = reinterpret_cast<float *>(scr + SC_QGM);
+        float *kim = reinterpret_cast<float *>(scr + SC_KIM);
+        float *ls = reinterpret_cast<float *>(scr + SC_LS);
+        float *tbf = reinterpret_cast<float *>(scr + SC_TBF);
         // beta is a strided gather (one value per token): load it a tile ahead
         // so its latency hides behind a tile of work.
         auto load_beta = [&](int tt) {
@@ -265,14 +224,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             return (c < C && tt < ntiles && tok < eos)
                        ? __bfloat162float(gbeta[static_cast<size_t>(tok) * a.H + h]) : 0.f;
         };
-        float bt_next = load_beta(0);
-        for (int t = 0; t < ntiles; ++t) {
+        float bt_next = load_beta(pg);
+        for (int t = pg; t < ntiles; t += NPROD) {
             const int s = t % NS;
             uint8_t *st = base + s * STAGE_BYTES;
             const int t0 = bos + t * C;
             const int nv = min(C, eos - t0);
             const float bt = bt_next;
-            bt_next = load_beta(t + 1);
+            bt_next = load_beta(t + NPROD);
             if (!mbar_wait(&bars[B_RAW + s], (t / NS) & 1, kWaitLimitNs)) note_timeout(abort_flag);
 
             // Gate and decays in log2 units, branch-free: g2 = g / ln 2, the
@@ -316,24 +275,30 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 kgm[r * PADF + c] = to_tf32(kg);
                 kim[r * PADF + c] = to_tf32(kd * inv_gC);
             }
-            if (named_bar_or(1, 128, *abort_flag != 0)) break;   // uniform across the warpgroup
+            if (named_bar_or(pbar, 128, *abort_flag != 0)) break;   // uniform across the warpgroup
 
             {
                 // one 16x8 block per warp: pw 0/1 -> L columns 0-7/8-15, pw 2/3 -> A
                 const int g = lane >> 2, tq = lane & 3;
                 const float *lhs = pw < 2 ? kgm : qgm;
                 const int n0 = (pw & 1) * 8;
-                float d4[4] = {0.f, 0.f, 0.f, 0.f};
+                float d4[4] = {0.f, 0.f, 0.f, 0.f}, d4b[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int k0 = 0; k0 < D; k0 += 8) {
-                    const uint32_t a0 = __float_as_uint(lhs[g * PADF + k0 + tq]);
-                    const uint32_t a1 = __float_as_uint(lhs[(g + 8) * PADF + k0 + tq]);
-                    const uint32_t a2 = __float_as_uint(lhs[g * PADF + k0 + tq + 4]);
-                    const uint32_t a3 = __float_as_uint(lhs[(g + 8) * PADF + k0 + tq + 4]);
-                    const uint32_t b0 = __float_as_uint(kim[(n0 + g) * PADF + k0 + tq]);
-                    const uint32_t b1 = __float_as_uint(kim[(n0 + g) * PADF + k0 + tq + 4]);
-                    mma_1688_tf32(d4, a0, a1, a2, a3, b0, b1);
+                for (int k0 = 0; k0 < D; k0 += 16) {
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int kb = k0 + 8 * hh;
+                        const uint32_t a0 = __float_as_uint(lhs[g * PADF + kb + tq]);
+                        const uint32_t a1 = __float_as_uint(lhs[(g + 8) * PADF + kb + tq]);
+                        const uint32_t a2 = __float_as_uint(lhs[g * PADF + kb + tq + 4]);
+                        const uint32_t a3 = __float_as_uint(lhs[(g + 8) * PADF + kb + tq + 4]);
+                        const uint32_t b0 = __float_as_uint(kim[(n0 + g) * PADF + kb + tq]);
+                        const uint32_t b1 = __float_as_uint(kim[(n0 + g) * PADF + kb + tq + 4]);
+                        mma_1688_tf32(hh ? d4b : d4, a0, a1, a2, a3, b0, b1);
+                    }
                 }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) d4[e] += d4b[e];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int row = g + (e >> 1) * 8;
@@ -344,7 +309,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         st_h(st + ST_AT + off_kmajor_none(row, col, C), col <= row ? d4[e] : 0.f);
                 }
             }
-            named_bar_sync(1, 128);
+            named_bar_sync(pbar, 128);
             if (pw == 0 && lane < C) {
                 // T = (I + Diag(beta) L)^-1 by forward substitution; lane s owns column s.
                 const float *betas = reinterpret_cast<const float *>(st + ST_BETA);
@@ -360,7 +325,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
                 for (int r = 0; r < C; ++r) tbf[r * TBS + lane] = to_tf32(tcol[r] * bs);
             }
-            named_bar_sync(1, 128);
+            named_bar_sync(pbar, 128);
             // W = T Diag(beta) (K e^b) -> rows 0..15 of the (e) B operand hold -W;
             // U = T Diag(beta) V (fp32) for the chain.  16 x 16 x 128 each, tf32
             // mma.sync; warp pw covers channels [32 pw, 32 pw + 32).
@@ -409,85 +374,166 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int hf = tid >> 7;           // which half of the key rows / tile columns
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         constexpr int HR = D / 2;          // state rows per thread
+        constexpr uint32_t id_e = idesc_f16kind(kTypeF16, 128, 32, 0, 0);
+        constexpr uint32_t id_g = idesc_f16kind(kTypeF16, 128, 16, 0, 0);
+        constexpr uint32_t id_h = idesc_f16kind(kTypeF16, 128, 128, 0, 1);
+        const uint32_t sb = smem_u32(base);
+        // TMA loads of tile tt into its ring stage (one thread).
+        auto issue_tma = [&](int tt) {
+            const int ss = tt % NS;
+            uint8_t *stg = base + ss * STAGE_BYTES;
+            const int tok = bos + tt * C;
+            mbar_arrive_expect_tx(&bars[B_RAW + ss], TX_BYTES);
+            tma_load_3d(stg + ST_Q, &tm_q, &bars[B_RAW + ss], 0, h, tok);
+            tma_load_3d(stg + ST_K, &tm_k, &bars[B_RAW + ss], 0, h, tok);
+            tma_load_3d(stg + ST_Z, &tm_z, &bars[B_RAW + ss], 0, h, tok);
+            tma_load_3d(stg + ST_V, &tm_v, &bars[B_RAW + ss], 0, h, tok);
+        };
+        constexpr int TMA_TID = 32, OST_TID = 64;   // lane 0 of chain warps 1 and 2
+        if (tid == TMA_TID)
+            for (int tt = 0; tt < NS && tt < ntiles; ++tt) issue_tma(tt);
+        // (e) for tile tt, issued by one thread once the tile's operands are ready.
+        auto issue_e = [&](int tt) -> bool {
+            const int ss = tt % NS;
+            if (!mbar_wait(&bars[B_FULL + ss], (tt / NS) & 1, kWaitLimitNs)) return false;
+            tc_fence_after();
+            const uint32_t st = sb + ss * STAGE_BYTES;
+            const uint32_t e_acc = tmem + TM_E + E_BUF * static_cast<uint32_t>(tt & 1);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int k = kk * 16;
+                const uint32_t b_off = ST_WQ + (k >> 6) * (32 * 128) + (k & 63) * 2;
+                mma_f16kind_tmem_a(e_acc + 32u * (kk % NACC), tmem + TM_ST + 8 * kk,
+                                   smem_desc(st + b_off, 16, 1024, kLayoutSW128), id_e, kk >= NACC ? 1u : 0u);
+            }
+            mma_commit(&bars[B_VT]);
+            return true;
+        };
+
         float S[HR];
 #pragma unroll
         for (int cc = 0; cc < HR; ++cc)
             S[cc] = a.init_state ? a.init_state[state_off + static_cast<size_t>(hf * HR + cc) * D + j] : 0.f;
-        uint8_t *sT = base + OFF_ST;
+        // fp16 S^T row j, K range [64 hf, 64 hf + 64) -> 32 TMEM columns
         auto write_sT = [&]() {
+            uint32_t pk[HR / 2];
 #pragma unroll
-            for (int q8 = 0; q8 < HR / 8; ++q8) {
-                uint4 v;
-                v.x = pack_h2(S[q8 * 8 + 0], S[q8 * 8 + 1]);
-                v.y = pack_h2(S[q8 * 8 + 2], S[q8 * 8 + 3]);
-                v.z = pack_h2(S[q8 * 8 + 4], S[q8 * 8 + 5]);
-                v.w = pack_h2(S[q8 * 8 + 6], S[q8 * 8 + 7]);
-                *reinterpret_cast<uint4 *>(sT + off_kmajor_sw128(j, hf * HR + q8 * 8, D)) = v;
-            }
+            for (int i = 0; i < HR / 2; ++i) pk[i] = pack_h2(S[2 * i], S[2 * i + 1]);
+            tmem_st32(tmem + TM_ST + lane_base + hf * (HR / 2), pk);
+            tmem_st_wait();
         };
         write_sT();
-        fence_proxy_async_smem();
+        tc_fence_before();
         named_bar_sync(2, NCHAIN);
-        if (tid == 0) mbar_arrive(&bars[B_SRDY]);
+        if (tid == 0 && ntiles > 0 && !issue_e(0)) note_timeout(abort_flag);
 
         __nv_bfloat16 *gout = static_cast<__nv_bfloat16 *>(a.out);
-        uint8_t *vt = base + OFF_VT;
+        uint8_t *ost = base + OFF_OST;
+        // O of tile tt, rows [8 hf, 8 hf + 8): sum of the accumulators' columns
+        // 16..31.  Full tiles go to the staging tile (stored by TMA), a
+        // sequence's partial last tile straight to global memory.
+        auto read_out = [&](int tt) {
+            const uint32_t eb = tmem + TM_E + E_BUF * static_cast<uint32_t>(tt & 1) + lane_base + 16 + 8 * hf;
+            float o[8], x[8];
+            tmem_ld8(eb, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int p = 1; p < NACC; ++p) {
+                tmem_ld8(eb + 32u * p, x);
+                tmem_ld_wait();
+#pragma unroll
+                for (int r = 0; r < 8; ++r) o[r] += x[r];
+            }
+            const int tt0 = bos + tt * C;
+            const int nvv = min(C, eos - tt0);
+            if (nvv == C) {
+                __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(ost + (tt & 1) * (C * D * 2));
+#pragma unroll
+                for (int r = 0; r < 8; ++r) stg[(8 * hf + r) * D + j] = __float2bfloat16_rn(a.scale * o[r]);
+                fence_proxy_async_smem();
+            } else {
+                __nv_bfloat16 *op = gout + static_cast<size_t>(tt0 + 8 * hf) * a.H * D + static_cast<size_t>(h) * D + j;
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+                    if (8 * hf + r < nvv) op[static_cast<size_t>(r) * a.H * D] = __float2bfloat16_rn(a.scale * o[r]);
+            }
+        };
+        // after a chain barrier that follows read_out(tt): one thread stores the staged tile
+        auto store_out = [&](int tt) {
+            const int tt0 = bos + tt * C;
+            if (min(C, eos - tt0) == C) {
+                tma_store_3d(&tm_o, ost + (tt & 1) * (C * D * 2), 0, h, tt0);
+                bulk_commit();
+            }
+            bulk_wait_read<1>();   // the other staging tile is free again
+        };
         for (int t = 0; t < ntiles; ++t) {
             const int s = t % NS;
             const uint8_t *st = base + s * STAGE_BYTES;
-            const int t0 = bos + t * C;
-            const int nv = min(C, eos - t0);
-            if (!mbar_wait(&bars[B_VT], t & 1, kWaitLimitNs)) note_timeout(abort_flag);
+            const uint32_t e_acc = tmem + TM_E + E_BUF * static_cast<uint32_t>(t & 1);
+            bool ok = mbar_wait(&bars[B_VT], t & 1, kWaitLimitNs);
+            ok = mbar_wait(&bars[B_FULL + s], (t / NS) & 1, kWaitLimitNs) && ok;   // U, e^{b_C} visible
+            if (!ok) note_timeout(abort_flag);
             tc_fence_after();
             {
                 // tile columns [8 hf, 8 hf + 8) of Vt^T = U^T - (W S)^T
-                float v[8];
-                tmem_ld8(tmem + lane_base + 8 * hf, v);
                 const float *u = reinterpret_cast<const float *>(st + ST_U);
-                float uj[8];
+                float uj[8], v[8];
 #pragma unroll
                 for (int r = 0; r < 8; ++r) uj[r] = u[(8 * hf + r) * D + j];
-                tmem_ld_wait();
-                uint4 p;
-                p.x = pack_h2(uj[0] + v[0], uj[1] + v[1]);
-                p.y = pack_h2(uj[2] + v[2], uj[3] + v[3]);
-                p.z = pack_h2(uj[4] + v[4], uj[5] + v[5]);
-                p.w = pack_h2(uj[6] + v[6], uj[7] + v[7]);
-                *reinterpret_cast<uint4 *>(vt + off_kmajor_none(j, 8 * hf, C)) = p;
+#pragma unroll
+                for (int p = 0; p < NACC; ++p) {
+                    tmem_ld8(e_acc + 32u * p + lane_base + 8 * hf, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) uj[r] += v[r];
+                }
+                uint32_t p[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) p[i] = pack_h2(uj[2 * i], uj[2 * i + 1]);
+                tmem_st4(tmem + TM_VT + lane_base + 4 * hf, p);
+                tmem_st_wait();
             }
-            fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&bars[B_VTS]);
+            if (named_bar_or(2, NCHAIN, *abort_flag != 0)) break;   // uniform across the chain
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t stb = sb + s * STAGE_BYTES;
+                // (g) E[:,16:32] += Vt^T A^T ; (h) H = Vt^T (K e^{b_C - b})
+                mma_f16kind_tmem_a(e_acc + 16, tmem + TM_VT, smem_desc(stb + ST_AT, 128, 256, kLayoutNone), id_g, 1);
+                mma_f16kind_tmem_a(tmem + TM_H, tmem + TM_VT, smem_desc(stb + ST_KD, 2048, 1024, kLayoutSW128),
+                                   id_h, 0);
+                mma_commit(&bars[B_UPD]);
+            }
+            if (t > 0) read_out(t - 1);    // overlaps (g)/(h)
             if (!mbar_wait(&bars[B_UPD], t & 1, kWaitLimitNs)) note_timeout(abort_flag);
             tc_fence_after();
-            {
-                float o[8];
-                tmem_ld8(tmem + lane_base + 16 + 8 * hf, o);
-                tmem_ld_wait();
-                __nv_bfloat16 *op = gout + static_cast<size_t>(t0 + 8 * hf) * a.H * D + static_cast<size_t>(h) * D + j;
-#pragma unroll
-                for (int r = 0; r < 8; ++r)
-                    if (8 * hf + r < nv) op[static_cast<size_t>(r) * a.H * D] = __float2bfloat16_rn(a.scale * o[r]);
-            }
             const float *gc = reinterpret_cast<const float *>(st + ST_GC) + hf * HR;
 #pragma unroll
             for (int cb = 0; cb < HR / 16; ++cb) {
                 float inc[16];
-                tmem_ld16(tmem + lane_base + 32 + hf * HR + cb * 16, inc);
+                tmem_ld16(tmem + TM_H + lane_base + hf * HR + cb * 16, inc);
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 16; ++i) S[cb * 16 + i] = fmaf(gc[cb * 16 + i], S[cb * 16 + i], inc[i]);
             }
             write_sT();
-            fence_proxy_async_smem();
             tc_fence_before();
             if (named_bar_or(2, NCHAIN, *abort_flag != 0)) break;   // uniform across the chain
-            if (tid == 0) {
-                mbar_arrive(&bars[B_SRDY]);
-                mbar_arrive(&bars[B_EMPTY + s]);
-            }
+            // every read of this stage (TMA tiles, U, e^{b_C}, MMA operands) is done
+            if (tid == 0 && t + 1 < ntiles && !issue_e(t + 1)) note_timeout(abort_flag);
+            if (tid == TMA_TID && t + NS < ntiles) issue_tma(t + NS);
+            if (tid == OST_TID && t > 0) store_out(t - 1);
         }
-        if (a.final_state && !*abort_flag) {
+        // uniform decision: every chain thread takes the same branch
+        const bool aborted = named_bar_or(2, NCHAIN, *abort_flag != 0);
+        if (ntiles > 0 && !aborted) {
+            read_out(ntiles - 1);
+            named_bar_sync(2, NCHAIN);
+            if (tid == OST_TID) store_out(ntiles - 1);
+        }
+        if (tid == OST_TID) bulk_wait_all();
+        if (a.final_state && !aborted) {
 #pragma unroll
             for (int cc = 0; cc < HR; ++cc)
                 a.final_state[state_off + static_cast<size_t>(hf * HR + cc) * D + j] = S[cc];
@@ -534,15 +580,16 @@ bool make_map(CUtensorMap *m, const void *ptr, int H, int T_total, int box_d, bo
 bool prefill_tc_supported(kda_dtype dt, int dk, int dv) { return dt == KDA_BF16 && dk == D && dv == D; }
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
-    CUtensorMap tq, tk, tz, tv;
+    CUtensorMap tq, tk, tz, tv, to;
     if (!make_map(&tq, a.q, a.H, a.T_total, D, false) || !make_map(&tk, a.k, a.H, a.T_total, D, false) ||
-        !make_map(&tz, a.g, a.H, a.T_total, D, false) || !make_map(&tv, a.v, a.H, a.T_total, D, false))
+        !make_map(&tz, a.g, a.H, a.T_total, D, false) || !make_map(&tv, a.v, a.H, a.T_total, D, false) ||
+        !make_map(&to, a.out, a.H, a.T_total, D, false))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(a.N) * static_cast<unsigned>(a.H));
-    prefill_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, s>>>(tq, tk, tz, tv, a);
+    prefill_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, s>>>(tq, tk, tz, tv, to, a);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;
