@@ -24,9 +24,11 @@
 // Every tensor-core product is computed transposed so that its M side is a
 // 128-wide head dimension (tcgen05 M = 128, TMEM lane j = value channel j):
 // The chain writes the two operands it produces (the fp16 copy of S^T and
-// Vt^T) straight into tensor memory, where the MMAs read them as A.  (e) is
-// split over 4 independent accumulators (K slices 16 p .. mod 64) that the
-// chain sums, so the 8 instructions do not serialise on one accumulator.
+// Vt^T) straight into tensor memory, where the MMAs read them as A.  A
+// tcgen05.mma occupies its issuing thread for ~110 cycles whatever its N
+// (measured), while different threads' MMAs proceed concurrently; so (e) is
+// split over 4 independent accumulators (K slices p, p + 4) issued by 4
+// threads at once and summed by the chain, and (g), (h) are issued by two.
 //   (e) E[:, 0:32]   = S^T [-W ; Q e^b]^T                M128 N32  K128
 //       -> E[:, 0:16] = -(W S_0)^T, E[:, 16:32] = ((Q e^b) S_0)^T
 //   (g) E[:, 16:32] += Vt^T A^T                          M128 N16  K16
@@ -73,7 +75,7 @@ using namespace sm100;
 
 constexpr int D = 128;           // dk = dv
 constexpr int C = 16;            // tile tokens
-constexpr int NS = 3;            // ring stages
+constexpr int NS = 4;            // ring stages
 constexpr int NTHREADS = 512;
 constexpr int NPROD = 2;           // producer warpgroups
 constexpr int NCHAIN = 256;        // chain threads (two warpgroups)
@@ -185,8 +187,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             mbar_init(&bars[B_RAW + s], 1);
             mbar_init(&bars[B_FULL + s], 128);
         }
-        mbar_init(&bars[B_VT], 1);
-        mbar_init(&bars[B_UPD], 1);
+        mbar_init(&bars[B_VT], NACC);     // one commit per (e) issuer
+        mbar_init(&bars[B_UPD], 2);       // commits of the (g) and (h) issuers
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -389,26 +391,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tma_load_3d(stg + ST_Z, &tm_z, &bars[B_RAW + ss], 0, h, tok);
             tma_load_3d(stg + ST_V, &tm_v, &bars[B_RAW + ss], 0, h, tok);
         };
-        constexpr int TMA_TID = 32, OST_TID = 64;   // lane 0 of chain warps 1 and 2
+        constexpr int TMA_TID = 160, OST_TID = 192;  // lane 0 of chain warps 5 and 6
         if (tid == TMA_TID)
             for (int tt = 0; tt < NS && tt < ntiles; ++tt) issue_tma(tt);
-        // (e) for tile tt, issued by one thread once the tile's operands are ready.
-        auto issue_e = [&](int tt) -> bool {
+        // (e) for tile tt: issuer p (lane 0 of chain warp p) issues the K slices
+        // p and p + 4 into accumulator p once the tile's operands are ready.
+        auto issue_e = [&](int tt, int p) -> bool {
             const int ss = tt % NS;
             if (!mbar_wait(&bars[B_FULL + ss], (tt / NS) & 1, kWaitLimitNs)) return false;
             tc_fence_after();
             const uint32_t st = sb + ss * STAGE_BYTES;
-            const uint32_t e_acc = tmem + TM_E + E_BUF * static_cast<uint32_t>(tt & 1);
+            const uint32_t e_acc = tmem + TM_E + E_BUF * static_cast<uint32_t>(tt & 1) + 32u * p;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
+            for (int h2 = 0; h2 < D / 16 / NACC; ++h2) {
+                const int kk = p + NACC * h2;
                 const int k = kk * 16;
                 const uint32_t b_off = ST_WQ + (k >> 6) * (32 * 128) + (k & 63) * 2;
-                mma_f16kind_tmem_a(e_acc + 32u * (kk % NACC), tmem + TM_ST + 8 * kk,
-                                   smem_desc(st + b_off, 16, 1024, kLayoutSW128), id_e, kk >= NACC ? 1u : 0u);
+                mma_f16kind_tmem_a(e_acc, tmem + TM_ST + 8 * kk, smem_desc(st + b_off, 16, 1024, kLayoutSW128),
+                                   id_e, h2 > 0 ? 1u : 0u);
             }
             mma_commit(&bars[B_VT]);
             return true;
         };
+        const bool e_issuer = lane == 0 && warp < NACC;   // chain warps 0..3, lane 0
 
         float S[HR];
 #pragma unroll
@@ -425,7 +430,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         write_sT();
         tc_fence_before();
         named_bar_sync(2, NCHAIN);
-        if (tid == 0 && ntiles > 0 && !issue_e(0)) note_timeout(abort_flag);
+        if (e_issuer && ntiles > 0 && !issue_e(0, warp)) note_timeout(abort_flag);
 
         __nv_bfloat16 *gout = static_cast<__nv_bfloat16 *>(a.out);
         uint8_t *ost = base + OFF_OST;
@@ -496,13 +501,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             tc_fence_before();
             if (named_bar_or(2, NCHAIN, *abort_flag != 0)) break;   // uniform across the chain
-            if (tid == 0) {
+            if (lane == 0 && warp < 2) {
                 tc_fence_after();
                 const uint32_t stb = sb + s * STAGE_BYTES;
-                // (g) E[:,16:32] += Vt^T A^T ; (h) H = Vt^T (K e^{b_C - b})
-                mma_f16kind_tmem_a(e_acc + 16, tmem + TM_VT, smem_desc(stb + ST_AT, 128, 256, kLayoutNone), id_g, 1);
-                mma_f16kind_tmem_a(tmem + TM_H, tmem + TM_VT, smem_desc(stb + ST_KD, 2048, 1024, kLayoutSW128),
-                                   id_h, 0);
+                if (warp == 0)      // (g) E[:,16:32] += Vt^T A^T
+                    mma_f16kind_tmem_a(e_acc + 16, tmem + TM_VT, smem_desc(stb + ST_AT, 128, 256, kLayoutNone),
+                                       id_g, 1);
+                else                // (h) H = Vt^T (K e^{b_C - b})
+                    mma_f16kind_tmem_a(tmem + TM_H, tmem + TM_VT, smem_desc(stb + ST_KD, 2048, 1024, kLayoutSW128),
+                                       id_h, 0);
                 mma_commit(&bars[B_UPD]);
             }
             if (t > 0) read_out(t - 1);    // overlaps (g)/(h)
@@ -521,7 +528,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc_fence_before();
             if (named_bar_or(2, NCHAIN, *abort_flag != 0)) break;   // uniform across the chain
             // every read of this stage (TMA tiles, U, e^{b_C}, MMA operands) is done
-            if (tid == 0 && t + 1 < ntiles && !issue_e(t + 1)) note_timeout(abort_flag);
+            if (e_issuer && t + 1 < ntiles && !issue_e(t + 1, warp)) note_timeout(abort_flag);
             if (tid == TMA_TID && t + NS < ntiles) issue_tma(t + NS);
             if (tid == OST_TID && t > 0) store_out(t - 1);
         }
