@@ -102,9 +102,11 @@ constexpr int OFF_SCR = OFF_VT;                   // per-producer scratch, SCR_B
 constexpr int SC_KGM = 0;                         //   fp32 [16][PADF]: K e^b   (tf32-rounded)
 constexpr int SC_QGM = C * PADF * 4;              //   fp32 [16][PADF]: Q e^b   (tf32-rounded)
 constexpr int SC_KIM = 2 * C * PADF * 4;          //   fp32 [16][PADF]: K e^-b  (tf32-rounded)
-constexpr int SC_LS = 3 * C * PADF * 4;           //   fp32 [16][17]: L
-constexpr int SC_TBF = SC_LS + C * 17 * 4;        //   fp32 [16][TBS]: T Diag(beta) (tf32-rounded)
-constexpr int SCR_BYTES = (SC_TBF + C * TBS * 4 + 127) & ~127;
+constexpr int LSS = 20;                           //   row stride of L (16-byte aligned rows)
+constexpr int SC_LS = 3 * C * PADF * 4;           //   fp32 [16][LSS]: L
+constexpr int SC_TBF = SC_LS + C * LSS * 4;       //   fp32 [16][TBS]: T Diag(beta) (tf32-rounded)
+constexpr int SC_T11 = SC_TBF + C * TBS * 4;      //   fp32 [8][8]: lower-right block of T (solve)
+constexpr int SCR_BYTES = (SC_T11 + 64 * 4 + 127) & ~127;
 constexpr int OFF_BAR = (OFF_SCR + NPROD * SCR_BYTES + 63) & ~63;
 enum { B_RAW = 0, B_FULL = NS, B_VT = 2 * NS, B_UPD, NUM_BARS };
 constexpr int NACC = 4;          // independent accumulators of (e)
@@ -124,6 +126,10 @@ constexpr uint32_t TX_BYTES = 4 * C * D * 2;
 
 __device__ __forceinline__ float bf16_at(const uint8_t *p) {
     return __bfloat162float(__ushort_as_bfloat16(*reinterpret_cast<const uint16_t *>(p)));
+}
+// One of the two bf16 values packed in a 32-bit word (ch 0 = low half).
+__device__ __forceinline__ float bf16_half(uint32_t w, int ch) {
+    return __uint_as_float(ch ? (w & 0xffff0000u) : (w << 16));
 }
 __device__ __forceinline__ void st_h(uint8_t *p, float x) {
     *reinterpret_cast<uint16_t *>(p) = __half_as_ushort(__float2half_rn(x));
@@ -219,6 +225,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         float *kim = reinterpret_cast<float *>(scr + SC_KIM);
         float *ls = reinterpret_cast<float *>(scr + SC_LS);
         float *tbf = reinterpret_cast<float *>(scr + SC_TBF);
+        float *t11 = reinterpret_cast<float *>(scr + SC_T11);
         // beta is a strided gather (one value per token): load it a tile ahead
         // so its latency hides behind a tile of work.
         auto load_beta = [&](int tt) {
@@ -236,46 +243,67 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             bt_next = load_beta(t + NPROD);
             if (!mbar_wait(&bars[B_RAW + s], (t / NS) & 1, kWaitLimitNs)) note_timeout(abort_flag);
 
-            // Gate and decays in log2 units, branch-free: g2 = g / ln 2, the
-            // retention a_r = 2^{g2_r}; prefix products give e^{b_r}, suffix
+            // Gate and decays in log2 units, branch-free: the retention
+            // a_r = 2^{g_r / ln 2}; prefix products give e^{b_r}, suffix
             // products e^{b_C - b_r}, and e^{-b_r} = e^{b_C - b_r} / e^{b_C}.
-            float kr[C], qr[C], pre[C], suf[C];
+            // Thread (cp, hh) owns channels c0, c0 + 1 of rows 8 hh .. 8 hh + 7;
+            // the two row halves (lanes l, l ^ 16) join their products by shuffle.
+            const int cp = lane & 15, hh = lane >> 4;
+            const int c0 = 32 * pw + 2 * cp;
+            float kx[2][8], qx[2][8], pre[2][8], suf[2][8];
 #pragma unroll
-            for (int r = 0; r < C; ++r) {
-                const float m = r < nv ? 1.f : 0.f;
-                const float z = bf16_at(st + ST_Z + r * 256 + c * 2);
-                kr[r] = m * bf16_at(st + ST_K + r * 256 + c * 2);
-                qr[r] = m * bf16_at(st + ST_Q + r * 256 + c * 2);
-                const float sig = rcp_approx(1.f + ex2_approx(-kLog2e * escale * z));
-                suf[r] = ex2_approx(m * (kLog2e * a.g_min) * sig);      // retention a_r (1 past the end)
-            }
-            float run = 1.f;
+            for (int r = 0; r < 8; ++r) {
+                const int row = 8 * hh + r;
+                const float m = row < nv ? 1.f : 0.f;
+                const uint32_t zz = *reinterpret_cast<const uint32_t *>(st + ST_Z + row * 256 + c0 * 2);
+                const uint32_t kk = *reinterpret_cast<const uint32_t *>(st + ST_K + row * 256 + c0 * 2);
+                const uint32_t qq = *reinterpret_cast<const uint32_t *>(st + ST_Q + row * 256 + c0 * 2);
 #pragma unroll
-            for (int r = 0; r < C; ++r) {
-                run *= suf[r];
-                pre[r] = run;                                          // e^{b_r}
+                for (int ch = 0; ch < 2; ++ch) {
+                    const float z = bf16_half(zz, ch);
+                    kx[ch][r] = m * bf16_half(kk, ch);
+                    qx[ch][r] = m * bf16_half(qq, ch);
+                    const float sig = rcp_approx(1.f + ex2_approx(-kLog2e * escale * z));
+                    suf[ch][r] = ex2_approx(m * (kLog2e * a.g_min) * sig);   // a_r (1 past the end)
+                }
             }
-            const float gC = run;                                      // e^{b_C}
-            run = 1.f;
+            float gC[2], inv_gC[2];
 #pragma unroll
-            for (int r = C - 1; r >= 0; --r) {
-                const float a_r = suf[r];
-                suf[r] = run;                                          // e^{b_C - b_r}
-                run *= a_r;
+            for (int ch = 0; ch < 2; ++ch) {
+                float run = 1.f;
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    run *= suf[ch][r];
+                    pre[ch][r] = run;
+                }
+                const float other = __shfl_xor_sync(0xffffffffu, run, 16);   // the other half's product
+                gC[ch] = run * other;                                       // e^{b_C}
+                const float lead = hh ? other : 1.f;                        // decay before this half
+                const float tail = hh ? 1.f : other;                        // decay after this half
+                float back = tail;
+#pragma unroll
+                for (int r = 7; r >= 0; --r) {
+                    const float a_r = suf[ch][r];
+                    suf[ch][r] = back;                                      // e^{b_C - b_r}
+                    back *= a_r;
+                    pre[ch][r] *= lead;                                     // e^{b_r}
+                }
+                inv_gC[ch] = rcp_approx(gC[ch]);
             }
-            const float inv_gC = rcp_approx(gC);
-            reinterpret_cast<float *>(st + ST_GC)[c] = gC;
+            if (hh == 0) *reinterpret_cast<float2 *>(st + ST_GC + c0 * 4) = make_float2(gC[0], gC[1]);
             if (c < C) reinterpret_cast<float *>(st + ST_BETA)[c] = bt;
 #pragma unroll
-            for (int r = 0; r < C; ++r) {
-                const float kg = kr[r] * pre[r];
-                const float qg = qr[r] * pre[r];
-                const float kd = kr[r] * suf[r];
-                st_h(st + ST_WQ + off_kmajor_sw128(16 + r, c, 32), qg);
-                st_h(st + ST_KD + off_mnmajor_sw128(c, r, C), kd);
-                qgm[r * PADF + c] = to_tf32(qg);
-                kgm[r * PADF + c] = to_tf32(kg);
-                kim[r * PADF + c] = to_tf32(kd * inv_gC);
+            for (int r = 0; r < 8; ++r) {
+                const int row = 8 * hh + r;
+                const float kg0 = kx[0][r] * pre[0][r], kg1 = kx[1][r] * pre[1][r];
+                const float qg0 = qx[0][r] * pre[0][r], qg1 = qx[1][r] * pre[1][r];
+                const float kd0 = kx[0][r] * suf[0][r], kd1 = kx[1][r] * suf[1][r];
+                *reinterpret_cast<uint32_t *>(st + ST_WQ + off_kmajor_sw128(16 + row, c0, 32)) = pack_h2(qg0, qg1);
+                *reinterpret_cast<uint32_t *>(st + ST_KD + off_mnmajor_sw128(c0, row, C)) = pack_h2(kd0, kd1);
+                *reinterpret_cast<float2 *>(qgm + row * PADF + c0) = make_float2(to_tf32(qg0), to_tf32(qg1));
+                *reinterpret_cast<float2 *>(kgm + row * PADF + c0) = make_float2(to_tf32(kg0), to_tf32(kg1));
+                *reinterpret_cast<float2 *>(kim + row * PADF + c0) =
+                    make_float2(to_tf32(kd0 * inv_gC[0]), to_tf32(kd1 * inv_gC[1]));
             }
             if (named_bar_or(pbar, 128, *abort_flag != 0)) break;   // uniform across the warpgroup
 
@@ -306,26 +334,74 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     const int row = g + (e >> 1) * 8;
                     const int col = n0 + 2 * tq + (e & 1);
                     if (pw < 2)
-                        ls[row * 17 + col] = col < row ? d4[e] : 0.f;
+                        ls[row * LSS + col] = col < row ? d4[e] : 0.f;
                     else
                         st_h(st + ST_AT + off_kmajor_none(row, col, C), col <= row ? d4[e] : 0.f);
                 }
             }
             named_bar_sync(pbar, 128);
             if (pw == 0 && lane < C) {
-                // T = (I + Diag(beta) L)^-1 by forward substitution; lane s owns column s.
+                // T = (I + N)^-1, N = Diag(beta) L strictly lower, in 8x8 blocks:
+                // T00 = (I + N00)^-1 and T11 = (I + N11)^-1 by forward substitution
+                // (lanes 0-7 / 8-15 own one column each, in parallel), then
+                // T10 = -T11 N10 T00.  Stored as T Diag(beta), tf32-rounded.
                 const float *betas = reinterpret_cast<const float *>(st + ST_BETA);
-                float tcol[C];
+                const int j = lane, blk = j >> 3, r0 = 8 * blk;
+                auto row8 = [&](const float *p, float (&x)[8]) {   // 8 floats, two 16-byte loads
+                    const float4 lo = *reinterpret_cast<const float4 *>(p);
+                    const float4 hi = *reinterpret_cast<const float4 *>(p + 4);
+                    x[0] = lo.x; x[1] = lo.y; x[2] = lo.z; x[3] = lo.w;
+                    x[4] = hi.x; x[5] = hi.y; x[6] = hi.z; x[7] = hi.w;
+                };
+                float tb[8];
 #pragma unroll
-                for (int r = 0; r < C; ++r) {
+                for (int i = 0; i < 8; ++i) {
+                    const int r = r0 + i;
+                    float lr[8];
+                    row8(ls + r * LSS + r0, lr);
                     float acc = 0.f;
 #pragma unroll
-                    for (int i = 0; i < r; ++i) acc += ls[r * 17 + i] * tcol[i];
-                    tcol[r] = (r == lane ? 1.f : 0.f) - betas[r] * acc;
+                    for (int i2 = 0; i2 < i; ++i2) acc = fmaf(lr[i2], tb[i2], acc);
+                    tb[i] = (r == j ? 1.f : 0.f) - betas[r] * acc;
                 }
-                const float bs = betas[lane];
+                const float bj = betas[j];
+                if (blk == 1) {
 #pragma unroll
-                for (int r = 0; r < C; ++r) tbf[r * TBS + lane] = to_tf32(tcol[r] * bs);
+                    for (int i = 0; i < 8; ++i) {
+                        t11[i * 8 + (j - 8)] = tb[i];
+                        tbf[(8 + i) * TBS + j] = to_tf32(tb[i] * bj);
+                        tbf[i * TBS + j] = 0.f;
+                    }
+                }
+                __syncwarp(0x0000ffffu);
+                if (blk == 0) {
+                    float y[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float lr[8];
+                        row8(ls + (8 + i) * LSS, lr);
+                        float acc = 0.f;
+#pragma unroll
+                        for (int i2 = 0; i2 < 8; ++i2) acc = fmaf(lr[i2], tb[i2], acc);
+                        y[i] = betas[8 + i] * acc;
+                    }
+                    // all loads before any store (the stores may alias them)
+                    float t10[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float tr[8];
+                        row8(t11 + i * 8, tr);
+                        float acc = 0.f;
+#pragma unroll
+                        for (int m2 = 0; m2 < 8; ++m2) acc = fmaf(tr[m2], y[m2], acc);
+                        t10[i] = acc;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        tbf[(8 + i) * TBS + j] = to_tf32(-t10[i] * bj);
+                        tbf[i * TBS + j] = to_tf32(tb[i] * bj);
+                    }
+                }
             }
             named_bar_sync(pbar, 128);
             // W = T Diag(beta) (K e^b) -> rows 0..15 of the (e) B operand hold -W;
@@ -343,10 +419,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     ta[ks][3] = __float_as_uint(tbf[(g + 8) * TBS + k0 + tq + 4]);
                 }
                 float *u = reinterpret_cast<float *>(st + ST_U);
+                // all fragment loads and MMAs first, then the stores (which may alias)
+                float dw[4][4], du[4][4];
 #pragma unroll
                 for (int nb = 0; nb < 4; ++nb) {
                     const int cn = pw * 32 + nb * 8 + g;          // B-fragment column (channel)
-                    float dw[4] = {0.f, 0.f, 0.f, 0.f}, du[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) dw[nb][e] = du[nb][e] = 0.f;
 #pragma unroll
                     for (int ks = 0; ks < 2; ++ks) {
                         const int s0 = ks * 8 + tq;
@@ -354,17 +433,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         const uint32_t bw1 = __float_as_uint(kgm[(s0 + 4) * PADF + cn]);
                         const uint32_t bu0 = __float_as_uint(bf16_at(st + ST_V + s0 * 256 + cn * 2));
                         const uint32_t bu1 = __float_as_uint(bf16_at(st + ST_V + (s0 + 4) * 256 + cn * 2));
-                        mma_1688_tf32(dw, ta[ks][0], ta[ks][1], ta[ks][2], ta[ks][3], bw0, bw1);
-                        mma_1688_tf32(du, ta[ks][0], ta[ks][1], ta[ks][2], ta[ks][3], bu0, bu1);
+                        mma_1688_tf32(dw[nb], ta[ks][0], ta[ks][1], ta[ks][2], ta[ks][3], bw0, bw1);
+                        mma_1688_tf32(du[nb], ta[ks][0], ta[ks][1], ta[ks][2], ta[ks][3], bu0, bu1);
                     }
-                    const int c0 = pw * 32 + nb * 8 + 2 * tq;
+                }
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int row = g + (e >> 1) * 8;
-                        st_h(st + ST_WQ + off_kmajor_sw128(row, c0 + (e & 1), 32), -dw[e]);
-                    }
-                    *reinterpret_cast<float2 *>(u + g * D + c0) = make_float2(du[0], du[1]);
-                    *reinterpret_cast<float2 *>(u + (g + 8) * D + c0) = make_float2(du[2], du[3]);
+                for (int nb = 0; nb < 4; ++nb) {
+                    const int c0 = pw * 32 + nb * 8 + 2 * tq;
+                    *reinterpret_cast<uint32_t *>(st + ST_WQ + off_kmajor_sw128(g, c0, 32)) =
+                        pack_h2(-dw[nb][0], -dw[nb][1]);
+                    *reinterpret_cast<uint32_t *>(st + ST_WQ + off_kmajor_sw128(g + 8, c0, 32)) =
+                        pack_h2(-dw[nb][2], -dw[nb][3]);
+                    *reinterpret_cast<float2 *>(u + g * D + c0) = make_float2(du[nb][0], du[nb][1]);
+                    *reinterpret_cast<float2 *>(u + (g + 8) * D + c0) = make_float2(du[nb][2], du[nb][3]);
                 }
             }
             fence_proxy_async_smem();
@@ -520,9 +601,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             for (int cb = 0; cb < HR / 16; ++cb) {
                 float inc[16];
                 tmem_ld16(tmem + TM_H + lane_base + hf * HR + cb * 16, inc);
+                float gv[16];   // e^{b_C}: the same 16 values for the whole warp, four 16-byte loads
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const float4 g4 = *reinterpret_cast<const float4 *>(gc + cb * 16 + q4 * 4);
+                    gv[q4 * 4 + 0] = g4.x; gv[q4 * 4 + 1] = g4.y; gv[q4 * 4 + 2] = g4.z; gv[q4 * 4 + 3] = g4.w;
+                }
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) S[cb * 16 + i] = fmaf(gc[cb * 16 + i], S[cb * 16 + i], inc[i]);
+                for (int i = 0; i < 16; ++i) S[cb * 16 + i] = fmaf(gv[i], S[cb * 16 + i], inc[i]);
             }
             write_sT();
             tc_fence_before();
