@@ -11,6 +11,10 @@ prefill inputs, 1.6 GB of decode state), so no L2 flush is needed.
 value      : prefill tokens/s (token positions, all 96 heads each), timed over
              the prefill launches with CUDA events on the launching stream.
 decode     : state GB/s of the decode step (2 * N*H*dk*dv*4 bytes per step).
+spec_replay: speculative replay (kda_decode_steps) of 256 sequences x 8
+             verified tokens with 1..8 accepted, timed after the main region:
+             algorithmic GB/s (state once in and out + the applied tokens'
+             inputs and outputs) and applied tokens/s.
 roofline   : the dominant kernel's algorithmic bytes / launch time vs the
              measured HBM copy bandwidth.
 e2e        : prefill tokens/s through the same API with pinned host buffers:
@@ -45,6 +49,7 @@ from gated_delta_rule_11_gb300 import inputs as kin  # noqa: E402
 METRIC = "KDA prefill tokens/s (H=96,d=128) + % TC peak; decode step state GB/s vs HBM"
 PREFILL = kin.WORKLOADS["varlen_bf16_H96_237568"]
 DECODE = kin.WORKLOADS["decode_bf16_N256_H96"]
+SPEC = kin.WORKLOADS["spec_bf16_N256_H96_K8"]
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # Algorithmic work per token and head, d = dk = dv = 128, 16-token tiles:
@@ -66,7 +71,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
-    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "spec"], default="all",
                     help="run one leg only (for profiling captures; the JSON line needs 'all')")
     ap.add_argument("--prefill-workload", default="varlen_bf16_H96_237568",
                     choices=[k for k, w in kin.WORKLOADS.items() if w.kind == "prefill" and w.dtype == "bf16"],
@@ -272,11 +277,17 @@ def run_single_leg(args, kda, dev):
         a = [inp[n] for n in ("q", "k", "v", "g_raw", "beta")]
         out, fin = kda.kda_chunk_fwd(*a, inp["init_state"], inp["cu_seqlens"])
         fn = lambda i: kda.kda_chunk_fwd(*a, inp["init_state"], inp["cu_seqlens"], out=out, final_state=fin)
-    else:
+    elif args.only == "decode":
         w = DECODE
         S = kin.make_decode_state(w, device=dev)
         t = kin.make_decode_token(w, 0, device=dev)
         fn = lambda i: kda.kda_decode_step(t["q"], t["k"], t["v"], t["g_raw"], t["beta"], S)
+    else:
+        w = SPEC
+        S = kin.make_decode_state(w, device=dev)
+        t = kin.make_decode_drafts(w, 0, device=dev)
+        fn = lambda i: kda.kda_decode_steps(t["q"], t["k"], t["v"], t["g_raw"], t["beta"], S,
+                                            t["accepted"])
     for i in range(args.warmup):
         fn(i)
     torch.cuda.synchronize()
@@ -385,6 +396,8 @@ def run_ours(args, rank, world, local):
     p_traffic = recorded_traffic("prefill", prefill_src)
     d_traffic = recorded_traffic("decode", decode_src)
 
+    spec = run_spec(kda, dev, rank, world, args.steps, args.warmup, hbm_peak, peak_src)
+
     e2e = None
     if not args.no_e2e:   # every rank: the timing is reduced over ranks
         e2e = run_e2e(kda, q, k, v, g, b, cu, out, fin, args.e2e_steps, world, T_total)
@@ -423,11 +436,49 @@ def run_ours(args, rank, world, local):
                    "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": d_gbs,
                                 "peak": hbm_peak, "unit": "GB/s", "frac": d_gbs / hbm_peak,
                                 "traffic": d_traffic, "peak_source": peak_src}},
+        "spec_replay": spec,
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches,
         "clocks": clocks, "wall_s_timed": t_wall,
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def run_spec(kda, dev, rank, world, steps, warmup, hbm_peak, peak_src):
+    """Speculative replay on the spec workload: `steps` launches, each with its
+    own drafts and accepted counts (a few batches cycled), the state carried
+    from launch to launch.  Returns the report object."""
+    w = SPEC
+    S = kin.make_decode_state(w, device=dev, seed=w.seed + 1000 * rank)
+    batches = [kin.make_decode_drafts(w, i, device=dev, seed=w.seed + 1000 * rank) for i in range(4)]
+    out = torch.empty((w.N, w.drafts, w.H, w.dv), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fn(i):
+        t = batches[i % len(batches)]
+        kda.kda_decode_steps(t["q"], t["k"], t["v"], t["g_raw"], t["beta"], S, t["accepted"],
+                             out=out)
+
+    for i in range(warmup):
+        fn(i)
+    barrier(world)
+    torch.cuda.synchronize()
+    evs = time_region(fn, steps, stream)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    applied = [int(batches[i % len(batches)]["accepted"].sum()) for i in range(steps)]
+    mean_ms = reduce_max(statistics.fmean(ms), world)
+    state_bytes = 2 * w.N * w.H * w.dk * w.dv * 4
+    tok_bytes = w.H * (3 * w.dk * 2 + w.dv * 2 + 2 + w.dv * 2)   # q, k, g_raw, v, beta in; out
+    mean_applied = statistics.fmean(applied)
+    alg = state_bytes + mean_applied * tok_bytes
+    gbs = alg / (mean_ms * 1e-3) / 1e9
+    return {"workload": w.name, "N": w.N, "K": w.drafts, "H": w.H,
+            "mean_accepted_per_seq": mean_applied / w.N, "ms": mean_ms,
+            "applied_tokens_per_s": mean_applied * world / (mean_ms * 1e-3),
+            "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": gbs,
+                         "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                         "algorithmic_bytes_per_launch": alg, "peak_source": peak_src}}
 
 
 def run_e2e(kda, q, k, v, g, b, cu, out, fin, steps, world, T_total):

@@ -74,13 +74,32 @@ kda_status kda_check_device_status(void) {
     return kda::take_tc_timeouts() ? KDA_ERR_TIMEOUT : KDA_OK;
 }
 
-kda_status kda_chunk_fwd(kda_dtype dt, int B, int T, int H, int dk, int dv,
-                         const void *q, const void *k, const void *v,
-                         const void *g_raw, const void *beta,
-                         const float *init_state,
-                         const int32_t *cu_seqlens, int N,
-                         void *out, float *final_state,
-                         const kda_params *p, kda_stream_t stream) {
+long long kda_checkpoint_rows(int B, int T, const int32_t *cu_seqlens_host, int N,
+                              int checkpoint_every) {
+    if (checkpoint_every <= 0 || checkpoint_every % 16 != 0 || B < 0 || T < 0 || N < 0) return -1;
+    if (!cu_seqlens_host) {
+        if (N != B) return -1;
+        return static_cast<long long>(B) * (T / checkpoint_every);
+    }
+    if (B != 1 || N < 1) return -1;
+    long long rows = 0;
+    for (int n = 0; n < N; ++n) {
+        const long long len = static_cast<long long>(cu_seqlens_host[n + 1]) - cu_seqlens_host[n];
+        if (len < 0 || cu_seqlens_host[n] < 0 || cu_seqlens_host[n + 1] > T) return -1;
+        rows += len / checkpoint_every;
+    }
+    return rows;
+}
+
+kda_status kda_chunk_fwd_checkpointed(kda_dtype dt, int B, int T, int H, int dk, int dv,
+                                      const void *q, const void *k, const void *v,
+                                      const void *g_raw, const void *beta,
+                                      const float *init_state,
+                                      const int32_t *cu_seqlens, int N,
+                                      void *out, float *final_state,
+                                      int checkpoint_every, float *checkpoints,
+                                      long long checkpoint_rows,
+                                      const kda_params *p, kda_stream_t stream) {
     if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_DTYPE;
     if (B < 0 || T < 0 || H <= 0 || N < 0) return KDA_ERR_ARG;
     if (!head_dim_ok(dk) || !head_dim_ok(dv)) return KDA_ERR_SHAPE;
@@ -89,10 +108,12 @@ kda_status kda_chunk_fwd(kda_dtype dt, int B, int T, int H, int dk, int dv,
     } else if (N != B) {
         return KDA_ERR_ARG;
     }
+    if (checkpoints && (checkpoint_every <= 0 || checkpoint_every % 16 != 0 || checkpoint_rows < 0))
+        return KDA_ERR_ARG;
     const long long total = static_cast<long long>(B) * T;
     if (total > INT32_MAX || static_cast<long long>(N) * H > INT32_MAX) return KDA_ERR_ARG;
     if (total > 0 && (!q || !k || !v || !g_raw || !beta || !out)) return KDA_ERR_ARG;
-    const void *ptrs[] = {q, k, v, g_raw, init_state, out, final_state};
+    const void *ptrs[] = {q, k, v, g_raw, init_state, out, final_state, checkpoints};
     for (const void *ptr : ptrs)
         if (ptr && !aligned16(ptr)) return KDA_ERR_ALIGN;
     if (!aligned_to(beta, dt == KDA_F32 ? 4 : 2) || !aligned_to(cu_seqlens, 4)) return KDA_ERR_ALIGN;
@@ -104,6 +125,10 @@ kda_status kda_chunk_fwd(kda_dtype dt, int B, int T, int H, int dk, int dv,
     a.cu_seqlens = cu_seqlens;
     a.out = out;
     a.final_state = final_state;
+    const bool ck = checkpoints && checkpoint_rows > 0;
+    a.ckpt = ck ? checkpoints : nullptr;
+    a.ckpt_rows = ck ? checkpoint_rows : 0;
+    a.ckpt_every = ck ? checkpoint_every : 0;
     resolve_params(p, a.g_min, a.A_log, a.scale);
     if (a.A_log && !aligned_to(a.A_log, 4)) return KDA_ERR_ALIGN;
     a.N = N;
@@ -116,31 +141,53 @@ kda_status kda_chunk_fwd(kda_dtype dt, int B, int T, int H, int dk, int dv,
     return from_cuda(kda::launch_prefill_simt(dt, dk, dv, a, s));
 }
 
-kda_status kda_decode_step(kda_dtype dt, int N, int H, int dk, int dv,
-                           const void *q, const void *k, const void *v,
-                           const void *g_raw, const void *beta,
-                           float *state, void *out,
-                           const kda_params *p, kda_stream_t stream) {
+kda_status kda_chunk_fwd(kda_dtype dt, int B, int T, int H, int dk, int dv,
+                         const void *q, const void *k, const void *v,
+                         const void *g_raw, const void *beta,
+                         const float *init_state,
+                         const int32_t *cu_seqlens, int N,
+                         void *out, float *final_state,
+                         const kda_params *p, kda_stream_t stream) {
+    return kda_chunk_fwd_checkpointed(dt, B, T, H, dk, dv, q, k, v, g_raw, beta, init_state,
+                                      cu_seqlens, N, out, final_state, 0, nullptr, 0, p, stream);
+}
+
+kda_status kda_decode_steps(kda_dtype dt, int N, int K, int H, int dk, int dv,
+                            const void *q, const void *k, const void *v,
+                            const void *g_raw, const void *beta, const int32_t *accepted,
+                            float *state, void *out,
+                            const kda_params *p, kda_stream_t stream) {
     if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_DTYPE;
-    if (N < 0 || H <= 0) return KDA_ERR_ARG;
+    if (N < 0 || K < 1 || H <= 0) return KDA_ERR_ARG;
     if (!head_dim_ok(dk) || !head_dim_ok(dv)) return KDA_ERR_SHAPE;
-    if (static_cast<long long>(N) * H > INT32_MAX) return KDA_ERR_ARG;
+    if (static_cast<long long>(N) * H > INT32_MAX || static_cast<long long>(N) * K * H > INT32_MAX)
+        return KDA_ERR_ARG;
     if (N == 0) return KDA_OK;
     if (!q || !k || !v || !g_raw || !beta || !state || !out) return KDA_ERR_ARG;
     const void *ptrs[] = {q, k, v, g_raw, state, out};
     for (const void *ptr : ptrs)
         if (!aligned16(ptr)) return KDA_ERR_ALIGN;
-    if (!aligned_to(beta, dt == KDA_F32 ? 4 : 2)) return KDA_ERR_ALIGN;
+    if (!aligned_to(beta, dt == KDA_F32 ? 4 : 2) || !aligned_to(accepted, 4)) return KDA_ERR_ALIGN;
     kda::DecodeArgs a;
     a.q = q; a.k = k; a.v = v; a.g = g_raw; a.beta = beta;
+    a.accepted = accepted;
     a.state = state;
     a.out = out;
     resolve_params(p, a.g_min, a.A_log, a.scale);
     if (a.A_log && !aligned_to(a.A_log, 4)) return KDA_ERR_ALIGN;
     a.N = N;
+    a.K = K;
     a.H = H;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return from_cuda(kda::launch_decode(dt, dk, dv, a, s));
+}
+
+kda_status kda_decode_step(kda_dtype dt, int N, int H, int dk, int dv,
+                           const void *q, const void *k, const void *v,
+                           const void *g_raw, const void *beta,
+                           float *state, void *out,
+                           const kda_params *p, kda_stream_t stream) {
+    return kda_decode_steps(dt, N, 1, H, dk, dv, q, k, v, g_raw, beta, nullptr, state, out, p, stream);
 }
 
 }  // extern "C"

@@ -1,32 +1,72 @@
-// Single-token KDA step ("a third kernel": decode), one CTA per (sequence,
-// head).  The fp32 state S [dk, dv] (row = key channel c, column = value
-// channel j) is streamed from HBM once and written back once, in place.
+// KDA decode: each (sequence, head) advances by the first `accepted` of K
+// drafted tokens in one pass over its state (K = 1, all accepted: the plain
+// single-token step, "a third kernel" of "Kimi K3: Two point eight trillion
+// parameters, open weights, and forty-seven pages of how", §The machine
+// underneath).  Replaying only the accepted prefix of speculative drafts on
+// chip, with no per-draft state copy, is the scheme of that section and of
+// "Kimi K3：从三条信息流到完整系统", §recurrent speculative decoding 不能复制整个状态.
+// One CTA per (sequence, head); the fp32 state S [dk, dv] (row = key channel
+// c, column = value channel j) is read from HBM once, kept in registers
+// across the tokens, and written back once, in place.
 //
 // Recurrence: "Kimi K3：从三条信息流到完整系统", §KDA 是带逐通道遗忘的 delta
-// rule, eq. (1) in its expanded form.  With D = Diag(alpha) S:
+// rule, eq. (1) in its expanded form.  Per token, with D = Diag(alpha) S:
 //     a_j = sum_c alpha_c k_c S_cj      (= (D^T k)_j)
 //     b_j = sum_c alpha_c q_c S_cj      (= (D^T q)_j)
 //     u_j = beta (v_j - a_j)
 //     S'_cj = alpha_c S_cj + k_c u_j
 //     o_j = scale * (S'^T q)_j = scale * (b_j + (k.q) u_j)
-// so both reductions happen in the single read pass, and the write pass
-// needs only u.  alpha follows eq. (5) of §下界 log-decay 是一个 kernel 设计.
+// so both reductions happen in a single pass over the state.  alpha follows
+// eq. (5) of §下界 log-decay 是一个 kernel 设计.
 //
-// Layout of the work: 256 threads; a row of S is dv/4 float4s; thread t
-// owns float4 column (t % (dv/4)) of rows (t / (dv/4)) + m * rows_per_pass,
-// holding its whole slice in registers between the two passes.
+// Layout of the work: 256 threads = 8 warps; warp w owns the column slab
+// [w dv/8, (w+1) dv/8) of every row, as CG = dv/32 float4 column groups x
+// RG = 32/CG row groups (lane = rg * CG + cg; rows rg + m RG).  Both
+// reductions over c then stay inside the warp (shuffles), so applying a token
+// needs no block barrier.  The per-token channel vectors (alpha k, alpha q)
+// and (alpha, k), v, beta and k.q are computed for a block of up to 8 tokens at
+// once into shared memory, with their loads in flight beside the state's.
 #include "kda_internal.cuh"
 
 namespace kda {
 namespace {
 
 constexpr int kDecodeThreads = 256;
+constexpr int kTokBlock = 8;                         // tokens prepared per barrier
 
 __device__ __forceinline__ float4 ld_stream(const float4 *p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(float4 *p, float4 v) { __stcs(p, v); }
 
+// Packed two-lane fp32 arithmetic on 64-bit register pairs (fma.rn.f32x2 /
+// mul.rn.f32x2): each lane rounds exactly like fmaf / __fmul_rn, at half the
+// instruction count.  A pair (lo, hi) is kept as one 64-bit value.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 unpack2(f32x2 r) {
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+__device__ __forceinline__ f32x2 ffma2(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f32x2 fmul2(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Single-token step with whole rows per warp (a warp instruction touches one
+// 512-byte row of S): rows row0 + m * RPP per thread, the reductions over c
+// combined across warps through shared memory.  K = 1, every token applied.
 template <typename Tin, int DK, int DV>
-__global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kDecodeThreads, 2) decode1_kernel(DecodeArgs a) {
     constexpr int V4 = DV / 4;                       // float4 per state row
     constexpr int RPP = kDecodeThreads / V4;         // rows per pass
     constexpr int PASSES = DK / RPP;
@@ -45,8 +85,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(DecodeArgs a)
     const int row0 = tid / V4;
 
     float4 *S = reinterpret_cast<float4 *>(a.state) + static_cast<size_t>(nh) * (DK * V4);
-
-    // Issue the state loads first: they dominate the kernel's time.
     float4 st[PASSES];
 #pragma unroll
     for (int m = 0; m < PASSES; ++m) st[m] = ld_stream(S + (row0 + m * RPP) * V4 + col4);
@@ -73,14 +111,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(DecodeArgs a)
     if (tid < DV) s_v[tid] = ld_in(v + tid);
     __syncthreads();
 
-    // Pass 1 (in registers): partial a_j and b_j over this thread's rows.
     float4 pa = make_float4(0.f, 0.f, 0.f, 0.f), pb = pa;
 #pragma unroll
     for (int m = 0; m < PASSES; ++m) {
         const int c = row0 + m * RPP;
         const float ak = s_ak[c], aq = s_aq[c];
-        pa.x += ak * st[m].x; pa.y += ak * st[m].y; pa.z += ak * st[m].z; pa.w += ak * st[m].w;
-        pb.x += aq * st[m].x; pb.y += aq * st[m].y; pb.z += aq * st[m].z; pb.w += aq * st[m].w;
+        pa.x = fmaf(ak, st[m].x, pa.x); pa.y = fmaf(ak, st[m].y, pa.y);
+        pa.z = fmaf(ak, st[m].z, pa.z); pa.w = fmaf(ak, st[m].w, pa.w);
+        pb.x = fmaf(aq, st[m].x, pb.x); pb.y = fmaf(aq, st[m].y, pb.y);
+        pb.z = fmaf(aq, st[m].z, pb.z); pb.w = fmaf(aq, st[m].w, pb.w);
     }
     *reinterpret_cast<float4 *>(&s_red[0][row0][col4 * 4]) = pa;
     *reinterpret_cast<float4 *>(&s_red[1][row0][col4 * 4]) = pb;
@@ -99,22 +138,164 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(DecodeArgs a)
         const float u = beta * (s_v[tid] - av);
         s_u[tid] = u;
         Tin *o = static_cast<Tin *>(a.out) + static_cast<size_t>(nh) * DV;
-        st_out(o + tid, a.scale * (bv + kq * u));
+        st_out(o + tid, a.scale * fmaf(kq, u, bv));
     }
     __syncthreads();
 
-    // Pass 2: S' = Diag(alpha) S + k u^T, written in place.
     const float4 u4 = *reinterpret_cast<const float4 *>(&s_u[col4 * 4]);
 #pragma unroll
     for (int m = 0; m < PASSES; ++m) {
         const int c = row0 + m * RPP;
         const float al = s_alpha[c], kc = s_k[c];
         float4 r;
-        r.x = al * st[m].x + kc * u4.x;
-        r.y = al * st[m].y + kc * u4.y;
-        r.z = al * st[m].z + kc * u4.z;
-        r.w = al * st[m].w + kc * u4.w;
+        r.x = fmaf(al, st[m].x, kc * u4.x); r.y = fmaf(al, st[m].y, kc * u4.y);
+        r.z = fmaf(al, st[m].z, kc * u4.z); r.w = fmaf(al, st[m].w, kc * u4.w);
         st_stream(S + c * V4 + col4, r);
+    }
+}
+
+template <int DK, int DV>
+struct DecodeSmem {
+    ulonglong2 akq[kTokBlock][DK];     // pairs (alpha k, alpha k), (alpha q, alpha q) per token and channel
+    ulonglong2 alk[kTokBlock][DK];     // pairs (alpha, alpha), (k, k)
+    float red[2][kDecodeThreads / (DV / 4)][DV];      // [a|b][row group][column]
+    float4 u[DV / 4];
+    float v[kTokBlock][DV];
+    float kq[kTokBlock][DK / 32];      // per-warp partial sums of k.q
+    float beta[kTokBlock];
+};
+
+// State load that the compiler may neither drop nor move below a branch:
+// the loads are issued before the accepted count is known.
+__device__ __forceinline__ float4 ld_state(const float4 *p) {
+    float4 v;
+    asm volatile("ld.global.cs.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+
+// Multi-token replay, same row layout as the single step: RPP row groups x
+// V4 float4 columns; thread (rg, c4) holds rows rg + m RPP of column c4.  Per
+// token: in-thread partial sums over its rows; barrier; dv threads add the
+// RPP partials of one column each, form u_j and o_j; barrier; every thread
+// applies u to its rows.  The second barrier also orders the partials' reads
+// before the next token's writes, so one buffer serves all tokens.
+template <typename Tin, int DK, int DV>
+__global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(DecodeArgs a) {
+    constexpr int V4 = DV / 4;                       // float4 per state row
+    constexpr int RPP = kDecodeThreads / V4;         // row groups
+    constexpr int RPL = DK / RPP;                    // rows per thread
+    static_assert(RPL >= 1 && DK % RPP == 0, "tiling");
+
+    __shared__ __align__(16) DecodeSmem<DK, DV> sm;
+
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int c4 = tid % V4, rg = tid / V4;
+    const int nh = blockIdx.x;                       // n * H + h
+    const int n = nh / a.H, h = nh % a.H;
+
+    const int acc_raw = a.accepted ? __ldg(a.accepted + n) : a.K;
+    // Issue the state loads first: they dominate the kernel's time.
+    float4 *S = reinterpret_cast<float4 *>(a.state) + static_cast<size_t>(nh) * (DK * V4);
+    f32x2 st[RPL][2];
+#pragma unroll
+    for (int m = 0; m < RPL; ++m) {
+        const float4 x = ld_state(S + (rg + m * RPP) * V4 + c4);
+        st[m][0] = pack2(x.x, x.y);
+        st[m][1] = pack2(x.z, x.w);
+    }
+
+    const float escale = a.A_log ? expf(__ldg(a.A_log + h)) : 1.0f;
+    const size_t tok_k = static_cast<size_t>(a.H) * DK, tok_v = static_cast<size_t>(a.H) * DV;
+    const Tin *gq = static_cast<const Tin *>(a.q);
+    const Tin *gk = static_cast<const Tin *>(a.k);
+    const Tin *gz = static_cast<const Tin *>(a.g);
+    const Tin *gv = static_cast<const Tin *>(a.v);
+    const Tin *gb = static_cast<const Tin *>(a.beta);
+    Tin *go = static_cast<Tin *>(a.out);
+
+    // Per-token vectors of tokens [i0, i0 + nb) (a warp's 32 channels share a token).
+    auto prepare = [&](int i0, int nb) {
+#pragma unroll 1
+        for (int idx = tid; idx < nb * DK; idx += kDecodeThreads) {
+            const int i = idx / DK, c = idx % DK;
+            const size_t o = (static_cast<size_t>(n) * a.K + i0 + i) * tok_k + static_cast<size_t>(h) * DK + c;
+            const float kc = ld_in(gk + o), qc = ld_in(gq + o), zc = ld_in(gz + o);
+            const float alpha = expf(log_decay(zc, escale, a.g_min));
+            sm.akq[i][c] = make_ulonglong2(pack2(alpha * kc, alpha * kc), pack2(alpha * qc, alpha * qc));
+            sm.alk[i][c] = make_ulonglong2(pack2(alpha, alpha), pack2(kc, kc));
+            float kq = kc * qc;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+            if (lane == 0) sm.kq[i][c / 32] = kq;
+        }
+        for (int idx = tid; idx < nb * DV; idx += kDecodeThreads)
+            sm.v[idx / DV][idx % DV] =
+                ld_in(gv + (static_cast<size_t>(n) * a.K + i0 + idx / DV) * tok_v + static_cast<size_t>(h) * DV + idx % DV);
+        if (tid < nb) sm.beta[tid] = ld_in(gb + (static_cast<size_t>(n) * a.K + i0 + tid) * a.H + h);
+    };
+    // The first block is prepared for every drafted token, before the accepted
+    // count is used, so its loads overlap the state's.
+    prepare(0, min(kTokBlock, a.K));
+    __syncthreads();
+    const int n_acc = min(max(acc_raw, 0), a.K);
+    if (n_acc == 0) return;                          // state and outputs untouched
+
+#pragma unroll 1
+    for (int i0 = 0; i0 < n_acc; i0 += kTokBlock) {
+        const int nb = min(kTokBlock, n_acc - i0);
+        if (i0 > 0) {
+            __syncthreads();                         // previous block's vectors are consumed
+            prepare(i0, nb);
+            __syncthreads();
+        }
+#pragma unroll 1
+        for (int i = 0; i < nb; ++i) {
+            // partial a_j = sum_c alpha_c k_c S_cj and b_j = sum_c alpha_c q_c S_cj over this thread's rows
+            f32x2 pa0 = 0ull, pa1 = 0ull, pb0 = 0ull, pb1 = 0ull;     // +0.0f in both lanes
+#pragma unroll
+            for (int m = 0; m < RPL; ++m) {
+                const ulonglong2 ch = sm.akq[i][rg + m * RPP];
+                pa0 = ffma2(ch.x, st[m][0], pa0); pa1 = ffma2(ch.x, st[m][1], pa1);
+                pb0 = ffma2(ch.y, st[m][0], pb0); pb1 = ffma2(ch.y, st[m][1], pb1);
+            }
+            {
+                const float2 a0 = unpack2(pa0), a1 = unpack2(pa1), b0 = unpack2(pb0), b1 = unpack2(pb1);
+                *reinterpret_cast<float4 *>(&sm.red[0][rg][4 * c4]) = make_float4(a0.x, a0.y, a1.x, a1.y);
+                *reinterpret_cast<float4 *>(&sm.red[1][rg][4 * c4]) = make_float4(b0.x, b0.y, b1.x, b1.y);
+            }
+            __syncthreads();
+            if (tid < DV) {
+                float av = 0.f, bv = 0.f;
+#pragma unroll
+                for (int r = 0; r < RPP; ++r) {
+                    av += sm.red[0][r][tid];
+                    bv += sm.red[1][r][tid];
+                }
+                float kq = 0.f;
+#pragma unroll
+                for (int w = 0; w < DK / 32; ++w) kq += sm.kq[i][w];
+                const float u = sm.beta[i] * (sm.v[i][tid] - av);
+                reinterpret_cast<float *>(sm.u)[tid] = u;
+                st_out(go + (static_cast<size_t>(n) * a.K + i0 + i) * tok_v + static_cast<size_t>(h) * DV + tid,
+                       a.scale * fmaf(kq, u, bv));
+            }
+            __syncthreads();
+            // S = Diag(alpha) S + k u^T
+            const float4 u = sm.u[c4];
+            const f32x2 u0 = pack2(u.x, u.y), u1 = pack2(u.z, u.w);
+#pragma unroll
+            for (int m = 0; m < RPL; ++m) {
+                const ulonglong2 ch = sm.alk[i][rg + m * RPP];
+                st[m][0] = ffma2(ch.x, st[m][0], fmul2(ch.y, u0));
+                st[m][1] = ffma2(ch.x, st[m][1], fmul2(ch.y, u1));
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < RPL; ++m) {
+        const float2 x = unpack2(st[m][0]), y = unpack2(st[m][1]);
+        st_stream(S + (rg + m * RPP) * V4 + c4, make_float4(x.x, x.y, y.x, y.y));
     }
 }
 
@@ -122,9 +303,11 @@ template <typename Tin>
 cudaError_t launch_t(int dk, int dv, const DecodeArgs &a, cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>(a.N) * static_cast<unsigned>(a.H));
     const dim3 block(kDecodeThreads);
+    const bool single = a.K == 1 && !a.accepted;
 #define KDA_DEC_CASE(DK_, DV_)                                            \
     if (dk == DK_ && dv == DV_) {                                         \
-        decode_kernel<Tin, DK_, DV_><<<grid, block, 0, s>>>(a);           \
+        if (single) decode1_kernel<Tin, DK_, DV_><<<grid, block, 0, s>>>(a); \
+        else decode_kernel<Tin, DK_, DV_><<<grid, block, 0, s>>>(a);      \
         const cudaError_t e = cudaGetLastError();                         \
         if (e == cudaSuccess) count_launches(1);                          \
         return e;                                                         \

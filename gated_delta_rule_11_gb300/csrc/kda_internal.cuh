@@ -22,14 +22,23 @@ struct PrefillArgs {
     const float *A_log;         // device [H] or nullptr
     int N, H, T_total, T_seq;
     float g_min, scale;
+    // State checkpoints: every ckpt_every tokens of each sequence (a multiple
+    // of 16; 0 = none) into ckpt [ckpt_rows, H, dk, dv]; rows at or past
+    // ckpt_rows are never written.
+    float *ckpt;
+    long long ckpt_rows;
+    int ckpt_every;
 };
 
+// Decode: q, k, g_raw [N, K, H, dk]; v, out [N, K, H, dv]; beta [N, K, H];
+// sequence n applies its first accepted[n] tokens (all K when accepted is null).
 struct DecodeArgs {
     const void *q, *k, *v, *g, *beta;
+    const int32_t *accepted;
     float *state;
     void *out;
     const float *A_log;
-    int N, H;
+    int N, K, H;
     float g_min, scale;
 };
 
@@ -69,6 +78,32 @@ __device__ __forceinline__ void seq_span(const PrefillArgs &a, int n, int &bos, 
         bos = n * a.T_seq;
         eos = bos + a.T_seq;
     }
+}
+
+// Row of sequence n's first checkpoint: the checkpoints of sequences 0..n-1
+// (floor(length / ckpt_every) each).  Called by whole warps.
+__device__ __forceinline__ long long ckpt_first_row(const PrefillArgs &a, int n) {
+    if (!a.cu_seqlens) return static_cast<long long>(n) * (a.T_seq / a.ckpt_every);
+    long long cnt = 0;
+    for (int m = threadIdx.x & 31; m < n; m += 32) {
+        int b, e;
+        seq_span(a, m, b, e);
+        cnt += (e - b) / a.ckpt_every;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    return cnt;
+}
+
+// Checkpoint slot after `done` tokens of a sequence whose first checkpoint
+// row is `row0`, or nullptr when no checkpoint falls there or the row is past
+// the buffer.
+__device__ __forceinline__ float *ckpt_slot(const PrefillArgs &a, long long row0, int done, int h,
+                                            size_t state_elems) {
+    if (!a.ckpt || done <= 0 || done % a.ckpt_every != 0) return nullptr;
+    const long long row = row0 + done / a.ckpt_every - 1;
+    if (row >= a.ckpt_rows) return nullptr;
+    return a.ckpt + (static_cast<size_t>(row) * a.H + h) * state_elems;
 }
 
 // Record n successfully enqueued kernels (backs kda_launch_count).

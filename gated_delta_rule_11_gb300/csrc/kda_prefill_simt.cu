@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
         sm.S[c][j] = a.init_state ? a.init_state[state_off + static_cast<size_t>(c) * DV + j0 + j] : 0.f;
     }
 
+    const long long ck_row0 = a.ckpt ? ckpt_first_row(a, n) : 0;
     for (int t0 = bos; t0 < eos; t0 += C) {
         const int nv = min(C, eos - t0);
         __syncthreads();  // previous tile is done with shared memory
@@ -196,6 +197,13 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
 #pragma unroll
             for (int r = 0; r < C; ++r) acc += sm.kdec[r][c] * vt[r];
             sm.S[c][j] = acc;
+        }
+        if (float *cp = ckpt_slot(a, ck_row0, t0 + nv - bos, h, static_cast<size_t>(DK) * DV)) {
+            __syncthreads();   // uniform: every thread sees the same slot
+            for (int idx = tid; idx < DK * BV; idx += NT) {
+                const int c = idx / BV, jj = idx % BV;
+                cp[static_cast<size_t>(c) * DV + j0 + jj] = sm.S[c][jj];
+            }
         }
     }
     __syncthreads();

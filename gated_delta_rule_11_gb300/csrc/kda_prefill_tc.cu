@@ -456,6 +456,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int j = tid & 127;           // value channel = TMEM lane
         const int hf = tid >> 7;           // which half of the key rows / tile columns
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const long long ck_row0 = a.ckpt ? ckpt_first_row(a, n) : 0;
         constexpr int HR = D / 2;          // state rows per thread
         constexpr uint32_t id_e = idesc_f16kind(kTypeF16, 128, 32, 0, 0);
         constexpr uint32_t id_g = idesc_f16kind(kTypeF16, 128, 16, 0, 0);
@@ -618,6 +619,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (e_issuer && t + 1 < ntiles && !issue_e(t + 1, warp)) note_timeout(abort_flag);
             if (tid == TMA_TID && t + NS < ntiles) issue_tma(t + NS);
             if (tid == OST_TID && t > 0) store_out(t - 1);
+            // state checkpoint after this tile (off the chain's critical path)
+            if (float *cp = ckpt_slot(a, ck_row0, min((t + 1) * C, eos - bos), h, D * D)) {
+#pragma unroll
+                for (int cc = 0; cc < HR; ++cc) __stcs(cp + static_cast<size_t>(hf * HR + cc) * D + j, S[cc]);
+            }
         }
         // uniform decision: every chain thread takes the same branch
         const bool aborted = named_bar_or(2, NCHAIN, *abort_flag != 0);

@@ -42,6 +42,7 @@ class Workload:
     seqlens: tuple = field(default=())   # packed sequences (varlen) if non-empty
     N: int = 0                 # decode: number of sequences
     steps: int = 0             # decode: consecutive steps
+    drafts: int = 0            # speculative replay: tokens verified per sequence
 
     @property
     def torch_dtype(self):
@@ -49,13 +50,13 @@ class Workload:
 
     @property
     def total_tokens(self) -> int:
-        if self.kind == "decode":
+        if self.kind in ("decode", "spec"):
             return self.N
         return sum(self.seqlens) if self.seqlens else self.B * self.T
 
     @property
     def n_seqs(self) -> int:
-        if self.kind == "decode":
+        if self.kind in ("decode", "spec"):
             return self.N
         return len(self.seqlens) if self.seqlens else self.B
 
@@ -73,6 +74,11 @@ WORKLOADS = {
                                        seqlens=(131072, 65536, 32768, 8192)),
     "decode_bf16_N256_H96": Workload("decode_bf16_N256_H96", "decode", H=96, dk=128, dv=128,
                                      dtype="bf16", z_std=2.0, s0_std=0.1, seed=4, N=256, steps=100),
+    # Speculative replay: 8 tokens verified per sequence (the last committed
+    # token and 7 drafts), of which an accepted prefix of 1..8 is replayed.
+    "spec_bf16_N256_H96_K8": Workload("spec_bf16_N256_H96_K8", "spec", H=96, dk=128, dv=128,
+                                      dtype="bf16", z_std=2.0, s0_std=0.1, seed=5, N=256,
+                                      steps=20, drafts=8),
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
@@ -153,3 +159,29 @@ def make_decode_token(w: Workload, step: int, device="cpu", seed: int | None = N
     beta = torch.sigmoid(_draw((N, H), g, device)).to(dt)
     g_raw = _draw((N, H, w.dk), g, device, w.z_std).to(dt)
     return dict(q=q, k=k, v=v, g_raw=g_raw, beta=beta)
+
+
+def make_decode_drafts(w: Workload, step: int, device="cpu", seed: int | None = None, *,
+                       N: int | None = None, H: int | None = None, K: int | None = None,
+                       min_accepted: int = 1):
+    """One speculative-replay batch: K verified tokens per sequence and how
+    many of them each sequence accepts.
+
+    Returns q, k, g_raw [N, K, H, dk]; v [N, K, H, dv]; beta [N, K, H] in the
+    workload dtype, and accepted int32 [N] drawn uniformly from
+    [min_accepted, K].
+    """
+    seed = w.seed if seed is None else seed
+    N = w.N if N is None else N
+    H = w.H if H is None else H
+    K = w.drafts if K is None else K
+    g = _gen(device, seed * 1_000_003 + 7919 * (step + 1))
+    dt = w.torch_dtype
+    q = _unit_rows(_draw((N, K, H, w.dk), g, device)).to(dt)
+    k = _unit_rows(_draw((N, K, H, w.dk), g, device)).to(dt)
+    v = _draw((N, K, H, w.dv), g, device).to(dt)
+    beta = torch.sigmoid(_draw((N, K, H), g, device)).to(dt)
+    g_raw = _draw((N, K, H, w.dk), g, device, w.z_std).to(dt)
+    accepted = torch.randint(min_accepted, K + 1, (N,), generator=g, device=device,
+                             dtype=torch.int32)
+    return dict(q=q, k=k, v=v, g_raw=g_raw, beta=beta, accepted=accepted)

@@ -12,6 +12,7 @@ import ctypes
 import os
 import threading
 
+import numpy as np
 import torch
 
 from . import build as _build
@@ -24,7 +25,8 @@ _lib = None
 _lock = threading.Lock()
 
 EXPORTED = ("kda_chunk_fwd", "kda_decode_step", "kda_status_str", "kda_last_cuda_error",
-            "kda_version", "kda_launch_count", "kda_check_device_status", "kda_chunk_fwd_kernel")
+            "kda_version", "kda_launch_count", "kda_check_device_status", "kda_chunk_fwd_kernel",
+            "kda_decode_steps", "kda_chunk_fwd_checkpointed", "kda_checkpoint_rows")
 
 
 class KdaError(RuntimeError):
@@ -63,6 +65,15 @@ def load_library(build_if_missing: bool = False):
         lib.kda_decode_step.restype = i
         lib.kda_decode_step.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp,
                                         ctypes.POINTER(KdaParams), vp]
+        lib.kda_chunk_fwd_checkpointed.restype = i
+        lib.kda_chunk_fwd_checkpointed.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, i,
+                                                   vp, vp, i, vp, ctypes.c_longlong,
+                                                   ctypes.POINTER(KdaParams), vp]
+        lib.kda_checkpoint_rows.restype = ctypes.c_longlong
+        lib.kda_checkpoint_rows.argtypes = [i, i, vp, i, i]
+        lib.kda_decode_steps.restype = i
+        lib.kda_decode_steps.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, vp,
+                                         ctypes.POINTER(KdaParams), vp]
         lib.kda_status_str.restype = ctypes.c_char_p
         lib.kda_status_str.argtypes = [i]
         lib.kda_last_cuda_error.restype = i
@@ -149,17 +160,74 @@ def kda_chunk_fwd(q, k, v, g_raw, beta, init_state=None, cu_seqlens=None, *,
     None; cu_seqlens int32 [N+1] on the device (then B == 1) or None.
     Returns (out [B, T, H, dv], final_state [N, H, dk, dv] float32 or None).
     """
+    out, final_state, _ = _chunk_fwd(q, k, v, g_raw, beta, init_state, cu_seqlens, out,
+                                     final_state, output_final_state, g_min, A_log, scale,
+                                     stream, 0, None, 0, "kda_chunk_fwd")
+    return out, final_state
+
+
+def checkpoint_layout(cu_seqlens, B: int, T: int, every: int):
+    """Rows of the checkpoint buffer and each sequence's first row.
+
+    cu_seqlens: int32 [N+1] (any device; read on the host) or None for B
+    sequences of length T.  Returns (rows, first_rows list of N ints):
+    sequence n's checkpoint i (state after (i + 1) * every tokens) is row
+    first_rows[n] + i.
+    """
+    lib = load_library()
+    if cu_seqlens is None:
+        cu = np.arange(B + 1, dtype=np.int32) * T
+        rows = lib.kda_checkpoint_rows(B, T, None, B, int(every))
+    else:
+        cu = np.ascontiguousarray(cu_seqlens.detach().cpu().numpy().astype(np.int32))
+        rows = lib.kda_checkpoint_rows(1, int(T), cu.ctypes.data, len(cu) - 1, int(every))
+    if rows < 0:
+        raise ValueError("checkpoint layout: every must be a positive multiple of 16 and "
+                         "cu_seqlens non-decreasing within [0, T]")
+    per = np.diff(cu.astype(np.int64)) // int(every)
+    first = np.concatenate([[0], np.cumsum(per)[:-1]]).astype(np.int64).tolist()
+    return int(rows), first
+
+
+def kda_chunk_fwd_checkpointed(q, k, v, g_raw, beta, init_state=None, cu_seqlens=None, *,
+                               checkpoint_every: int, checkpoints=None, out=None,
+                               final_state=None, output_final_state: bool = True,
+                               g_min: float = -5.0, A_log=None, scale: float = 1.0,
+                               stream=None):
+    """kda_chunk_fwd that also saves the state every ``checkpoint_every``
+    tokens (a positive multiple of 16) of each sequence.
+
+    Returns (out, final_state, checkpoints [rows, H, dk, dv] float32,
+    first_rows): checkpoint i of sequence n (the state after its first
+    (i + 1) * checkpoint_every tokens) is checkpoints[first_rows[n] + i].
+    """
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    rows, first = checkpoint_layout(cu_seqlens, B, T, checkpoint_every)
+    if checkpoints is None:
+        checkpoints = torch.empty((rows, H, dk, dv), dtype=torch.float32, device=q.device)
+    else:
+        _check(checkpoints, "checkpoints", (rows, H, dk, dv), torch.float32, q.device)
+    out, final_state, _ = _chunk_fwd(q, k, v, g_raw, beta, init_state, cu_seqlens, out,
+                                     final_state, output_final_state, g_min, A_log, scale,
+                                     stream, int(checkpoint_every), checkpoints, rows,
+                                     "kda_chunk_fwd_checkpointed")
+    return out, final_state, checkpoints, first
+
+
+def _chunk_fwd(q, k, v, g_raw, beta, init_state, cu_seqlens, out, final_state,
+               output_final_state, g_min, A_log, scale, stream, every, ckpt, ckpt_rows, name):
     lib = load_library()
     dev = q.device
     if dev.type != "cuda":
-        raise ValueError("kda_chunk_fwd runs on CUDA tensors only")
+        raise ValueError(f"{name} runs on CUDA tensors only")
     dt = q.dtype
     B, T, H, dk = q.shape
     dv = v.shape[-1]
-    for name, t, shp in (("q", q, (B, T, H, dk)), ("k", k, (B, T, H, dk)),
-                         ("g_raw", g_raw, (B, T, H, dk)), ("v", v, (B, T, H, dv)),
-                         ("beta", beta, (B, T, H))):
-        _check(t, name, shp, dt, dev)
+    for nm, t, shp in (("q", q, (B, T, H, dk)), ("k", k, (B, T, H, dk)),
+                       ("g_raw", g_raw, (B, T, H, dk)), ("v", v, (B, T, H, dv)),
+                       ("beta", beta, (B, T, H))):
+        _check(t, nm, shp, dt, dev)
     if cu_seqlens is not None:
         if cu_seqlens.dtype != torch.int32 or cu_seqlens.device != dev or cu_seqlens.dim() != 1:
             raise ValueError("cu_seqlens must be a 1-D int32 tensor on the inputs' device")
@@ -181,13 +249,16 @@ def kda_chunk_fwd(q, k, v, g_raw, beta, init_state=None, cu_seqlens=None, *,
     elif final_state is not None:
         _check(final_state, "final_state", (N, H, dk, dv), torch.float32, dev)
     prm = _params(g_min, A_log, scale)
-    st = lib.kda_chunk_fwd(_dtype_code(q), B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v),
-                           _ptr(g_raw), _ptr(beta), _ptr(init_state), _ptr(cu_seqlens), N,
-                           _ptr(out), _ptr(final_state), ctypes.byref(prm),
-                           _stream_handle(dev, stream))
+    common = (_dtype_code(q), B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw),
+              _ptr(beta), _ptr(init_state), _ptr(cu_seqlens), N, _ptr(out), _ptr(final_state))
+    if ckpt is None:
+        st = lib.kda_chunk_fwd(*common, ctypes.byref(prm), _stream_handle(dev, stream))
+    else:
+        st = lib.kda_chunk_fwd_checkpointed(*common, int(every), _ptr(ckpt), int(ckpt_rows),
+                                            ctypes.byref(prm), _stream_handle(dev, stream))
     if st != 0:
-        _raise(lib, "kda_chunk_fwd", st)
-    return out, final_state
+        _raise(lib, name, st)
+    return out, final_state, ckpt
 
 
 def kda_decode_step(q, k, v, g_raw, beta, state, *, out=None, g_min: float = -5.0,
@@ -218,4 +289,40 @@ def kda_decode_step(q, k, v, g_raw, beta, state, *, out=None, g_min: float = -5.
                              ctypes.byref(prm), _stream_handle(dev, stream))
     if st != 0:
         _raise(lib, "kda_decode_step", st)
+    return out
+
+
+def kda_decode_steps(q, k, v, g_raw, beta, state, accepted=None, *, out=None,
+                     g_min: float = -5.0, A_log=None, scale: float = 1.0, stream=None):
+    """Speculative replay: sequence n applies its first accepted[n] of K drafted
+    tokens to ``state`` [N, H, dk, dv] (float32, in place) in one pass.
+    q, k, g_raw [N, K, H, dk]; v [N, K, H, dv]; beta [N, K, H]; accepted int32
+    [N] on the device or None (all K).  Returns out [N, K, H, dv] (rows of
+    tokens that are not applied are left as they were in ``out``)."""
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("kda_decode_steps runs on CUDA tensors only")
+    dt = q.dtype
+    N, K, H, dk = q.shape
+    dv = v.shape[-1]
+    for name, t, shp in (("q", q, (N, K, H, dk)), ("k", k, (N, K, H, dk)),
+                         ("g_raw", g_raw, (N, K, H, dk)), ("v", v, (N, K, H, dv)),
+                         ("beta", beta, (N, K, H))):
+        _check(t, name, shp, dt, dev)
+    _check(state, "state", (N, H, dk, dv), torch.float32, dev)
+    if accepted is not None:
+        _check(accepted, "accepted", (N,), torch.int32, dev)
+    if A_log is not None:
+        _check(A_log, "A_log", (H,), torch.float32, dev)
+    if out is None:
+        out = torch.zeros((N, K, H, dv), dtype=dt, device=dev)
+    else:
+        _check(out, "out", (N, K, H, dv), dt, dev)
+    prm = _params(g_min, A_log, scale)
+    st = lib.kda_decode_steps(_dtype_code(q), N, K, H, dk, dv, _ptr(q), _ptr(k), _ptr(v),
+                              _ptr(g_raw), _ptr(beta), _ptr(accepted), _ptr(state), _ptr(out),
+                              ctypes.byref(prm), _stream_handle(dev, stream))
+    if st != 0:
+        _raise(lib, "kda_decode_steps", st)
     return out

@@ -110,6 +110,46 @@ kda_status kda_chunk_fwd(kda_dtype dt, int B, int T, int H, int dk, int dv,
                          const kda_params *p, kda_stream_t stream);
 
 /*
+ * kda_chunk_fwd_checkpointed -- kda_chunk_fwd that also saves the state at
+ * chosen positions inside each sequence, for a prefix cache that restores
+ * from a boundary rather than from the start ("Kimi K3：从三条信息流到完整系统",
+ * §Hybrid prefix cache: state checkpoint 与 KV 同池; the checkpoint is the
+ * same S_t that eq. (1) carries, so a later call resumed from it via
+ * init_state continues the sequence).
+ *
+ * checkpoint_every: E > 0, a multiple of 16.  Sequence n of length L_n
+ *   gets floor(L_n / E) checkpoints: checkpoint i (0-based) is the state
+ *   after its first (i + 1) * E tokens (the last one equals final_state
+ *   when E divides L_n).
+ * checkpoints: DEVICE fp32 [checkpoint_rows, H, dk, dv], caller-owned,
+ *   16-byte aligned.  Sequence n's checkpoints are rows r_n .. r_n +
+ *   floor(L_n / E) - 1, r_n = sum over m < n of floor(L_m / E) (without
+ *   cu_seqlens: r_n = n * floor(T / E)).  Rows at or past checkpoint_rows
+ *   are never written; kda_checkpoint_rows gives the count to allocate.
+ * checkpoints == NULL (or checkpoint_rows == 0) is kda_chunk_fwd itself.
+ * Other arguments and errors as kda_chunk_fwd; KDA_ERR_ARG also for E not
+ * a positive multiple of 16 or checkpoint_rows < 0 with a buffer given.
+ */
+kda_status kda_chunk_fwd_checkpointed(kda_dtype dt, int B, int T, int H, int dk, int dv,
+                                      const void *q, const void *k, const void *v,
+                                      const void *g_raw, const void *beta,
+                                      const float *init_state,
+                                      const int32_t *cu_seqlens, int N,
+                                      void *out, float *final_state,
+                                      int checkpoint_every, float *checkpoints,
+                                      long long checkpoint_rows,
+                                      const kda_params *p, kda_stream_t stream);
+
+/*
+ * kda_checkpoint_rows -- host helper: rows of the checkpoint buffer for
+ * these sequences (cu_seqlens_host: HOST [N+1] or NULL for B rows of T).
+ * Returns -1 for arguments kda_chunk_fwd would reject (E not a positive
+ * multiple of 16, a decreasing or out-of-range cu_seqlens).  No GPU work.
+ */
+long long kda_checkpoint_rows(int B, int T, const int32_t *cu_seqlens_host, int N,
+                              int checkpoint_every);
+
+/*
  * kda_decode_step -- advance N independent sequences by one token each.
  *
  * Inputs (dtype dt): q, k, g_raw [N, H, dk]; v [N, H, dv]; beta [N, H].
@@ -129,6 +169,30 @@ kda_status kda_decode_step(kda_dtype dt, int N, int H, int dk, int dv,
  * "prefill_simt_kernel": fp32 CUDA cores, every other supported case), or
  * NULL for an unsupported combination. */
 const char *kda_chunk_fwd_kernel(kda_dtype dt, int dk, int dv);
+
+/*
+ * kda_decode_steps -- speculative replay: advance N sequences by up to K
+ * drafted tokens each in one pass over the state.  Sequence n applies, in
+ * order, its first accepted[n] tokens (clamped to [0, K]); the remaining
+ * drafts leave no trace.  Only the drafts' projected inputs are kept, and
+ * the accepted prefix is replayed on chip with no per-draft state copy
+ * ("Kimi K3: Two point eight trillion parameters, open weights, and
+ * forty-seven pages of how", §The machine underneath; "Kimi K3：从三条信息流到
+ * 完整系统", §recurrent speculative decoding 不能复制整个状态).
+ *
+ * Inputs (dtype dt): q, k, g_raw [N, K, H, dk]; v [N, K, H, dv];
+ *   beta [N, K, H]; accepted: DEVICE [N] int32, or NULL for all K.
+ * In/out: state [N, H, dk, dv] fp32, read once and written once (left
+ *   untouched for a sequence with accepted[n] == 0).
+ * Output: out [N, K, H, dv]: o for every applied token; the rows of
+ *   tokens that are not applied are not written.
+ * kda_decode_step is the K = 1 case with every token applied.
+ */
+kda_status kda_decode_steps(kda_dtype dt, int N, int K, int H, int dk, int dv,
+                            const void *q, const void *k, const void *v,
+                            const void *g_raw, const void *beta, const int32_t *accepted,
+                            float *state, void *out,
+                            const kda_params *p, kda_stream_t stream);
 
 /* Static string for a status code (never NULL). */
 const char *kda_status_str(kda_status s);

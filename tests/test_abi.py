@@ -92,3 +92,41 @@ def test_python_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(1, 16, 1, 32)
     with pytest.raises(ValueError):
         kda.kda_chunk_fwd(x, x, x, x, torch.zeros(1, 16, 1))
+
+
+def test_checkpoint_rows_host_helper(lib):
+    """Rows of the checkpoint buffer: floor(L_n / E) per sequence; no GPU."""
+    cu = (ctypes.c_int32 * 7)(0, 16, 116, 116, 149, 405, 452)
+    assert lib.kda_checkpoint_rows(1, 452, cu, 6, 16) == 1 + 6 + 0 + 2 + 16 + 2
+    assert lib.kda_checkpoint_rows(1, 452, cu, 6, 64) == 0 + 1 + 0 + 0 + 4 + 0
+    assert lib.kda_checkpoint_rows(3, 200, None, 3, 48) == 3 * 4
+    assert lib.kda_checkpoint_rows(2, 15, None, 2, 16) == 0
+    assert lib.kda_checkpoint_rows(1, 452, cu, 6, 24) == -1          # not a multiple of 16
+    assert lib.kda_checkpoint_rows(1, 452, cu, 6, 0) == -1
+    assert lib.kda_checkpoint_rows(1, 400, cu, 6, 16) == -1          # past T
+    bad = (ctypes.c_int32 * 3)(0, 40, 20)
+    assert lib.kda_checkpoint_rows(1, 40, bad, 2, 16) == -1          # decreasing
+    rows, first = kda.checkpoint_layout(None, 3, 200, 48)
+    assert rows == 12 and first == [0, 4, 8]
+    import torch
+    rows, first = kda.checkpoint_layout(torch.tensor([0, 16, 116, 116, 149, 405, 452],
+                                                     dtype=torch.int32), 1, 452, 16)
+    assert rows == 27 and first == [0, 1, 7, 7, 9, 25]
+
+
+def test_checkpointed_validation_rejects_before_launch(lib):
+    p = ctypes.c_void_p(4096)
+
+    def ck(every, buf, rows, dt=1):
+        return lib.kda_chunk_fwd_checkpointed(dt, 1, 64, 1, 128, 128, p, p, p, p, p, None, None,
+                                              1, p, None, every, buf, rows, None, None)
+    assert ck(24, p, 4) == 1                       # interval not a multiple of 16
+    assert ck(0, p, 4) == 1
+    assert ck(16, p, -1) == 1
+    assert ck(16, ctypes.c_void_p(4104), 4) == 4   # buffer needs 16-byte alignment
+    assert ck(16, p, 4, dt=9) == 2
+    p0 = ctypes.c_void_p(4096)
+    assert lib.kda_decode_steps(1, 4, 0, 2, 128, 128, p0, p0, p0, p0, p0, None, p0, p0,
+                                None, None) == 1   # K must be >= 1
+    assert lib.kda_decode_steps(1, 4, 3, 2, 128, 128, p0, p0, p0, p0, p0, ctypes.c_void_p(4098),
+                                p0, p0, None, None) == 4   # accepted needs 4-byte alignment
