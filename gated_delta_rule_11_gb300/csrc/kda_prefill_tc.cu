@@ -106,7 +106,9 @@ constexpr int LSS = 20;                           //   row stride of L (16-byte 
 constexpr int SC_LS = 3 * C * PADF * 4;           //   fp32 [16][LSS]: L
 constexpr int SC_TBF = SC_LS + C * LSS * 4;       //   fp32 [16][TBS]: T Diag(beta) (tf32-rounded)
 constexpr int SC_T11 = SC_TBF + C * TBS * 4;      //   fp32 [8][8]: lower-right block of T (solve)
-constexpr int SCR_BYTES = (SC_T11 + 64 * 4 + 127) & ~127;
+constexpr int SC_T00 = SC_T11 + 64 * 4;           //   fp32 [8][8]: upper-left block of T
+constexpr int SC_Y = SC_T00 + 64 * 4;             //   fp32 [8][8]: Diag(beta) L10 T00
+constexpr int SCR_BYTES = (SC_Y + 64 * 4 + 127) & ~127;
 constexpr int OFF_BAR = (OFF_SCR + NPROD * SCR_BYTES + 63) & ~63;
 enum { B_RAW = 0, B_FULL = NS, B_VT = 2 * NS, B_UPD, NUM_BARS };
 constexpr int NACC = 4;          // independent accumulators of (e)
@@ -226,6 +228,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         float *ls = reinterpret_cast<float *>(scr + SC_LS);
         float *tbf = reinterpret_cast<float *>(scr + SC_TBF);
         float *t11 = reinterpret_cast<float *>(scr + SC_T11);
+        float *t00 = reinterpret_cast<float *>(scr + SC_T00);
+        float *ysc = reinterpret_cast<float *>(scr + SC_Y);
         // beta is a strided gather (one value per token): load it a tile ahead
         // so its latency hides behind a tile of work.
         auto load_beta = [&](int tt) {
@@ -340,19 +344,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
             }
             named_bar_sync(pbar, 128);
+            // T = (I + N)^-1, N = Diag(beta) L strictly lower, in 8x8 blocks:
+            // T00 = (I + N00)^-1 and T11 = (I + N11)^-1 by forward substitution
+            // (lanes 0-7 / 8-15 of the first warp own one column each), then
+            // T10 = -T11 (N10 T00) as two 8x8 products over 64 threads.  Stored
+            // as T Diag(beta), tf32-rounded.
+            const float *betas = reinterpret_cast<const float *>(st + ST_BETA);
+            auto row8 = [&](const float *p, float (&x)[8]) {   // 8 floats, two 16-byte loads
+                const float4 lo = *reinterpret_cast<const float4 *>(p);
+                const float4 hi = *reinterpret_cast<const float4 *>(p + 4);
+                x[0] = lo.x; x[1] = lo.y; x[2] = lo.z; x[3] = lo.w;
+                x[4] = hi.x; x[5] = hi.y; x[6] = hi.z; x[7] = hi.w;
+            };
             if (pw == 0 && lane < C) {
-                // T = (I + N)^-1, N = Diag(beta) L strictly lower, in 8x8 blocks:
-                // T00 = (I + N00)^-1 and T11 = (I + N11)^-1 by forward substitution
-                // (lanes 0-7 / 8-15 own one column each, in parallel), then
-                // T10 = -T11 N10 T00.  Stored as T Diag(beta), tf32-rounded.
-                const float *betas = reinterpret_cast<const float *>(st + ST_BETA);
                 const int j = lane, blk = j >> 3, r0 = 8 * blk;
-                auto row8 = [&](const float *p, float (&x)[8]) {   // 8 floats, two 16-byte loads
-                    const float4 lo = *reinterpret_cast<const float4 *>(p);
-                    const float4 hi = *reinterpret_cast<const float4 *>(p + 4);
-                    x[0] = lo.x; x[1] = lo.y; x[2] = lo.z; x[3] = lo.w;
-                    x[4] = hi.x; x[5] = hi.y; x[6] = hi.z; x[7] = hi.w;
-                };
                 float tb[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -365,43 +370,32 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     tb[i] = (r == j ? 1.f : 0.f) - betas[r] * acc;
                 }
                 const float bj = betas[j];
-                if (blk == 1) {
+                float *tdiag = blk ? t11 : t00;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        t11[i * 8 + (j - 8)] = tb[i];
-                        tbf[(8 + i) * TBS + j] = to_tf32(tb[i] * bj);
-                        tbf[i * TBS + j] = 0.f;
-                    }
+                for (int i = 0; i < 8; ++i) {
+                    tdiag[i * 8 + (j - r0)] = tb[i];
+                    tbf[(r0 + i) * TBS + j] = to_tf32(tb[i] * bj);
+                    if (blk) tbf[i * TBS + j] = 0.f;           // T01 = 0
                 }
-                __syncwarp(0x0000ffffu);
-                if (blk == 0) {
-                    float y[8];
+            }
+            named_bar_sync(pbar, 128);
+            const int bi = c >> 3, bj8 = c & 7;                 // block entry (bi, bj8) for c < 64
+            if (c < 64) {                                       // Y = Diag(beta_8..15) L10 T00
+                float lr[8];
+                row8(ls + (8 + bi) * LSS, lr);
+                float acc = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        float lr[8];
-                        row8(ls + (8 + i) * LSS, lr);
-                        float acc = 0.f;
+                for (int m2 = 0; m2 < 8; ++m2) acc = fmaf(lr[m2], t00[m2 * 8 + bj8], acc);
+                ysc[bi * 8 + bj8] = betas[8 + bi] * acc;
+            }
+            named_bar_sync(pbar, 128);
+            if (c < 64) {                                       // T10 = -T11 Y
+                float tr[8];
+                row8(t11 + bi * 8, tr);
+                float acc = 0.f;
 #pragma unroll
-                        for (int i2 = 0; i2 < 8; ++i2) acc = fmaf(lr[i2], tb[i2], acc);
-                        y[i] = betas[8 + i] * acc;
-                    }
-                    // all loads before any store (the stores may alias them)
-                    float t10[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        float tr[8];
-                        row8(t11 + i * 8, tr);
-                        float acc = 0.f;
-#pragma unroll
-                        for (int m2 = 0; m2 < 8; ++m2) acc = fmaf(tr[m2], y[m2], acc);
-                        t10[i] = acc;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        tbf[(8 + i) * TBS + j] = to_tf32(-t10[i] * bj);
-                        tbf[i * TBS + j] = to_tf32(tb[i] * bj);
-                    }
-                }
+                for (int m2 = 0; m2 < 8; ++m2) acc = fmaf(tr[m2], ysc[m2 * 8 + bj8], acc);
+                tbf[(8 + bi) * TBS + bj8] = to_tf32(-acc * betas[bj8]);
             }
             named_bar_sync(pbar, 128);
             // W = T Diag(beta) (K e^b) -> rows 0..15 of the (e) B operand hold -W;
@@ -521,16 +515,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // sequence's partial last tile straight to global memory.
         auto read_out = [&](int tt) {
             const uint32_t eb = tmem + TM_E + E_BUF * static_cast<uint32_t>(tt & 1) + lane_base + 16 + 8 * hf;
-            float o[8], x[8];
+            float o[8], x[NACC - 1][8];
             tmem_ld8(eb, o);
+#pragma unroll
+            for (int p = 1; p < NACC; ++p) tmem_ld8(eb + 32u * p, x[p - 1]);
             tmem_ld_wait();
 #pragma unroll
-            for (int p = 1; p < NACC; ++p) {
-                tmem_ld8(eb + 32u * p, x);
-                tmem_ld_wait();
+            for (int p = 1; p < NACC; ++p)
 #pragma unroll
-                for (int r = 0; r < 8; ++r) o[r] += x[r];
-            }
+                for (int r = 0; r < 8; ++r) o[r] += x[p - 1][r];
             const int tt0 = bos + tt * C;
             const int nvv = min(C, eos - tt0);
             if (nvv == C) {
@@ -565,16 +558,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             {
                 // tile columns [8 hf, 8 hf + 8) of Vt^T = U^T - (W S)^T
                 const float *u = reinterpret_cast<const float *>(st + ST_U);
-                float uj[8], v[8];
+                float uj[8], v[NACC][8];
+#pragma unroll
+                for (int p = 0; p < NACC; ++p) tmem_ld8(e_acc + 32u * p + lane_base + 8 * hf, v[p]);
 #pragma unroll
                 for (int r = 0; r < 8; ++r) uj[r] = u[(8 * hf + r) * D + j];
+                tmem_ld_wait();
 #pragma unroll
-                for (int p = 0; p < NACC; ++p) {
-                    tmem_ld8(e_acc + 32u * p + lane_base + 8 * hf, v);
-                    tmem_ld_wait();
+                for (int p = 0; p < NACC; ++p)
 #pragma unroll
-                    for (int r = 0; r < 8; ++r) uj[r] += v[r];
-                }
+                    for (int r = 0; r < 8; ++r) uj[r] += v[p][r];
                 uint32_t p[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) p[i] = pack_h2(uj[2 * i], uj[2 * i + 1]);
@@ -599,18 +592,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc_fence_after();
             const float *gc = reinterpret_cast<const float *>(st + ST_GC) + hf * HR;
 #pragma unroll
-            for (int cb = 0; cb < HR / 16; ++cb) {
-                float inc[16];
-                tmem_ld16(tmem + TM_H + lane_base + hf * HR + cb * 16, inc);
-                float gv[16];   // e^{b_C}: the same 16 values for the whole warp, four 16-byte loads
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const float4 g4 = *reinterpret_cast<const float4 *>(gc + cb * 16 + q4 * 4);
-                    gv[q4 * 4 + 0] = g4.x; gv[q4 * 4 + 1] = g4.y; gv[q4 * 4 + 2] = g4.z; gv[q4 * 4 + 3] = g4.w;
-                }
+            for (int cb = 0; cb < HR / 16; cb += 2) {      // two TMEM loads per wait
+                float inc[2][16];
+                tmem_ld16(tmem + TM_H + lane_base + hf * HR + cb * 16, inc[0]);
+                tmem_ld16(tmem + TM_H + lane_base + hf * HR + cb * 16 + 16, inc[1]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) S[cb * 16 + i] = fmaf(gv[i], S[cb * 16 + i], inc[i]);
+                for (int b2 = 0; b2 < 2; ++b2) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {   // e^{b_C}: the same 16 values for the whole warp
+                        const float4 g4 = *reinterpret_cast<const float4 *>(gc + (cb + b2) * 16 + q4 * 4);
+                        float *sp = S + (cb + b2) * 16 + q4 * 4;
+                        const float *ip = inc[b2] + q4 * 4;
+                        sp[0] = fmaf(g4.x, sp[0], ip[0]); sp[1] = fmaf(g4.y, sp[1], ip[1]);
+                        sp[2] = fmaf(g4.z, sp[2], ip[2]); sp[3] = fmaf(g4.w, sp[3], ip[3]);
+                    }
+                }
             }
             write_sT();
             tc_fence_before();

@@ -113,7 +113,7 @@ kda_status kda_chunk_fwd(kda_dtype dt, int B, int T, int H, int dk, int dv,
  * kda_chunk_fwd_checkpointed -- kda_chunk_fwd that also saves the state at
  * chosen positions inside each sequence, for a prefix cache that restores
  * from a boundary rather than from the start ("Kimi K3：从三条信息流到完整系统",
- * §Hybrid prefix cache: state checkpoint 与 KV 同池; the checkpoint is the
+ * §在线推理：两类记忆必须共同命中, "hybrid prefix cache"; the checkpoint is the
  * same S_t that eq. (1) carries, so a later call resumed from it via
  * init_state continues the sequence).
  *
