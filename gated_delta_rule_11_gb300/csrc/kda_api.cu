@@ -16,15 +16,37 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool aligned_to(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 bool head_dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
 
-void resolve_params(const kda_params *p, float &g_min, const float *&A_log, float &scale) {
+void resolve_params(const kda_params *p, float &g_min, const float *&A_log, float &scale,
+                    int &gate_mode, int &gate_scalar) {
     g_min = -5.0f;
     A_log = nullptr;
     scale = 1.0f;
+    gate_mode = KDA_GATE_BOUNDED;
+    gate_scalar = 0;
     if (p) {
         if (p->g_min != 0.0f) g_min = p->g_min;
         A_log = p->A_log;
         if (p->scale != 0.0f) scale = p->scale;
+        gate_mode = p->gate_mode;
+        gate_scalar = p->gate_per_head != 0;
     }
+}
+
+bool gate_mode_ok(const kda_params *p) {
+    return !p || (p->gate_mode >= KDA_GATE_BOUNDED && p->gate_mode <= KDA_GATE_NONE);
+}
+
+// g_raw: required unless the gate is off; 16-byte aligned per channel,
+// element-aligned per head.
+kda_status check_gate(const kda_params *p, kda_dtype dt, const void *g_raw, bool needed) {
+    if (!gate_mode_ok(p)) return KDA_ERR_ARG;
+    const bool none = p && p->gate_mode == KDA_GATE_NONE;
+    const bool scalar = p && p->gate_per_head;
+    if (none) return KDA_OK;
+    if (needed && !g_raw) return KDA_ERR_ARG;
+    if (!g_raw) return KDA_OK;
+    if (scalar) return aligned_to(g_raw, dt == KDA_F32 ? 4 : 2) ? KDA_OK : KDA_ERR_ALIGN;
+    return aligned16(g_raw) ? KDA_OK : KDA_ERR_ALIGN;
 }
 
 kda_status from_cuda(cudaError_t e) {
@@ -112,11 +134,12 @@ kda_status kda_chunk_fwd_checkpointed(kda_dtype dt, int B, int T, int H, int dk,
         return KDA_ERR_ARG;
     const long long total = static_cast<long long>(B) * T;
     if (total > INT32_MAX || static_cast<long long>(N) * H > INT32_MAX) return KDA_ERR_ARG;
-    if (total > 0 && (!q || !k || !v || !g_raw || !beta || !out)) return KDA_ERR_ARG;
-    const void *ptrs[] = {q, k, v, g_raw, init_state, out, final_state, checkpoints};
+    if (total > 0 && (!q || !k || !v || !beta || !out)) return KDA_ERR_ARG;
+    const void *ptrs[] = {q, k, v, init_state, out, final_state, checkpoints};
     for (const void *ptr : ptrs)
         if (ptr && !aligned16(ptr)) return KDA_ERR_ALIGN;
     if (!aligned_to(beta, dt == KDA_F32 ? 4 : 2) || !aligned_to(cu_seqlens, 4)) return KDA_ERR_ALIGN;
+    if (const kda_status gs = check_gate(p, dt, g_raw, total > 0)) return gs;
     if (N == 0 || (total == 0 && !final_state)) return KDA_OK;  // nothing to compute
 
     kda::PrefillArgs a;
@@ -129,14 +152,15 @@ kda_status kda_chunk_fwd_checkpointed(kda_dtype dt, int B, int T, int H, int dk,
     a.ckpt = ck ? checkpoints : nullptr;
     a.ckpt_rows = ck ? checkpoint_rows : 0;
     a.ckpt_every = ck ? checkpoint_every : 0;
-    resolve_params(p, a.g_min, a.A_log, a.scale);
+    resolve_params(p, a.g_min, a.A_log, a.scale, a.gate_mode, a.gate_scalar);
     if (a.A_log && !aligned_to(a.A_log, 4)) return KDA_ERR_ALIGN;
     a.N = N;
     a.H = H;
     a.T_total = static_cast<int>(total);
     a.T_seq = T;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (kda::prefill_tc_supported(dt, dk, dv) && a.T_total > 0)
+    const bool default_gate = a.gate_mode == KDA_GATE_BOUNDED && !a.gate_scalar;
+    if (default_gate && kda::prefill_tc_supported(dt, dk, dv) && a.T_total > 0)
         return from_cuda(kda::launch_prefill_tc(a, s));
     return from_cuda(kda::launch_prefill_simt(dt, dk, dv, a, s));
 }
@@ -163,17 +187,18 @@ kda_status kda_decode_steps(kda_dtype dt, int N, int K, int H, int dk, int dv,
     if (static_cast<long long>(N) * H > INT32_MAX || static_cast<long long>(N) * K * H > INT32_MAX)
         return KDA_ERR_ARG;
     if (N == 0) return KDA_OK;
-    if (!q || !k || !v || !g_raw || !beta || !state || !out) return KDA_ERR_ARG;
-    const void *ptrs[] = {q, k, v, g_raw, state, out};
+    if (!q || !k || !v || !beta || !state || !out) return KDA_ERR_ARG;
+    const void *ptrs[] = {q, k, v, state, out};
     for (const void *ptr : ptrs)
         if (!aligned16(ptr)) return KDA_ERR_ALIGN;
     if (!aligned_to(beta, dt == KDA_F32 ? 4 : 2) || !aligned_to(accepted, 4)) return KDA_ERR_ALIGN;
+    if (const kda_status gs = check_gate(p, dt, g_raw, true)) return gs;
     kda::DecodeArgs a;
     a.q = q; a.k = k; a.v = v; a.g = g_raw; a.beta = beta;
     a.accepted = accepted;
     a.state = state;
     a.out = out;
-    resolve_params(p, a.g_min, a.A_log, a.scale);
+    resolve_params(p, a.g_min, a.A_log, a.scale, a.gate_mode, a.gate_scalar);
     if (a.A_log && !aligned_to(a.A_log, 4)) return KDA_ERR_ALIGN;
     a.N = N;
     a.K = K;

@@ -5,6 +5,8 @@
 // underneath).  Replaying only the accepted prefix of speculative drafts on
 // chip, with no per-draft state copy, is the scheme of that section and of
 // "Kimi K3：从三条信息流到完整系统", §recurrent speculative decoding 不能复制整个状态.
+// The gate input becomes alpha under any kda_gate_mode (eq. (5) by
+// default), one gate per key channel or one per head.
 // One CTA per (sequence, head); the fp32 state S [dk, dv] (row = key channel
 // c, column = value channel j) is read from HBM once, kept in registers
 // across the tokens, and written back once, in place.
@@ -91,14 +93,17 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode1_kernel(DecodeArgs a
 
     const Tin *q = static_cast<const Tin *>(a.q) + static_cast<size_t>(nh) * DK;
     const Tin *k = static_cast<const Tin *>(a.k) + static_cast<size_t>(nh) * DK;
-    const Tin *z = static_cast<const Tin *>(a.g) + static_cast<size_t>(nh) * DK;
+    // gate input of key channel c: per channel [N, H, dk] or per head [N, H]
+    const Tin *z = static_cast<const Tin *>(a.g) + (a.gate_scalar ? static_cast<size_t>(nh)
+                                                                   : static_cast<size_t>(nh) * DK);
     const Tin *v = static_cast<const Tin *>(a.v) + static_cast<size_t>(nh) * DV;
     const float beta = ld_in(static_cast<const Tin *>(a.beta) + nh);
     const float escale = a.A_log ? expf(__ldg(a.A_log + h)) : 1.0f;
 
     if (tid < DK) {
         const float kc = ld_in(k + tid), qc = ld_in(q + tid);
-        const float alpha = expf(log_decay(ld_in(z + tid), escale, a.g_min));
+        const float zc = a.gate_mode == KDA_GATE_NONE ? 0.f : ld_in(z + (a.gate_scalar ? 0 : tid));
+        const float alpha = expf(gate_log_decay(a.gate_mode, zc, escale, a.g_min));
         s_alpha[tid] = alpha;
         s_k[tid] = kc;
         s_ak[tid] = alpha * kc;
@@ -220,8 +225,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(DecodeArgs a)
         for (int idx = tid; idx < nb * DK; idx += kDecodeThreads) {
             const int i = idx / DK, c = idx % DK;
             const size_t o = (static_cast<size_t>(n) * a.K + i0 + i) * tok_k + static_cast<size_t>(h) * DK + c;
-            const float kc = ld_in(gk + o), qc = ld_in(gq + o), zc = ld_in(gz + o);
-            const float alpha = expf(log_decay(zc, escale, a.g_min));
+            const float kc = ld_in(gk + o), qc = ld_in(gq + o);
+            const size_t og = a.gate_scalar ? (static_cast<size_t>(n) * a.K + i0 + i) * a.H + h : o;
+            const float zc = a.gate_mode == KDA_GATE_NONE ? 0.f : ld_in(gz + og);
+            const float alpha = expf(gate_log_decay(a.gate_mode, zc, escale, a.g_min));
             sm.akq[i][c] = make_ulonglong2(pack2(alpha * kc, alpha * kc), pack2(alpha * qc, alpha * qc));
             sm.alk[i][c] = make_ulonglong2(pack2(alpha, alpha), pack2(kc, kc));
             float kq = kc * qc;

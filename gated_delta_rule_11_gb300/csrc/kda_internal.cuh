@@ -22,6 +22,7 @@ struct PrefillArgs {
     const float *A_log;         // device [H] or nullptr
     int N, H, T_total, T_seq;
     float g_min, scale;
+    int gate_mode, gate_scalar;  // kda_gate_mode; 1 = one gate per (token, head)
     // State checkpoints: every ckpt_every tokens of each sequence (a multiple
     // of 16; 0 = none) into ckpt [ckpt_rows, H, dk, dv]; rows at or past
     // ckpt_rows are never written.
@@ -40,6 +41,7 @@ struct DecodeArgs {
     const float *A_log;
     int N, K, H;
     float g_min, scale;
+    int gate_mode, gate_scalar;
 };
 
 // Element loads/stores in the caller's dtype, computed in fp32.
@@ -64,6 +66,20 @@ __device__ __forceinline__ float log_decay(float z, float escale, float g_min) {
 // ~1e-6, far below the tensor-core paths' operand rounding).
 __device__ __forceinline__ float log_decay_fast(float z, float escale, float g_min) {
     return g_min * __frcp_rn(1.0f + __expf(-escale * z));
+}
+
+// Log-decay g of one gate input under each kda_gate_mode.  The negative
+// softplus is -(max(x, 0) + log(1 + e^-|x|)), which never overflows.
+__device__ __forceinline__ float gate_log_decay(int mode, float z, float escale, float g_min) {
+    switch (mode) {
+    case KDA_GATE_BOUNDED: return log_decay(z, escale, g_min);
+    case KDA_GATE_LOG_DECAY: return z;
+    case KDA_GATE_NEG_SOFTPLUS: {
+        const float x = escale * z;
+        return -(fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))));
+    }
+    default: return 0.f;
+    }
 }
 
 // Sequence span [bos, eos) of sequence n, clamped into [0, T_total].

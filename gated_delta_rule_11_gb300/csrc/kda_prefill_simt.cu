@@ -19,6 +19,17 @@
 // written out (Tril keeps the diagonal: a token reads its own write).
 // Tokens past the end of a sequence enter the last tile as k = q = v = 0,
 // beta = 0, g = 0, which leaves the state untouched.
+//
+// Gate variants (kda_gate_mode): the log-decay g comes from the gate input
+// under the chosen map, per key channel or one per head.  An unbounded gate
+// (the log-decay itself, or Kimi Linear's negative softplus, "Kimi K3: Two
+// point eight trillion parameters, open weights, and forty-seven pages of
+// how", §What changed between the paper and the model) can drive b far
+// below -80 within a tile, where e^{-b} overflows; for those the kernel
+// takes the position-pair path that the bound was introduced to avoid:
+//   L_rs = sum_c k_rc k_sc e^{b_rc - b_sc},  A_rs = sum_c q_rc k_sc e^{b_rc - b_sc}
+// (s <= r, so every exponent is <= 0), with the other factors unchanged
+// (e^{b}, e^{b_C - b} <= 1 never overflow).
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -39,11 +50,18 @@ struct SimtSmem {
     float beta[C];
     float ebC[DK];
 };
+// Extra shared memory of the position-pair path: raw k, raw q (masked) and b.
+template <int DK>
+struct SimtPairSmem {
+    float k[C][DK], q[C][DK], b[C][DK];
+};
 
 template <typename Tin, int DK, int DV>
 __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SimtSmem<DK> &sm = *reinterpret_cast<SimtSmem<DK> *>(smem_raw);
+    SimtPairSmem<DK> &pp = *reinterpret_cast<SimtPairSmem<DK> *>(smem_raw + sizeof(SimtSmem<DK>));
+    const bool pairs = a.gate_mode == KDA_GATE_LOG_DECAY || a.gate_mode == KDA_GATE_NEG_SOFTPLUS;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int chain = blockIdx.x;             // n * H + h
@@ -79,8 +97,10 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
             float zr[C], kr[C], qr[C];
 #pragma unroll
             for (int r = 0; r < C; ++r) {
-                const size_t off = static_cast<size_t>(t0 + min(r, nv - 1)) * tok_k + h * DK + c;
-                zr[r] = ld_in(gz + off);
+                const size_t tok = static_cast<size_t>(t0 + min(r, nv - 1));
+                const size_t off = tok * tok_k + h * DK + c;
+                zr[r] = a.gate_mode == KDA_GATE_NONE
+                            ? 0.f : ld_in(gz + (a.gate_scalar ? tok * a.H + h : off));
                 kr[r] = ld_in(gk + off);
                 qr[r] = ld_in(gq + off);
             }
@@ -88,7 +108,7 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
             float run = 0.f;
 #pragma unroll
             for (int r = 0; r < C; ++r) {
-                if (r < nv) run += log_decay(zr[r], escale, a.g_min);
+                if (r < nv) run += gate_log_decay(a.gate_mode, zr[r], escale, a.g_min);
                 else kr[r] = qr[r] = 0.f;
                 b[r] = run;
             }
@@ -97,9 +117,15 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
             for (int r = 0; r < C; ++r) {
                 const float eb = expf(b[r]);
                 sm.kg[r][c] = kr[r] * eb;
-                sm.kinv[r][c] = kr[r] * expf(-b[r]);
                 sm.qg[r][c] = qr[r] * eb;
                 sm.kdec[r][c] = kr[r] * expf(bC - b[r]);
+                if (pairs) {
+                    pp.k[r][c] = kr[r];
+                    pp.q[r][c] = qr[r];
+                    pp.b[r][c] = b[r];
+                } else {
+                    sm.kinv[r][c] = kr[r] * expf(-b[r]);
+                }
             }
             sm.ebC[c] = expf(bC);
         }
@@ -116,10 +142,18 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
             for (int i = 0; i < C; ++i) {
                 float l = 0.f, aa = 0.f;
                 if (i <= r) {
-                    for (int c = lane; c < DK; c += 32) {
-                        const float ki = sm.kinv[i][c];
-                        l += sm.kg[r][c] * ki;
-                        aa += sm.qg[r][c] * ki;
+                    if (pairs) {
+                        for (int c = lane; c < DK; c += 32) {
+                            const float ki = pp.k[i][c] * expf(pp.b[r][c] - pp.b[i][c]);
+                            l += pp.k[r][c] * ki;
+                            aa += pp.q[r][c] * ki;
+                        }
+                    } else {
+                        for (int c = lane; c < DK; c += 32) {
+                            const float ki = sm.kinv[i][c];
+                            l += sm.kg[r][c] * ki;
+                            aa += sm.qg[r][c] * ki;
+                        }
                     }
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) {
@@ -217,10 +251,11 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
 
 template <typename Tin, int DK, int DV>
 cudaError_t launch_one(const PrefillArgs &a, cudaStream_t s) {
-    const size_t smem = sizeof(SimtSmem<DK>);
+    const bool pairs = a.gate_mode == KDA_GATE_LOG_DECAY || a.gate_mode == KDA_GATE_NEG_SOFTPLUS;
+    const size_t smem = sizeof(SimtSmem<DK>) + (pairs ? sizeof(SimtPairSmem<DK>) : 0);
     auto kern = prefill_simt_kernel<Tin, DK, DV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+                                         static_cast<int>(sizeof(SimtSmem<DK>) + sizeof(SimtPairSmem<DK>)));
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(a.N) * static_cast<unsigned>(a.H), DV / BV);
     kern<<<grid, NT, smem, s>>>(a);

@@ -37,7 +37,12 @@ class KdaError(RuntimeError):
 
 
 class KdaParams(ctypes.Structure):
-    _fields_ = [("g_min", ctypes.c_float), ("A_log", ctypes.c_void_p), ("scale", ctypes.c_float)]
+    _fields_ = [("g_min", ctypes.c_float), ("A_log", ctypes.c_void_p), ("scale", ctypes.c_float),
+                ("gate_mode", ctypes.c_int), ("gate_per_head", ctypes.c_int)]
+
+
+# kda_gate_mode: how g_raw becomes the log-decay g (see include/kda.h)
+GATE_MODES = {"bounded": 0, "log_decay": 1, "neg_softplus": 2, "none": 3}
 
 
 def library_path() -> str:
@@ -133,9 +138,18 @@ def _check(t, name, shape, dtype, device):
         raise ValueError(f"{name} must be contiguous")
 
 
-def _params(g_min, A_log, scale):
+def _params(g_min, A_log, scale, gate_mode="bounded", gate_per_head=False):
+    if gate_mode not in GATE_MODES:
+        raise ValueError(f"gate_mode must be one of {sorted(GATE_MODES)}")
     return KdaParams(float(g_min or 0.0), None if A_log is None else A_log.data_ptr(),
-                     float(scale or 0.0))
+                     float(scale or 0.0), GATE_MODES[gate_mode], int(bool(gate_per_head)))
+
+
+def _check_gate(g_raw, lead, dk, dt, dev, gate_mode, gate_per_head):
+    """g_raw is [*lead, dk] per channel, [*lead] per head, unused with no gate."""
+    if gate_mode == "none" and g_raw is None:
+        return
+    _check(g_raw, "g_raw", tuple(lead) if gate_per_head else tuple(lead) + (dk,), dt, dev)
 
 
 def _stream_handle(device, stream):
@@ -152,17 +166,20 @@ def _raise(lib, fn, st):
 
 def kda_chunk_fwd(q, k, v, g_raw, beta, init_state=None, cu_seqlens=None, *,
                   out=None, final_state=None, output_final_state: bool = True,
-                  g_min: float = -5.0, A_log=None, scale: float = 1.0, stream=None):
+                  g_min: float = -5.0, A_log=None, scale: float = 1.0,
+                  gate_mode: str = "bounded", gate_per_head: bool = False, stream=None):
     """KDA forward over whole sequences (prefill).
 
     q, k, g_raw [B, T, H, dk]; v [B, T, H, dv]; beta [B, T, H] (all float32 or
     all bfloat16, on one CUDA device); init_state [N, H, dk, dv] float32 or
     None; cu_seqlens int32 [N+1] on the device (then B == 1) or None.
+    gate_mode: "bounded" (eq. (5)), "log_decay", "neg_softplus" or "none";
+    gate_per_head: g_raw is [B, T, H] (one gate per token and head).
     Returns (out [B, T, H, dv], final_state [N, H, dk, dv] float32 or None).
     """
     out, final_state, _ = _chunk_fwd(q, k, v, g_raw, beta, init_state, cu_seqlens, out,
                                      final_state, output_final_state, g_min, A_log, scale,
-                                     stream, 0, None, 0, "kda_chunk_fwd")
+                                     stream, 0, None, 0, "kda_chunk_fwd", gate_mode, gate_per_head)
     return out, final_state
 
 
@@ -193,6 +210,7 @@ def kda_chunk_fwd_checkpointed(q, k, v, g_raw, beta, init_state=None, cu_seqlens
                                checkpoint_every: int, checkpoints=None, out=None,
                                final_state=None, output_final_state: bool = True,
                                g_min: float = -5.0, A_log=None, scale: float = 1.0,
+                               gate_mode: str = "bounded", gate_per_head: bool = False,
                                stream=None):
     """kda_chunk_fwd that also saves the state every ``checkpoint_every``
     tokens (a positive multiple of 16) of each sequence.
@@ -211,12 +229,13 @@ def kda_chunk_fwd_checkpointed(q, k, v, g_raw, beta, init_state=None, cu_seqlens
     out, final_state, _ = _chunk_fwd(q, k, v, g_raw, beta, init_state, cu_seqlens, out,
                                      final_state, output_final_state, g_min, A_log, scale,
                                      stream, int(checkpoint_every), checkpoints, rows,
-                                     "kda_chunk_fwd_checkpointed")
+                                     "kda_chunk_fwd_checkpointed", gate_mode, gate_per_head)
     return out, final_state, checkpoints, first
 
 
 def _chunk_fwd(q, k, v, g_raw, beta, init_state, cu_seqlens, out, final_state,
-               output_final_state, g_min, A_log, scale, stream, every, ckpt, ckpt_rows, name):
+               output_final_state, g_min, A_log, scale, stream, every, ckpt, ckpt_rows, name,
+               gate_mode="bounded", gate_per_head=False):
     lib = load_library()
     dev = q.device
     if dev.type != "cuda":
@@ -225,9 +244,9 @@ def _chunk_fwd(q, k, v, g_raw, beta, init_state, cu_seqlens, out, final_state,
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     for nm, t, shp in (("q", q, (B, T, H, dk)), ("k", k, (B, T, H, dk)),
-                       ("g_raw", g_raw, (B, T, H, dk)), ("v", v, (B, T, H, dv)),
-                       ("beta", beta, (B, T, H))):
+                       ("v", v, (B, T, H, dv)), ("beta", beta, (B, T, H))):
         _check(t, nm, shp, dt, dev)
+    _check_gate(g_raw, (B, T, H), dk, dt, dev, gate_mode, gate_per_head)
     if cu_seqlens is not None:
         if cu_seqlens.dtype != torch.int32 or cu_seqlens.device != dev or cu_seqlens.dim() != 1:
             raise ValueError("cu_seqlens must be a 1-D int32 tensor on the inputs' device")
@@ -248,7 +267,7 @@ def _chunk_fwd(q, k, v, g_raw, beta, init_state, cu_seqlens, out, final_state,
         final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
     elif final_state is not None:
         _check(final_state, "final_state", (N, H, dk, dv), torch.float32, dev)
-    prm = _params(g_min, A_log, scale)
+    prm = _params(g_min, A_log, scale, gate_mode, gate_per_head)
     common = (_dtype_code(q), B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw),
               _ptr(beta), _ptr(init_state), _ptr(cu_seqlens), N, _ptr(out), _ptr(final_state))
     if ckpt is None:
@@ -262,10 +281,11 @@ def _chunk_fwd(q, k, v, g_raw, beta, init_state, cu_seqlens, out, final_state,
 
 
 def kda_decode_step(q, k, v, g_raw, beta, state, *, out=None, g_min: float = -5.0,
-                    A_log=None, scale: float = 1.0, stream=None):
+                    A_log=None, scale: float = 1.0, gate_mode: str = "bounded",
+                    gate_per_head: bool = False, stream=None):
     """Advance N sequences by one token; ``state`` [N, H, dk, dv] float32 is
-    updated in place.  q, k, g_raw [N, H, dk]; v [N, H, dv]; beta [N, H].
-    Returns out [N, H, dv]."""
+    updated in place.  q, k, g_raw [N, H, dk] (g_raw [N, H] with
+    gate_per_head); v [N, H, dv]; beta [N, H].  Returns out [N, H, dv]."""
     lib = load_library()
     dev = q.device
     if dev.type != "cuda":
@@ -273,9 +293,10 @@ def kda_decode_step(q, k, v, g_raw, beta, state, *, out=None, g_min: float = -5.
     dt = q.dtype
     N, H, dk = q.shape
     dv = v.shape[-1]
-    for name, t, shp in (("q", q, (N, H, dk)), ("k", k, (N, H, dk)), ("g_raw", g_raw, (N, H, dk)),
+    for name, t, shp in (("q", q, (N, H, dk)), ("k", k, (N, H, dk)),
                          ("v", v, (N, H, dv)), ("beta", beta, (N, H))):
         _check(t, name, shp, dt, dev)
+    _check_gate(g_raw, (N, H), dk, dt, dev, gate_mode, gate_per_head)
     _check(state, "state", (N, H, dk, dv), torch.float32, dev)
     if A_log is not None:
         _check(A_log, "A_log", (H,), torch.float32, dev)
@@ -283,7 +304,7 @@ def kda_decode_step(q, k, v, g_raw, beta, state, *, out=None, g_min: float = -5.
         out = torch.empty((N, H, dv), dtype=dt, device=dev)
     else:
         _check(out, "out", (N, H, dv), dt, dev)
-    prm = _params(g_min, A_log, scale)
+    prm = _params(g_min, A_log, scale, gate_mode, gate_per_head)
     st = lib.kda_decode_step(_dtype_code(q), N, H, dk, dv, _ptr(q), _ptr(k), _ptr(v),
                              _ptr(g_raw), _ptr(beta), _ptr(state), _ptr(out),
                              ctypes.byref(prm), _stream_handle(dev, stream))
@@ -293,7 +314,8 @@ def kda_decode_step(q, k, v, g_raw, beta, state, *, out=None, g_min: float = -5.
 
 
 def kda_decode_steps(q, k, v, g_raw, beta, state, accepted=None, *, out=None,
-                     g_min: float = -5.0, A_log=None, scale: float = 1.0, stream=None):
+                     g_min: float = -5.0, A_log=None, scale: float = 1.0,
+                     gate_mode: str = "bounded", gate_per_head: bool = False, stream=None):
     """Speculative replay: sequence n applies its first accepted[n] of K drafted
     tokens to ``state`` [N, H, dk, dv] (float32, in place) in one pass.
     q, k, g_raw [N, K, H, dk]; v [N, K, H, dv]; beta [N, K, H]; accepted int32
@@ -307,9 +329,9 @@ def kda_decode_steps(q, k, v, g_raw, beta, state, accepted=None, *, out=None,
     N, K, H, dk = q.shape
     dv = v.shape[-1]
     for name, t, shp in (("q", q, (N, K, H, dk)), ("k", k, (N, K, H, dk)),
-                         ("g_raw", g_raw, (N, K, H, dk)), ("v", v, (N, K, H, dv)),
-                         ("beta", beta, (N, K, H))):
+                         ("v", v, (N, K, H, dv)), ("beta", beta, (N, K, H))):
         _check(t, name, shp, dt, dev)
+    _check_gate(g_raw, (N, K, H), dk, dt, dev, gate_mode, gate_per_head)
     _check(state, "state", (N, H, dk, dv), torch.float32, dev)
     if accepted is not None:
         _check(accepted, "accepted", (N,), torch.int32, dev)
@@ -319,7 +341,7 @@ def kda_decode_steps(q, k, v, g_raw, beta, state, accepted=None, *, out=None,
         out = torch.zeros((N, K, H, dv), dtype=dt, device=dev)
     else:
         _check(out, "out", (N, K, H, dv), dt, dev)
-    prm = _params(g_min, A_log, scale)
+    prm = _params(g_min, A_log, scale, gate_mode, gate_per_head)
     st = lib.kda_decode_steps(_dtype_code(q), N, K, H, dk, dv, _ptr(q), _ptr(k), _ptr(v),
                               _ptr(g_raw), _ptr(beta), _ptr(accepted), _ptr(state), _ptr(out),
                               ctypes.byref(prm), _stream_handle(dev, stream))

@@ -22,8 +22,9 @@
  *     stream).  A KDA_OK return means the work was validated and enqueued.
  *   - Tensors are dense and row-major ("contiguous") in the stated shape.
  *   - Alignment (KDA_ERR_ALIGN otherwise): q, k, v, g_raw, out and the
- *     state tensors 16 bytes (they are moved by TMA / vector loads); beta
- *     and A_log to their element size; cu_seqlens to 4 bytes.
+ *     state tensors 16 bytes (they are moved by TMA / vector loads); beta,
+ *     A_log and a per-head (scalar) g_raw to their element size; cu_seqlens
+ *     and accepted to 4 bytes.
  *   - Arguments are validated on the host before any launch; a rejected
  *     call enqueues nothing and leaves every output untouched.  No call
  *     aborts, traps on the device or throws across this boundary.
@@ -59,17 +60,41 @@ typedef enum {
 } kda_dtype;
 
 /*
+ * Gate variants: how g_raw becomes the log-decay g (alpha = e^g).  The
+ * update rules before KDA and the gate it replaced ("Kimi K3: Two point
+ * eight trillion parameters, open weights, and forty-seven pages of how",
+ * §What changed between the paper and the model).
+ */
+typedef enum {
+    KDA_GATE_BOUNDED = 0,      /* eq. (5): g = g_min * Sigmoid(e^A z)             */
+    KDA_GATE_LOG_DECAY = 1,    /* g_raw is g itself (expected <= 0)              */
+    KDA_GATE_NEG_SOFTPLUS = 2, /* Kimi Linear: g = -Softplus(e^A z), unbounded   */
+    KDA_GATE_NONE = 3          /* alpha = 1: the plain delta rule; g_raw unused  */
+} kda_gate_mode;
+
+/*
  * Optional parameters.  A zero-initialised struct (or a NULL pointer)
  * selects the pages' defaults.
  *   g_min : floor of the log-decay in eq. (5); 0 selects -5.
  *   A_log : DEVICE pointer to H fp32 values, the per-head log-scale A of
  *           eq. (5) (the logit is multiplied by e^A); NULL selects A = 0.
  *   scale : factor applied to o_t; 0 selects 1.
+ *   gate_mode : a kda_gate_mode; 0 selects eq. (5).
+ *   gate_per_head : 0 = one gate per key channel (KDA, g_raw [.., H, dk]);
+ *           1 = one gate per token and head shared by every key channel
+ *           (gated delta, g_raw [.., H]).
+ * Only the default gate (bounded, per channel) runs on the tensor-core
+ * prefill; the others run on the fp32 prefill kernel.  The unbounded modes
+ * (LOG_DECAY, NEG_SOFTPLUS) evaluate the in-tile products with one
+ * exponential per position pair instead of dividing by the cumulative
+ * decay, which a 16-token tile can drive past fp32's range.
  */
 typedef struct {
     float g_min;
     const float *A_log;
     float scale;
+    int gate_mode;
+    int gate_per_head;
 } kda_params;
 
 /*
@@ -79,7 +104,8 @@ typedef struct {
  *   q, k   [B, T, H, dk]   queries and keys, used as given (already
  *                          normalised by the caller's projection chain).
  *   v      [B, T, H, dv]   values.
- *   g_raw  [B, T, H, dk]   gate pre-activation z of eq. (5).
+ *   g_raw  [B, T, H, dk]   gate pre-activation z of eq. (5) ([B, T, H] with
+ *                          gate_per_head; may be NULL with KDA_GATE_NONE).
  *   beta   [B, T, H]       write strength, already in (0, 1).
  *   init_state [N, H, dk, dv] fp32, or NULL for zeros: the state entering
  *                          each sequence (row = key channel).

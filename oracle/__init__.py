@@ -13,6 +13,12 @@ What it computes (from "Kimi K3：从三条信息流到完整系统", wineandcho
   freshly written state, as the kda_step example there fixes).
 * §下界 log-decay 是一个 kernel 设计, eq. (5): ``g = g_min *
   sigmoid(e^A z)``, ``alpha = e^g``, ``g_min = -5``.
+* Gate variants ("Kimi K3: Two point eight trillion parameters, open
+  weights, and forty-seven pages of how", §What changed between the paper
+  and the model, and the four update rules before it): Kimi Linear's
+  unbounded ``g = -softplus(e^A z)``, the gate given as ``g`` itself, no gate
+  (``alpha = 1``, the plain delta rule), and one scalar gate per (token,
+  head) shared by all key channels (gated delta).
 
 Inputs are widened to fp64 exactly (bf16 and fp32 values are representable),
 so input rounding never counts as error.  Parity status of each function is
@@ -36,6 +42,7 @@ _lib = None
 _lock = threading.Lock()
 
 G_MIN_DEFAULT = -5.0
+GATE_MODES = {"bounded": 0, "log_decay": 1, "neg_softplus": 2, "none": 3}
 
 
 def build(force: bool = False) -> str:
@@ -63,9 +70,12 @@ def _load():
             lib.kda_oracle_fwd.argtypes = [
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 dp, dp, dp, dp, dp, ip, ctypes.c_int, dp, dp,
-                ctypes.c_double, ctypes.c_double, ctypes.c_int, dp, dp, ctypes.c_int]
+                ctypes.c_double, ctypes.c_double, ctypes.c_int, ctypes.c_int, dp, dp, ctypes.c_int]
             lib.kda_oracle_gate.restype = ctypes.c_double
             lib.kda_oracle_gate.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.c_double]
+            lib.kda_oracle_log_decay.restype = ctypes.c_double
+            lib.kda_oracle_log_decay.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_double,
+                                                 ctypes.c_double]
             _lib = lib
     return _lib
 
@@ -103,24 +113,45 @@ def kda_oracle_gate(z, A_log: float = 0.0, g_min: float = G_MIN_DEFAULT):
     return out.reshape(z.shape)
 
 
+def kda_oracle_log_decay(z, gate_mode: str = "bounded", A_log: float = 0.0,
+                         g_min: float = G_MIN_DEFAULT):
+    """The log-decay g of each gate input under ``gate_mode`` (see GATE_MODES)."""
+    lib = _load()
+    mode = GATE_MODES[gate_mode]
+    z = _f64(z)
+    flat = z.reshape(-1)
+    out = np.empty_like(flat)
+    for i, zi in enumerate(flat):
+        out[i] = lib.kda_oracle_log_decay(mode, float(zi), float(A_log), float(g_min))
+    return out.reshape(z.shape)
+
+
 def kda_oracle_fwd(q, k, v, g_raw, beta, init_state=None, cu_seqlens=None, *,
                    A_log=None, g_min: float = G_MIN_DEFAULT, scale: float = 1.0,
-                   gate_is_log_decay: bool = False, nthreads: int | None = None):
+                   gate_is_log_decay: bool = False, gate_mode: str = "bounded",
+                   gate_scalar: bool = False, nthreads: int | None = None):
     """Sequential fp64 KDA forward.
 
-    Shapes: q, k, g_raw [B, T, H, dk]; v [B, T, H, dv]; beta [B, T, H];
-    init_state [N, H, dk, dv] or None (zeros); cu_seqlens [N+1] (then B == 1)
-    or None (then N = B, each batch row one sequence).  With
-    ``gate_is_log_decay`` the gate input is g = log(alpha) itself (used by
-    pins that need an exact alpha); otherwise it is z of eq. (5).
+    Shapes: q, k [B, T, H, dk]; g_raw [B, T, H, dk] ([B, T, H] with
+    ``gate_scalar``; ignored, may be None, with gate_mode "none"); v [B, T, H,
+    dv]; beta [B, T, H]; init_state [N, H, dk, dv] or None (zeros);
+    cu_seqlens [N+1] (then B == 1) or None (then N = B, each batch row one
+    sequence).  ``gate_mode`` picks the map from gate input to log-decay
+    (GATE_MODES; "bounded" is eq. (5)); ``gate_is_log_decay`` is the same as
+    gate_mode "log_decay" (the gate input is g = log(alpha) itself).
 
     Returns (out [B, T, H, dv], final_state [N, H, dk, dv]) in fp64.
     """
     lib = _load()
+    mode = GATE_MODES["log_decay" if gate_is_log_decay else gate_mode]
     q, k, v, g_raw, beta = (_f64(x) for x in (q, k, v, g_raw, beta))
     B, T, H, dk = q.shape
     dv = v.shape[-1]
-    assert k.shape == q.shape and g_raw.shape == q.shape
+    assert k.shape == q.shape
+    if mode != GATE_MODES["none"]:
+        assert g_raw.shape == ((B, T, H) if gate_scalar else q.shape)
+    else:
+        g_raw = None
     assert v.shape == (B, T, H, dv) and beta.shape == (B, T, H)
     if cu_seqlens is None:
         cu = np.arange(B + 1, dtype=np.int32) * T
@@ -141,7 +172,7 @@ def kda_oracle_fwd(q, k, v, g_raw, beta, init_state=None, cu_seqlens=None, *,
     rc = lib.kda_oracle_fwd(B * T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw),
                             _ptr(beta), cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
                             N, _ptr(S0), _ptr(Al), float(g_min), float(scale),
-                            int(bool(gate_is_log_decay)), _ptr(out), _ptr(fin), int(nt))
+                            int(mode), int(bool(gate_scalar)), _ptr(out), _ptr(fin), int(nt))
     if rc != 0:
         raise ValueError(f"kda_oracle_fwd rejected its arguments (code {rc})")
     return out, fin
@@ -149,6 +180,7 @@ def kda_oracle_fwd(q, k, v, g_raw, beta, init_state=None, cu_seqlens=None, *,
 
 def kda_oracle_decode(q, k, v, g_raw, beta, state, *, A_log=None,
                       g_min: float = G_MIN_DEFAULT, scale: float = 1.0,
+                      gate_mode: str = "bounded", gate_scalar: bool = False,
                       nthreads: int | None = None):
     """One decode step: every (sequence, head) advances by exactly one token.
 
@@ -159,7 +191,8 @@ def kda_oracle_decode(q, k, v, g_raw, beta, state, *, A_log=None,
     q, k, v, g_raw, beta = (_f64(x) for x in (q, k, v, g_raw, beta))
     N, H, dk = q.shape
     cu = np.arange(N + 1, dtype=np.int32)
-    out, fin = kda_oracle_fwd(q[None], k[None], v[None], g_raw[None], beta[None],
-                              init_state=state, cu_seqlens=cu, A_log=A_log,
-                              g_min=g_min, scale=scale, nthreads=nthreads)
+    out, fin = kda_oracle_fwd(q[None], k[None], v[None], None if g_raw is None else g_raw[None],
+                              beta[None], init_state=state, cu_seqlens=cu, A_log=A_log,
+                              g_min=g_min, scale=scale, gate_mode=gate_mode,
+                              gate_scalar=gate_scalar, nthreads=nthreads)
     return out[0], fin

@@ -17,6 +17,23 @@
  *         of the freshly written state.
  *       - §下界 log-decay 是一个 kernel 设计, eq. (5):
  *           g_t = g_min * Sigmoid(e^A z_t),  alpha_t = e^{g_t},  g_min = -5.
+ *         and, in the same section, the gate it replaced: Kimi Linear's
+ *         unbounded negative-softplus log-decay.
+ *   [K] "Kimi K3: Two point eight trillion parameters, open weights, and
+ *       forty-seven pages of how", §What changed between the paper and the
+ *       model (the negative softplus) and the four update rules before it:
+ *       the delta rule (no decay), gated delta (one scalar decay per step),
+ *       KDA (one decay per key channel).
+ *
+ * Gate variants (gate_mode), the readings taken where the pages give no
+ * formula:
+ *   0  bounded:       g = g_min * Sigmoid(e^A z)                 (eq. (5))
+ *   1  log-decay:     the gate input is g itself
+ *   2  neg-softplus:  g = -Softplus(e^A z) = -log(1 + e^{e^A z}), unbounded
+ *                     (the per-head scale enters as in eq. (5))
+ *   3  none:          g = 0, alpha = 1: the plain delta rule (gate unused)
+ * gate_scalar = 1: one gate value per (token, head), shared by every key
+ * channel (gated delta); the gate array is then [total_T, H].
  *
  * Layout: token-major packed sequences, [total_T, H, d] row-major, with
  * cu_seqlens[N+1] (host) splitting the token axis into N independent
@@ -45,33 +62,53 @@ double kda_oracle_gate(double z, double A_log, double g_min)
     return g_min * sig;
 }
 
+/* log(1 + e^x) without overflow: max(x, 0) + log(1 + e^{-|x|}). */
+static double softplus(double x)
+{
+    return (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x)));
+}
+
+/* The log-decay g of one gate input under each gate mode. */
+double kda_oracle_log_decay(int gate_mode, double z, double A_log, double g_min)
+{
+    switch (gate_mode) {
+    case 0: return kda_oracle_gate(z, A_log, g_min);
+    case 1: return z;
+    case 2: return -softplus(exp(A_log) * z);
+    default: return 0.0;
+    }
+}
+
 /*
  * One (sequence, head) chain, tokens t = 0..len-1.
- *   q, k, gate : element (t, c) at [t * tok_stride + c]
+ *   q, k       : element (t, c) at [t * tok_stride + c]
+ *   gate       : element (t, c) at [t * gate_stride + c * gate_cstride]
+ *                (gate_cstride = 0: one value per token, all channels)
  *   v          : element (t, j) at [t * tok_stride_v + j]
  *   beta       : element t at [t * beta_stride]
  *   out        : element (t, j) at [t * tok_stride_v + j]
  *   S          : dk x dv row-major, updated in place (entering -> final state)
- * gate_is_log_decay = 0: gate holds z, mapped through eq. (5);
- * gate_is_log_decay = 1: gate holds g = log(alpha) directly.
+ * gate_mode: see the header (0 = eq. (5)).
  */
 static void chain(int len, int dk, int dv,
                   const double *q, const double *k, const double *v,
                   const double *gate, const double *beta,
                   ptrdiff_t tok_stride, ptrdiff_t tok_stride_v, ptrdiff_t beta_stride,
-                  double A_log, double g_min, double scale, int gate_is_log_decay,
+                  ptrdiff_t gate_stride, ptrdiff_t gate_cstride,
+                  double A_log, double g_min, double scale, int gate_mode,
                   double *S, double *out, double *alpha, double *e)
 {
     for (int t = 0; t < len; ++t) {
         const double *qt = q + (ptrdiff_t)t * tok_stride;
         const double *kt = k + (ptrdiff_t)t * tok_stride;
         const double *vt = v + (ptrdiff_t)t * tok_stride_v;
-        const double *zt = gate + (ptrdiff_t)t * tok_stride;
+        const double *zt = gate ? gate + (ptrdiff_t)t * gate_stride : NULL;
         const double bt = beta[(ptrdiff_t)t * beta_stride];
 
         /* step 1-2: per-channel retention alpha_c = exp(g_c) */
         for (int c = 0; c < dk; ++c) {
-            double g = gate_is_log_decay ? zt[c] : kda_oracle_gate(zt[c], A_log, g_min);
+            double g = zt ? kda_oracle_log_decay(gate_mode, zt[(ptrdiff_t)c * gate_cstride], A_log, g_min)
+                          : 0.0;
             alpha[c] = exp(g);
         }
         /* step 3: decay row c of S (key channel c) by alpha_c */
@@ -105,7 +142,7 @@ typedef struct {
     const double *q, *k, *v, *gate, *beta, *init_state, *A_log;
     const int32_t *cu;
     double g_min, scale;
-    int gate_is_log_decay;
+    int gate_mode, gate_scalar;
     double *out, *final_state;
     const int *order;       /* chain indices, longest sequence first */
     int n_chains;
@@ -126,9 +163,20 @@ static void run_one(job_t *J, int ch, double *alpha, double *e)
     const ptrdiff_t tok = (ptrdiff_t)J->H * sdk, tokv = (ptrdiff_t)J->H * sdv;
     const ptrdiff_t base = (ptrdiff_t)bos * tok + (ptrdiff_t)h * sdk;
     const ptrdiff_t basev = (ptrdiff_t)bos * tokv + (ptrdiff_t)h * sdv;
-    chain(len, J->dk, J->dv, J->q + base, J->k + base, J->v + basev, J->gate + base,
-          J->beta + (ptrdiff_t)bos * J->H + h, tok, tokv, J->H,
-          J->A_log ? J->A_log[h] : 0.0, J->g_min, J->scale, J->gate_is_log_decay,
+    const double *gate = NULL;
+    ptrdiff_t gstride = tok, gcstride = 1;
+    if (J->gate_mode != 3) {
+        if (J->gate_scalar) {
+            gate = J->gate + (ptrdiff_t)bos * J->H + h;
+            gstride = J->H;
+            gcstride = 0;
+        } else {
+            gate = J->gate + base;
+        }
+    }
+    chain(len, J->dk, J->dv, J->q + base, J->k + base, J->v + basev, gate,
+          J->beta + (ptrdiff_t)bos * J->H + h, tok, tokv, J->H, gstride, gcstride,
+          J->A_log ? J->A_log[h] : 0.0, J->g_min, J->scale, J->gate_mode,
           S, J->out + basev, alpha, e);
 }
 
@@ -165,11 +213,12 @@ int kda_oracle_fwd(int total_T, int H, int dk, int dv,
                    const double *gate, const double *beta,
                    const int32_t *cu_seqlens, int N,
                    const double *init_state, const double *A_log,
-                   double g_min, double scale, int gate_is_log_decay,
+                   double g_min, double scale, int gate_mode, int gate_scalar,
                    double *out, double *final_state, int nthreads)
 {
     if (total_T < 0 || H <= 0 || dk <= 0 || dv <= 0 || N <= 0 || !cu_seqlens ||
-        !final_state || (total_T > 0 && (!q || !k || !v || !gate || !beta || !out)))
+        !final_state || gate_mode < 0 || gate_mode > 3 ||
+        (total_T > 0 && (!q || !k || !v || (!gate && gate_mode != 3) || !beta || !out)))
         return 1;
     if (cu_seqlens[0] != 0 || cu_seqlens[N] != total_T) return 2;
     for (int n = 0; n < N; ++n)
@@ -179,7 +228,7 @@ int kda_oracle_fwd(int total_T, int H, int dk, int dv,
     J.H = H; J.dk = dk; J.dv = dv; J.N = N;
     J.q = q; J.k = k; J.v = v; J.gate = gate; J.beta = beta;
     J.init_state = init_state; J.A_log = A_log; J.cu = cu_seqlens;
-    J.g_min = g_min; J.scale = scale; J.gate_is_log_decay = gate_is_log_decay;
+    J.g_min = g_min; J.scale = scale; J.gate_mode = gate_mode; J.gate_scalar = gate_scalar;
     J.out = out; J.final_state = final_state;
     J.n_chains = N * H;
     J.next = 0;

@@ -56,8 +56,9 @@ def assert_close(name, gpu, ref, tol):
     return e
 
 
-def oracle_heads(inp, heads, A_log=None, scale=1.0, g_min=-5.0):
-    """Run the oracle on a subset of heads of a prefill input dict.
+def oracle_heads(inp, heads, A_log=None, scale=1.0, g_min=-5.0, **gate_kw):
+    """Run the oracle on a subset of heads of a prefill input dict (gate_kw:
+    gate_mode / gate_scalar of the oracle).
     Returns (out [B, T, len(heads), dv], final [N, len(heads), dk, dv])."""
     hs = list(heads)
     sl = lambda t: None if t is None else t[:, :, hs].contiguous().cpu()
@@ -68,4 +69,4 @@ def oracle_heads(inp, heads, A_log=None, scale=1.0, g_min=-5.0):
     Al = None if A_log is None else A_log[hs].cpu()
     return oracle.kda_oracle_fwd(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["g_raw"]),
                                  inp["beta"][:, :, hs].contiguous().cpu(), init, cu,
-                                 A_log=Al, scale=scale, g_min=g_min)
+                                 A_log=Al, scale=scale, g_min=g_min, **gate_kw)

@@ -444,3 +444,100 @@ def test_pins_catch_planted_mistakes(kind):
     o2, _ = mut(k, k, v, g, np.ones(12), S0)
     ok_invariant = np.allclose(o2, v)
     assert not (ok_example and ok_invariant)
+
+
+# ----------------------------------------------------------------- gate variants
+
+def _run_mode(q, k, v, z, beta, S0=None, mode="bounded", scalar=False, **kw):
+    """Single chain with an explicit gate mode; z [T, dk] or [T] (scalar)."""
+    out, fin = oracle.kda_oracle_fwd(q[None, :, None], k[None, :, None], v[None, :, None],
+                                     None if z is None else z[None, :, None], beta[None, :, None],
+                                     init_state=None if S0 is None else S0[None, None],
+                                     gate_mode=mode, gate_scalar=scalar, **kw)
+    return out[0, :, 0], fin[0, 0]
+
+
+def test_neg_softplus_gate_closed_forms():
+    """Kimi Linear's negative softplus: g(0) = -log 2, g -> -z for large z
+    (unbounded below), g -> -e^z for very negative z, and the per-head scale
+    multiplies the input as in eq. (5)."""
+    g = oracle.kda_oracle_log_decay(np.array([0.0, 40.0, 100.0, -40.0, 2.0]), "neg_softplus")
+    np.testing.assert_allclose(g[0], -math.log(2.0), rtol=1e-15)
+    np.testing.assert_allclose(g[1], -40.0, rtol=1e-15)
+    assert g[2] == -100.0                       # no floor: far below g_min = -5
+    np.testing.assert_allclose(g[3], -math.exp(-40.0), rtol=1e-12)
+    np.testing.assert_allclose(g[4], -math.log1p(math.exp(2.0)), rtol=1e-15)
+    ga = oracle.kda_oracle_log_decay(np.array([1.5]), "neg_softplus", A_log=0.7)
+    gb = oracle.kda_oracle_log_decay(np.array([1.5 * math.exp(0.7)]), "neg_softplus")
+    np.testing.assert_allclose(ga, gb, rtol=1e-15)
+    assert oracle.kda_oracle_log_decay(np.array([3.0]), "log_decay")[0] == 3.0
+    assert oracle.kda_oracle_log_decay(np.array([3.0]), "none")[0] == 0.0
+
+
+def test_no_gate_is_the_plain_delta_rule():
+    """gate mode "none" (alpha = 1): orthonormal keys with beta = 1 from S_0 =
+    0 recall every stored value exactly, the textbook delta-rule property;
+    and it equals a log-decay gate of 0."""
+    rng = np.random.default_rng(41)
+    d, T = 16, 12
+    Qm, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    k = Qm[:T].copy()
+    v = rng.standard_normal((T, d))
+    out, fin = _run_mode(k, k, v, None, np.ones(T), mode="none")
+    np.testing.assert_allclose(out, v, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(fin, k.T @ v, rtol=0, atol=1e-12)
+    q = rng.standard_normal((T, d))
+    beta = rng.uniform(0, 1, T)
+    S0 = rng.standard_normal((d, d))
+    a = _run_mode(q, k, v, None, beta, S0, mode="none")
+    b = _run_mode(q, k, v, np.zeros((T, d)), beta, S0, mode="log_decay")
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("mode", ["bounded", "neg_softplus", "log_decay"])
+def test_scalar_gate_is_the_channel_gate_broadcast(mode):
+    """Gated delta: one gate per token shared by all key channels equals the
+    per-channel gate with that value in every channel."""
+    rng = np.random.default_rng(43)
+    T, dk, dv = 9, 6, 5
+    q, k, v, _, beta = rand_chain(rng, T, dk, dv)
+    z = rng.uniform(-3, 3, T) if mode != "log_decay" else rng.uniform(-4, 0, T)
+    S0 = rng.standard_normal((dk, dv))
+    a = _run_mode(q, k, v, z, beta, S0, mode=mode, scalar=True, A_log=np.array([0.3]))
+    b = _run_mode(q, k, v, np.repeat(z[:, None], dk, 1), beta, S0, mode=mode,
+                  A_log=np.array([0.3]))
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_scalar_gated_delta_brute_force():
+    """Gated delta in matrix form, S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1}
+    + beta_t k_t v_t^T with a scalar alpha_t = exp(g_t), on tiny inputs."""
+    rng = np.random.default_rng(44)
+    T, dk, dv = 7, 4, 3
+    q, k, v, _, beta = rand_chain(rng, T, dk, dv, unit=False)
+    z = rng.uniform(-6, 6, T)
+    S0 = rng.standard_normal((dk, dv))
+    out, fin = _run_mode(q, k, v, z, beta, S0, mode="neg_softplus", scalar=True)
+    S = S0.copy()
+    for t in range(T):
+        alpha = math.exp(-math.log1p(math.exp(z[t])))          # = 1 / (1 + e^z)
+        S = alpha * (np.eye(dk) - beta[t] * np.outer(k[t], k[t])) @ S + beta[t] * np.outer(k[t], v[t])
+        np.testing.assert_allclose(out[t], S.T @ q[t], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(fin, S, rtol=0, atol=1e-12)
+
+
+def test_unbounded_decay_wipes_the_state():
+    """A negative-softplus gate with z = 60 gives alpha = e^{-60} per step:
+    every step forgets the past (the carried term is ~1e-26), so S_t = beta_t
+    k_t v_t^T and o_t = beta_t (k_t . q_t) v_t up to rounding.  Over a 16-token tile the cumulative
+    log-decay reaches -960, far past the bounded gate's -80."""
+    rng = np.random.default_rng(45)
+    T, dk, dv = 20, 8, 5
+    q, k, v, _, beta = rand_chain(rng, T, dk, dv)
+    S0 = rng.standard_normal((dk, dv))
+    out, fin = _run_mode(q, k, v, np.full((T, dk), 60.0), beta, S0, mode="neg_softplus")
+    for t in range(T):
+        np.testing.assert_allclose(out[t], beta[t] * (k[t] @ q[t]) * v[t], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(fin, beta[-1] * np.outer(k[-1], v[-1]), rtol=1e-13, atol=1e-15)
