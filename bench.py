@@ -11,6 +11,11 @@ prefill inputs, 1.6 GB of decode state), so no L2 flush is needed.
 value      : prefill tokens/s (token positions, all 96 heads each), timed over
              the prefill launches with CUDA events on the launching stream.
 decode     : state GB/s of the decode step (2 * N*H*dk*dv*4 bytes per step).
+prep / post: the passes around the operator on the same 237,568 tokens x 96
+             heads: kda_qkv_prep (ShortConv + Swish + L2Norm of q, k, v and
+             Sigmoid of beta) and kda_output_gate (Sigmoid(gate) * RMSNorm(o)),
+             each timed after the main region: HBM GB/s of the bytes each
+             pass must move.
 spec_replay: speculative replay (kda_decode_steps) of 256 sequences x 8
              verified tokens with 1..8 accepted, timed after the main region:
              algorithmic GB/s (state once in and out + the applied tokens'
@@ -32,6 +37,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import itertools
 import json
 import os
 import statistics
@@ -71,7 +77,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "spec"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "spec", "prep", "post"],
+                    default="all",
                     help="run one leg only (for profiling captures; the JSON line needs 'all')")
     ap.add_argument("--prefill-workload", default="varlen_bf16_H96_237568",
                     choices=[k for k, w in kin.WORKLOADS.items() if w.kind == "prefill" and w.dtype == "bf16"],
@@ -282,6 +289,15 @@ def run_single_leg(args, kda, dev):
         S = kin.make_decode_state(w, device=dev)
         t = kin.make_decode_token(w, 0, device=dev)
         fn = lambda i: kda.kda_decode_step(t["q"], t["k"], t["v"], t["g_raw"], t["beta"], S)
+    elif args.only == "prep":
+        w = PREFILL
+        pi = kin.make_prep_inputs(w.total_tokens, w.H, w.dk, "bf16", device=dev)
+        cu = torch.tensor([0] + list(itertools.accumulate(w.seqlens)), dtype=torch.int32, device=dev)
+        fn = lambda i: kda.kda_qkv_prep(pi["x_qkv"], pi["conv_w"], pi["beta_logit"], cu)
+    elif args.only == "post":
+        w = PREFILL
+        po = kin.make_post_inputs(w.total_tokens * w.H, w.dv, "bf16", device=dev)
+        fn = lambda i: kda.kda_output_gate(po["o"], po["gate"], po["norm_w"])
     else:
         w = SPEC
         S = kin.make_decode_state(w, device=dev)
@@ -397,6 +413,7 @@ def run_ours(args, rank, world, local):
     d_traffic = recorded_traffic("decode", decode_src)
 
     spec = run_spec(kda, dev, rank, world, args.steps, args.warmup, hbm_peak, peak_src)
+    prep, post = run_prepost(kda, dev, world, min(args.steps, 10), args.warmup, hbm_peak, peak_src)
 
     e2e = None
     if not args.no_e2e:   # every rank: the timing is reduced over ranks
@@ -436,7 +453,7 @@ def run_ours(args, rank, world, local):
                    "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": d_gbs,
                                 "peak": hbm_peak, "unit": "GB/s", "frac": d_gbs / hbm_peak,
                                 "traffic": d_traffic, "peak_source": peak_src}},
-        "spec_replay": spec,
+        "spec_replay": spec, "prep": prep, "post": post,
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches,
         "clocks": clocks, "wall_s_timed": t_wall,
     }
@@ -479,6 +496,46 @@ def run_spec(kda, dev, rank, world, steps, warmup, hbm_peak, peak_src):
             "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": gbs,
                          "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
                          "algorithmic_bytes_per_launch": alg, "peak_source": peak_src}}
+
+
+def run_prepost(kda, dev, world, steps, warmup, hbm_peak, peak_src):
+    """The pre/post passes on the varlen workload's tokens and heads."""
+    w = PREFILL
+    T, H, d = w.total_tokens, w.H, w.dk
+    stream = torch.cuda.current_stream(dev)
+    cu = torch.tensor([0] + list(itertools.accumulate(w.seqlens)), dtype=torch.int32, device=dev)
+
+    def measure(fn, nbytes, kernel):
+        for i in range(warmup):
+            fn(i)
+        barrier(world)
+        torch.cuda.synchronize()
+        evs = time_region(fn, steps, stream)
+        torch.cuda.synchronize()
+        ms = reduce_max(statistics.fmean(a.elapsed_time(b) for a, b in evs), world)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"ms": ms, "roofline": {"kernel": kernel, "bound": "hbm", "achieved": gbs,
+                                       "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                                       "algorithmic_bytes_per_launch": nbytes,
+                                       "peak_source": peak_src}}
+
+    pi = kin.make_prep_inputs(T, H, d, "bf16", device=dev)
+    outs = [torch.empty((1, T, H, d), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    beta = torch.empty((1, T, H), dtype=torch.bfloat16, device=dev)
+    fn = lambda i: kda.kda_qkv_prep(pi["x_qkv"], pi["conv_w"], pi["beta_logit"], cu,
+                                    out=(*outs, beta))
+    prep_bytes = 2 * (3 * T * H * d * 2) + 2 * T * H * 2 + 3 * H * d * 16
+    prep = measure(fn, prep_bytes, "prep_kernel")
+    prep.update({"tokens": T, "H": H, "d": d})
+    del pi, outs, beta
+    po = kin.make_post_inputs(T * H, d, "bf16", device=dev)
+    y = torch.empty_like(po["o"])
+    fn = lambda i: kda.kda_output_gate(po["o"], po["gate"], po["norm_w"], out=y)
+    post = measure(fn, 3 * T * H * d * 2 + d * 4, "output_gate_kernel")
+    post.update({"rows": T * H, "d": d})
+    del po, y
+    torch.cuda.empty_cache()
+    return prep, post
 
 
 def run_e2e(kda, q, k, v, g, b, cu, out, fin, steps, world, T_total):

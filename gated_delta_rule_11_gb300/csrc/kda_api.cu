@@ -215,4 +215,57 @@ kda_status kda_decode_step(kda_dtype dt, int N, int H, int dk, int dv,
     return kda_decode_steps(dt, N, 1, H, dk, dv, q, k, v, g_raw, beta, nullptr, state, out, p, stream);
 }
 
+kda_status kda_qkv_prep(kda_dtype dt, int B, int T, int H, int d,
+                        const void *x_qkv, const float *conv_w, const void *beta_logit,
+                        const int32_t *cu_seqlens, int N,
+                        const void *conv_state_in, void *conv_state_out,
+                        void *q, void *k, void *v, void *beta,
+                        float l2_eps, kda_stream_t stream) {
+    if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_DTYPE;
+    if (B < 0 || T < 0 || H <= 0 || N < 0) return KDA_ERR_ARG;
+    if (!head_dim_ok(d)) return KDA_ERR_SHAPE;
+    if (cu_seqlens) {
+        if (B != 1 || N < 1) return KDA_ERR_ARG;
+    } else if (N != B) {
+        return KDA_ERR_ARG;
+    }
+    const long long total = static_cast<long long>(B) * T;
+    if (total > INT32_MAX || static_cast<long long>(N) * 3 * H * d > INT32_MAX) return KDA_ERR_ARG;
+    if (total > 0 && (!x_qkv || !conv_w || !q || !k || !v)) return KDA_ERR_ARG;
+    if ((beta_logit == nullptr) != (beta == nullptr)) return KDA_ERR_ARG;
+    const void *ptrs[] = {x_qkv, conv_w, conv_state_in, conv_state_out, q, k, v};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return KDA_ERR_ALIGN;
+    const uintptr_t es = dt == KDA_F32 ? 4 : 2;
+    if (!aligned_to(beta_logit, es) || !aligned_to(beta, es) || !aligned_to(cu_seqlens, 4))
+        return KDA_ERR_ALIGN;
+    if (N == 0 || (total == 0 && !conv_state_out)) return KDA_OK;
+    kda::PrepArgs a;
+    a.x = x_qkv; a.conv_w = conv_w; a.beta_logit = beta_logit;
+    a.cu_seqlens = cu_seqlens;
+    a.state_in = conv_state_in; a.state_out = conv_state_out;
+    a.q = q; a.k = k; a.v = v; a.beta = beta;
+    a.N = N; a.H = H; a.T_total = static_cast<int>(total); a.T_seq = T;
+    a.l2_eps = l2_eps > 0.f ? l2_eps : 1e-6f;
+    return from_cuda(kda::launch_prep(dt, d, a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_output_gate(kda_dtype dt, long long rows, int d, const void *o, const void *gate,
+                           const float *norm_w, float eps, void *y, kda_stream_t stream) {
+    if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_DTYPE;
+    if (rows < 0) return KDA_ERR_ARG;
+    if (!head_dim_ok(d)) return KDA_ERR_SHAPE;
+    if (rows == 0) return KDA_OK;
+    if (!o || !gate || !y) return KDA_ERR_ARG;
+    const void *ptrs[] = {o, gate, y};
+    for (const void *ptr : ptrs)
+        if (!aligned16(ptr)) return KDA_ERR_ALIGN;
+    if (!aligned_to(norm_w, 4)) return KDA_ERR_ALIGN;
+    kda::PostArgs a;
+    a.o = o; a.gate = gate; a.norm_w = norm_w; a.y = y;
+    a.rows = rows;
+    a.eps = eps > 0.f ? eps : 1e-5f;
+    return from_cuda(kda::launch_output_gate(dt, d, a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -68,6 +68,31 @@ __device__ __forceinline__ float log_decay_fast(float z, float escale, float g_m
     return g_min * __frcp_rn(1.0f + __expf(-escale * z));
 }
 
+// Pre/post passes.  prep: x [T, 3, H, d] (q | k | v projections), conv_w
+// [3, H, d, 4] fp32, beta_logit [T, H], conv states [N, 3, 3, H, d] (the
+// last three tokens' x, oldest first); outputs q, k, v [T, H, d], beta
+// [T, H].  post: o, gate, y [rows, d], norm_w [d] fp32.
+struct PrepArgs {
+    const void *x;
+    const float *conv_w;
+    const void *beta_logit;
+    const int32_t *cu_seqlens;
+    const void *state_in;
+    void *state_out;
+    void *q, *k, *v, *beta;
+    int N, H, T_total, T_seq;
+    float l2_eps;
+};
+struct PostArgs {
+    const void *o, *gate;
+    const float *norm_w;
+    void *y;
+    long long rows;
+    float eps;
+};
+cudaError_t launch_prep(kda_dtype dt, int d, const PrepArgs &a, cudaStream_t s);
+cudaError_t launch_output_gate(kda_dtype dt, int d, const PostArgs &a, cudaStream_t s);
+
 // Log-decay g of one gate input under each kda_gate_mode.  The negative
 // softplus is -(max(x, 0) + log(1 + e^-|x|)), which never overflows.
 __device__ __forceinline__ float gate_log_decay(int mode, float z, float escale, float g_min) {

@@ -1,0 +1,310 @@
+// The passes on either side of the KDA operator ("Kimi K3：从三条信息流到完整系统",
+// §从投影到 Chunkwise 的完整接口, eq. (2), and §下界 log-decay 是一个 kernel 设计,
+// eq. (6)):
+//
+//   prep : q, k = L2Norm(Swish(ShortConv(x_q|k))),  v = Swish(ShortConv(x_v)),
+//          beta = Sigmoid(beta_logit)
+//   post : y = Sigmoid(gate) * RMSNorm(o)            (before the W_o projection)
+//
+// The projections W x themselves are plain GEMMs and stay outside.  ShortConv
+// is the causal depthwise convolution of kernel size 4 along the tokens of
+// each sequence (the model's short_conv_kernel_size):
+//   y_t[ch] = sum_{i=0..3} w[ch][i] * x_{t-3+i}[ch],
+// with x before a sequence's first token taken from the caller's conv state
+// (the last three inputs of the previous call) or zero.  L2Norm divides each
+// head's d channels by sqrt(sum x^2 + eps); RMSNorm divides by
+// sqrt(mean x^2 + eps) and multiplies by a per-channel weight shared by the
+// heads.
+//
+// Both passes are HBM-bound streams.  prep: one warp owns a run of up to
+// 64 consecutive tokens of one (tensor, head); each lane holds d / 32
+// channels and keeps the three previous inputs of its channels in registers,
+// so every input element is read once (plus a three-token halo per run);
+// the L2 norm is a warp reduction.  Loads are issued four tokens at a time;
+// the register budget keeps three CTAs (24 warps) per SM, which measured
+// faster than deeper per-warp prefetch at two CTAs per SM.
+// post: one warp per (token, head) row, four rows per warp in flight.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kRun = 64;          // tokens per prep warp task
+constexpr int kWarps = 8;         // warps per CTA
+
+template <typename T, int CPL> struct Lanes;
+template <> struct Lanes<__nv_bfloat16, 4> {
+    static __device__ __forceinline__ void load(const __nv_bfloat16 *p, float (&x)[4]) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2 *>(p));
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&w.x);
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&w.y);
+        x[0] = __low2float(a); x[1] = __high2float(a); x[2] = __low2float(b); x[3] = __high2float(b);
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16 *p, const float (&x)[4]) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]), b = __floats2bfloat162_rn(x[2], x[3]);
+        uint2 w;
+        w.x = *reinterpret_cast<const uint32_t *>(&a);
+        w.y = *reinterpret_cast<const uint32_t *>(&b);
+        *reinterpret_cast<uint2 *>(p) = w;
+    }
+};
+template <> struct Lanes<float, 4> {
+    static __device__ __forceinline__ void load(const float *p, float (&x)[4]) {
+        const float4 w = __ldg(reinterpret_cast<const float4 *>(p));
+        x[0] = w.x; x[1] = w.y; x[2] = w.z; x[3] = w.w;
+    }
+    static __device__ __forceinline__ void store(float *p, const float (&x)[4]) {
+        *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    }
+};
+template <typename T, int CPL> struct LanesScalar {
+    static __device__ __forceinline__ void load(const T *p, float (&x)[CPL]) {
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) x[i] = ld_in(p + i);
+    }
+    static __device__ __forceinline__ void store(T *p, const float (&x)[CPL]) {
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) st_out(p + i, x[i]);
+    }
+};
+template <> struct Lanes<__nv_bfloat16, 2> : LanesScalar<__nv_bfloat16, 2> {};
+template <> struct Lanes<__nv_bfloat16, 1> : LanesScalar<__nv_bfloat16, 1> {};
+template <> struct Lanes<float, 2> : LanesScalar<float, 2> {};
+template <> struct Lanes<float, 1> : LanesScalar<float, 1> {};
+
+__device__ __forceinline__ float swish(float x) { return x / (1.0f + expf(-x)); }
+__device__ __forceinline__ float sigmoid(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Sequence of token t: the n with cu[n] <= t < cu[n+1] (binary search over
+// the clamped spans; empty sequences are skipped).
+__device__ __forceinline__ int seq_of(const PrepArgs &a, int t) {
+    if (!a.cu_seqlens) return t / a.T_seq;
+    int lo = 0, hi = a.N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (min(max(a.cu_seqlens[mid], 0), a.T_total) <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+__device__ __forceinline__ void span_of(const PrepArgs &a, int n, int &bos, int &eos) {
+    if (a.cu_seqlens) {
+        bos = min(max(a.cu_seqlens[n], 0), a.T_total);
+        eos = min(max(a.cu_seqlens[n + 1], bos), a.T_total);
+    } else {
+        bos = n * a.T_seq;
+        eos = bos + a.T_seq;
+    }
+}
+
+template <typename Tin, int D>
+__global__ void __launch_bounds__(kWarps * 32) prep_kernel(PrepArgs a) {
+    constexpr int CPL = D / 32;                 // channels per lane
+    const int lane = threadIdx.x & 31;
+    const long long task = static_cast<long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    const int H = a.H;
+    const long long row_tasks = static_cast<long long>(3) * H;     // (tensor, head) pairs
+    const long long run_tasks = static_cast<long long>((a.T_total + kRun - 1) / kRun) * row_tasks;
+    const Tin *x = static_cast<const Tin *>(a.x);
+    const Tin *sin = static_cast<const Tin *>(a.state_in);
+    Tin *sout = static_cast<Tin *>(a.state_out);
+    const size_t tok_x = static_cast<size_t>(3) * H * D;             // one token of x_qkv
+
+    if (task >= run_tasks) {
+        // conv state of an empty sequence passes through (or becomes zero)
+        const long long et = task - run_tasks;
+        if (et >= static_cast<long long>(a.N) * row_tasks || !sout) return;
+        const int n = static_cast<int>(et / row_tasks);
+        const int mh = static_cast<int>(et % row_tasks);
+        int bos, eos;
+        span_of(a, n, bos, eos);
+        if (eos > bos) return;
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            const size_t o = (static_cast<size_t>(n) * 3 + j) * tok_x + static_cast<size_t>(mh) * D + lane * CPL;
+            float w[CPL];
+            if (sin) Lanes<Tin, CPL>::load(sin + o, w);
+            else
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) w[i] = 0.f;
+            Lanes<Tin, CPL>::store(sout + o, w);
+        }
+        return;
+    }
+
+    const int run = static_cast<int>(task / row_tasks);
+    const int mh = static_cast<int>(task % row_tasks);     // m * H + h
+    const int m = mh / H, h = mh % H;
+    const int t_begin = run * kRun, t_end = min(t_begin + kRun, a.T_total);
+    const size_t col = static_cast<size_t>(mh) * D + lane * CPL;   // this lane's channels in a token of x
+
+    // conv taps of this lane's channels: w[ch][0..3], tap 3 = current token
+    float wt[CPL][4];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+        const float4 w4 = __ldg(reinterpret_cast<const float4 *>(a.conv_w) + static_cast<size_t>(mh) * D + lane * CPL + i);
+        wt[i][0] = w4.x; wt[i][1] = w4.y; wt[i][2] = w4.z; wt[i][3] = w4.w;
+    }
+    Tin *dst = static_cast<Tin *>(m == 0 ? a.q : (m == 1 ? a.k : a.v));
+    const size_t tok_o = static_cast<size_t>(H) * D;
+
+    int n = seq_of(a, t_begin), bos, eos;
+    span_of(a, n, bos, eos);
+    while (eos <= t_begin && n + 1 < a.N) {      // empty sequences at t_begin
+        ++n;
+        span_of(a, n, bos, eos);
+    }
+    // window: x of the three tokens before the current one (win[0] oldest)
+    float win[3][CPL];
+    auto fill_window = [&](int t) {              // window for token t of sequence n (bos <= t)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            const int p = t - 3 + j;
+            if (p >= bos) {
+                Lanes<Tin, CPL>::load(x + static_cast<size_t>(p) * tok_x + col, win[j]);
+            } else if (sin) {
+                const int tap = p - bos + 3;     // 0..2: state token bos - 3 + tap
+                Lanes<Tin, CPL>::load(sin + (static_cast<size_t>(n) * 3 + tap) * tok_x + col, win[j]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) win[j][i] = 0.f;
+            }
+        }
+    };
+    fill_window(t_begin);
+
+    for (int t0 = t_begin; t0 < t_end; t0 += 4) {
+        float xs[4][CPL];                         // this batch's inputs
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (t0 + u < t_end) Lanes<Tin, CPL>::load(x + static_cast<size_t>(t0 + u) * tok_x + col, xs[u]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int t = t0 + u;
+            if (t >= t_end) break;
+            if (t >= eos) {                       // next sequence: restart the window
+                do {
+                    ++n;
+                    span_of(a, n, bos, eos);
+                } while (eos <= t && n + 1 < a.N);
+                fill_window(t);
+            }
+            float y[CPL];
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) {
+                const float c = wt[i][0] * win[0][i] + wt[i][1] * win[1][i] + wt[i][2] * win[2][i] +
+                                wt[i][3] * xs[u][i];
+                y[i] = swish(c);
+                ss += y[i] * y[i];
+                win[0][i] = win[1][i];
+                win[1][i] = win[2][i];
+                win[2][i] = xs[u][i];
+            }
+            if (m < 2) {                          // q, k: L2Norm over the head's d channels
+                const float r = rsqrtf(warp_sum(ss) + a.l2_eps);
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) y[i] *= r;
+            }
+            Lanes<Tin, CPL>::store(dst + static_cast<size_t>(t) * tok_o + static_cast<size_t>(h) * D + lane * CPL, y);
+            if (t == eos - 1 && sout) {           // last token: save the window as conv state
+#pragma unroll
+                for (int j = 0; j < 3; ++j)
+                    Lanes<Tin, CPL>::store(sout + (static_cast<size_t>(n) * 3 + j) * tok_x + col, win[j]);
+            }
+        }
+    }
+    // beta = Sigmoid(logit) for this run's tokens and head h (the q-tensor warps)
+    if (m == 0 && a.beta_logit) {
+        const Tin *bl = static_cast<const Tin *>(a.beta_logit);
+        Tin *bo = static_cast<Tin *>(a.beta);
+        for (int t = t_begin + lane; t < t_end; t += 32)
+            st_out(bo + static_cast<size_t>(t) * H + h, sigmoid(ld_in(bl + static_cast<size_t>(t) * H + h)));
+    }
+}
+
+template <typename Tin, int D>
+__global__ void __launch_bounds__(kWarps * 32) output_gate_kernel(PostArgs a) {
+    constexpr int CPL = D / 32;
+    constexpr int RPW = 4;                       // rows per warp
+    const int lane = threadIdx.x & 31;
+    const long long row0 = (static_cast<long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5)) * RPW;
+    const Tin *o = static_cast<const Tin *>(a.o);
+    const Tin *g = static_cast<const Tin *>(a.gate);
+    Tin *y = static_cast<Tin *>(a.y);
+    float w[CPL];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) w[i] = a.norm_w ? __ldg(a.norm_w + lane * CPL + i) : 1.f;
+    float ov[RPW][CPL], gv[RPW][CPL];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+        if (row0 + r >= a.rows) break;
+        const size_t off = static_cast<size_t>(row0 + r) * D + lane * CPL;
+        Lanes<Tin, CPL>::load(o + off, ov[r]);
+        Lanes<Tin, CPL>::load(g + off, gv[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+        if (row0 + r >= a.rows) break;
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) ss += ov[r][i] * ov[r][i];
+        const float inv = rsqrtf(warp_sum(ss) / D + a.eps);
+        float out[CPL];
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) out[i] = sigmoid(gv[r][i]) * (ov[r][i] * inv * w[i]);
+        Lanes<Tin, CPL>::store(y + static_cast<size_t>(row0 + r) * D + lane * CPL, out);
+    }
+}
+
+template <typename Tin>
+cudaError_t launch_prep_t(int d, const PrepArgs &a, cudaStream_t s) {
+    const long long tasks = static_cast<long long>((a.T_total + kRun - 1) / kRun) * 3 * a.H +
+                            static_cast<long long>(a.N) * 3 * a.H;
+    const long long blocks = (tasks + kWarps - 1) / kWarps;
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>(blocks));
+    if (d == 128) prep_kernel<Tin, 128><<<grid, kWarps * 32, 0, s>>>(a);
+    else if (d == 64) prep_kernel<Tin, 64><<<grid, kWarps * 32, 0, s>>>(a);
+    else if (d == 32) prep_kernel<Tin, 32><<<grid, kWarps * 32, 0, s>>>(a);
+    else return cudaErrorInvalidValue;
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
+
+template <typename Tin>
+cudaError_t launch_post_t(int d, const PostArgs &a, cudaStream_t s) {
+    const long long blocks = (a.rows + kWarps * 4 - 1) / (kWarps * 4);
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>(blocks));
+    if (d == 128) output_gate_kernel<Tin, 128><<<grid, kWarps * 32, 0, s>>>(a);
+    else if (d == 64) output_gate_kernel<Tin, 64><<<grid, kWarps * 32, 0, s>>>(a);
+    else if (d == 32) output_gate_kernel<Tin, 32><<<grid, kWarps * 32, 0, s>>>(a);
+    else return cudaErrorInvalidValue;
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_prep(kda_dtype dt, int d, const PrepArgs &a, cudaStream_t s) {
+    if (dt == KDA_BF16) return launch_prep_t<__nv_bfloat16>(d, a, s);
+    return launch_prep_t<float>(d, a, s);
+}
+
+cudaError_t launch_output_gate(kda_dtype dt, int d, const PostArgs &a, cudaStream_t s) {
+    if (dt == KDA_BF16) return launch_post_t<__nv_bfloat16>(d, a, s);
+    return launch_post_t<float>(d, a, s);
+}
+
+}  // namespace kda

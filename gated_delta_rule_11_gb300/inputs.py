@@ -185,3 +185,28 @@ def make_decode_drafts(w: Workload, step: int, device="cpu", seed: int | None = 
     accepted = torch.randint(min_accepted, K + 1, (N,), generator=g, device=device,
                              dtype=torch.int32)
     return dict(q=q, k=k, v=v, g_raw=g_raw, beta=beta, accepted=accepted)
+
+
+def make_prep_inputs(T: int, H: int, d: int, dtype: str = "bf16", device="cpu", seed: int = 7,
+                     N_state: int = 0):
+    """Pre/post pass inputs: x_qkv [1, T, 3, H, d] ~ N(0, 1) (projection
+    outputs), conv taps [3, H, d, 4] ~ N(0, 0.5) fp32, beta logits [1, T, H]
+    ~ N(0, 1), and (N_state > 0) conv states [N_state, 3, 3, H, d] ~ N(0, 1)."""
+    g = _gen(device, seed * 1_000_003 + 17)
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    x = _draw((1, T, 3, H, d), g, device).to(dt)
+    w = _draw((3, H, d, 4), g, device, 0.5)
+    bl = _draw((1, T, H), g, device).to(dt)
+    st = _draw((N_state, 3, 3, H, d), g, device).to(dt) if N_state else None
+    return dict(x_qkv=x, conv_w=w, beta_logit=bl, conv_state=st)
+
+
+def make_post_inputs(rows: int, d: int, dtype: str = "bf16", device="cpu", seed: int = 8):
+    """Output-gate inputs: o [rows, d] ~ N(0, 0.3) (operator outputs), gate
+    logits ~ N(0, 1), norm weight [d] ~ U(0.5, 1.5) fp32."""
+    g = _gen(device, seed * 1_000_003 + 29)
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    o = _draw((rows, d), g, device, 0.3).to(dt)
+    gate = _draw((rows, d), g, device).to(dt)
+    w = torch.rand((d,), generator=g, device=device, dtype=torch.float32) + 0.5
+    return dict(o=o, gate=gate, norm_w=w)

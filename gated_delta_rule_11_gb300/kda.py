@@ -26,7 +26,8 @@ _lock = threading.Lock()
 
 EXPORTED = ("kda_chunk_fwd", "kda_decode_step", "kda_status_str", "kda_last_cuda_error",
             "kda_version", "kda_launch_count", "kda_check_device_status", "kda_chunk_fwd_kernel",
-            "kda_decode_steps", "kda_chunk_fwd_checkpointed", "kda_checkpoint_rows")
+            "kda_decode_steps", "kda_chunk_fwd_checkpointed", "kda_checkpoint_rows",
+            "kda_qkv_prep", "kda_output_gate")
 
 
 class KdaError(RuntimeError):
@@ -76,6 +77,11 @@ def load_library(build_if_missing: bool = False):
                                                    ctypes.POINTER(KdaParams), vp]
         lib.kda_checkpoint_rows.restype = ctypes.c_longlong
         lib.kda_checkpoint_rows.argtypes = [i, i, vp, i, i]
+        lib.kda_qkv_prep.restype = i
+        lib.kda_qkv_prep.argtypes = [i, i, i, i, i, vp, vp, vp, vp, i, vp, vp, vp, vp, vp, vp,
+                                     ctypes.c_float, vp]
+        lib.kda_output_gate.restype = i
+        lib.kda_output_gate.argtypes = [i, ctypes.c_longlong, i, vp, vp, vp, ctypes.c_float, vp, vp]
         lib.kda_decode_steps.restype = i
         lib.kda_decode_steps.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, vp,
                                          ctypes.POINTER(KdaParams), vp]
@@ -348,3 +354,74 @@ def kda_decode_steps(q, k, v, g_raw, beta, state, accepted=None, *, out=None,
     if st != 0:
         _raise(lib, "kda_decode_steps", st)
     return out
+
+
+def kda_qkv_prep(x_qkv, conv_w, beta_logit=None, cu_seqlens=None, conv_state_in=None, *,
+                 conv_state_out=None, output_conv_state: bool = False, l2_eps: float = 0.0,
+                 out=None, stream=None):
+    """q, k = L2Norm(Swish(ShortConv(x_q|k))), v = Swish(ShortConv(x_v)),
+    beta = Sigmoid(beta_logit).
+
+    x_qkv [B, T, 3, H, d]; conv_w [3, H, d, 4] float32; beta_logit [B, T, H] or
+    None; cu_seqlens int32 [N+1] on the device (then B == 1) or None;
+    conv_state_in [N, 3, 3, H, d] or None.  Returns (q, k, v [B, T, H, d],
+    beta [B, T, H] or None, conv_state_out [N, 3, 3, H, d] or None).
+    """
+    lib = load_library()
+    dev = x_qkv.device
+    if dev.type != "cuda":
+        raise ValueError("kda_qkv_prep runs on CUDA tensors only")
+    dt = x_qkv.dtype
+    B, T, three, H, d = x_qkv.shape
+    if three != 3:
+        raise ValueError("x_qkv must be [B, T, 3, H, d]")
+    _check(x_qkv, "x_qkv", (B, T, 3, H, d), dt, dev)
+    _check(conv_w, "conv_w", (3, H, d, 4), torch.float32, dev)
+    if cu_seqlens is not None:
+        if cu_seqlens.dtype != torch.int32 or cu_seqlens.device != dev or cu_seqlens.dim() != 1:
+            raise ValueError("cu_seqlens must be a 1-D int32 tensor on the inputs' device")
+        if B != 1:
+            raise ValueError("packed sequences (cu_seqlens) require B == 1")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    if beta_logit is not None:
+        _check(beta_logit, "beta_logit", (B, T, H), dt, dev)
+    if conv_state_in is not None:
+        _check(conv_state_in, "conv_state_in", (N, 3, 3, H, d), dt, dev)
+    if conv_state_out is None and output_conv_state:
+        conv_state_out = torch.empty((N, 3, 3, H, d), dtype=dt, device=dev)
+    elif conv_state_out is not None:
+        _check(conv_state_out, "conv_state_out", (N, 3, 3, H, d), dt, dev)
+    if out is None:
+        q, k, v = (torch.empty((B, T, H, d), dtype=dt, device=dev) for _ in range(3))
+        beta = None if beta_logit is None else torch.empty((B, T, H), dtype=dt, device=dev)
+    else:
+        q, k, v, beta = out
+    st = lib.kda_qkv_prep(_dtype_code(x_qkv), B, T, H, d, _ptr(x_qkv), _ptr(conv_w),
+                          _ptr(beta_logit), _ptr(cu_seqlens), N, _ptr(conv_state_in),
+                          _ptr(conv_state_out), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                          float(l2_eps), _stream_handle(dev, stream))
+    if st != 0:
+        _raise(lib, "kda_qkv_prep", st)
+    return q, k, v, beta, conv_state_out
+
+
+def kda_output_gate(o, gate, norm_w=None, *, eps: float = 0.0, out=None, stream=None):
+    """y = Sigmoid(gate) * RMSNorm(o) over the last axis (one head's dv
+    channels); o, gate [..., dv]; norm_w [dv] float32 or None."""
+    lib = load_library()
+    dev = o.device
+    if dev.type != "cuda":
+        raise ValueError("kda_output_gate runs on CUDA tensors only")
+    d = o.shape[-1]
+    _check(gate, "gate", tuple(o.shape), o.dtype, dev)
+    _check(o, "o", tuple(o.shape), o.dtype, dev)
+    if norm_w is not None:
+        _check(norm_w, "norm_w", (d,), torch.float32, dev)
+    y = torch.empty_like(o) if out is None else out
+    st = lib.kda_output_gate(_dtype_code(o), o.numel() // d, d, _ptr(o), _ptr(gate), _ptr(norm_w),
+                             float(eps), _ptr(y), _stream_handle(dev, stream))
+    if st != 0:
+        _raise(lib, "kda_output_gate", st)
+    return y

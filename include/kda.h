@@ -220,6 +220,48 @@ kda_status kda_decode_steps(kda_dtype dt, int N, int K, int H, int dk, int dv,
                             float *state, void *out,
                             const kda_params *p, kda_stream_t stream);
 
+/*
+ * kda_qkv_prep -- the projection chain's tail before the operator
+ * ("Kimi K3：从三条信息流到完整系统", §从投影到 Chunkwise 的完整接口, eq. (2)):
+ *     q, k = L2Norm(Swish(ShortConv(x_q | x_k))),  v = Swish(ShortConv(x_v)),
+ *     beta = Sigmoid(beta_logit)
+ * ShortConv is the causal depthwise convolution of kernel size 4 along each
+ * sequence's tokens, y_t = sum_i w[i] x_{t-3+i} per channel, no bias;
+ * L2Norm divides each head's d channels by sqrt(sum x^2 + l2_eps).
+ *
+ * Inputs (dtype dt unless stated):
+ *   x_qkv  [B, T, 3, H, d]  the q | k | v projections of each token.
+ *   conv_w [3, H, d, 4] fp32: taps per channel, tap 3 multiplies x_t.
+ *   beta_logit [B, T, H] or NULL (then beta must be NULL too).
+ *   cu_seqlens / N: as kda_chunk_fwd (sequences are convolved separately).
+ *   conv_state_in [N, 3, 3, H, d] or NULL (zeros): per sequence, the x_qkv
+ *          rows of the three tokens before its first token, oldest first.
+ * Outputs:
+ *   q, k, v [B, T, H, d]; beta [B, T, H] (dtype dt).
+ *   conv_state_out [N, 3, 3, H, d] or NULL: the last three x_qkv rows of
+ *          each sequence (with conv_state_in rows where it is shorter than
+ *          three), to continue it in a later call (decode: one token per
+ *          sequence).  Must not alias conv_state_in.
+ * l2_eps <= 0 selects 1e-6.
+ */
+kda_status kda_qkv_prep(kda_dtype dt, int B, int T, int H, int d,
+                        const void *x_qkv, const float *conv_w, const void *beta_logit,
+                        const int32_t *cu_seqlens, int N,
+                        const void *conv_state_in, void *conv_state_out,
+                        void *q, void *k, void *v, void *beta,
+                        float l2_eps, kda_stream_t stream);
+
+/*
+ * kda_output_gate -- the output epilogue before W_o ("Kimi K3：从三条信息流到
+ * 完整系统", §下界 log-decay 是一个 kernel 设计, eq. (6)):
+ *     y = Sigmoid(gate) * RMSNorm(o),  RMSNorm(o) = o / sqrt(mean(o^2) + eps) * norm_w
+ * over each row of d channels (one row = one token of one head).
+ *   o, gate, y [rows, d] (dtype dt); norm_w [d] fp32 or NULL (ones).
+ *   eps <= 0 selects 1e-5 (the model's rms_norm_eps).
+ */
+kda_status kda_output_gate(kda_dtype dt, long long rows, int d, const void *o, const void *gate,
+                           const float *norm_w, float eps, void *y, kda_stream_t stream);
+
 /* Static string for a status code (never NULL). */
 const char *kda_status_str(kda_status s);
 
