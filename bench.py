@@ -16,6 +16,10 @@ prep / post: the passes around the operator on the same 237,568 tokens x 96
              Sigmoid of beta) and kda_output_gate (Sigmoid(gate) * RMSNorm(o)),
              each timed after the main region: HBM GB/s of the bytes each
              pass must move.
+gate_variants: the 8192-token x 96-head prefill under Kimi Linear's
+             unbounded negative-softplus gate (fp32 prefill, position-pair
+             in-tile path) and under one bounded gate per head (gated
+             delta), timed after the main region.
 spec_replay: speculative replay (kda_decode_steps) of 256 sequences x 8
              verified tokens with 1..8 accepted, timed after the main region:
              algorithmic GB/s (state once in and out + the applied tokens'
@@ -414,6 +418,7 @@ def run_ours(args, rank, world, local):
 
     spec = run_spec(kda, dev, rank, world, args.steps, args.warmup, hbm_peak, peak_src)
     prep, post = run_prepost(kda, dev, world, min(args.steps, 10), args.warmup, hbm_peak, peak_src)
+    gates = run_gate_variants(kda, dev, world, min(args.steps, 5), args.warmup, hbm_peak, peak_src)
 
     e2e = None
     if not args.no_e2e:   # every rank: the timing is reduced over ranks
@@ -450,10 +455,10 @@ def run_ours(args, rank, world, local):
                    "peak_source": peak_src + " (sustained bf16)"},
         "decode": {"metric": "decode step state GB/s", "value": d_gbs, "unit": "GB/s",
                    "ms": d_mean, "state_bytes_per_step": dec_bytes,
-                   "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": d_gbs,
+                   "roofline": {"kernel": "decode1_kernel", "bound": "hbm", "achieved": d_gbs,
                                 "peak": hbm_peak, "unit": "GB/s", "frac": d_gbs / hbm_peak,
                                 "traffic": d_traffic, "peak_source": peak_src}},
-        "spec_replay": spec, "prep": prep, "post": post,
+        "spec_replay": spec, "prep": prep, "post": post, "gate_variants": gates,
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches,
         "clocks": clocks, "wall_s_timed": t_wall,
     }
@@ -496,6 +501,39 @@ def run_spec(kda, dev, rank, world, steps, warmup, hbm_peak, peak_src):
             "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": gbs,
                          "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
                          "algorithmic_bytes_per_launch": alg, "peak_source": peak_src}}
+
+
+def run_gate_variants(kda, dev, world, steps, warmup, hbm_peak, peak_src):
+    """Prefill of the layer-shaped workload under two non-default gates."""
+    w = kin.WORKLOADS["layer_bf16_H96_T8192"]
+    inp = kin.make_prefill_inputs(w, device=dev)
+    args = [inp[n] for n in ("q", "k", "v")]
+    out = torch.empty_like(inp["v"])
+    fin = torch.empty((1, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    g_head = inp["g_raw"][..., 0].contiguous()          # one gate per (token, head)
+    res = {"workload": w.name}
+    for name, g, mode, per_head in (("neg_softplus", inp["g_raw"], "neg_softplus", False),
+                                    ("gated_delta_per_head", g_head, "bounded", True)):
+        fn = lambda i: kda.kda_chunk_fwd(*args, g, inp["beta"], None, None, out=out, final_state=fin,
+                                         gate_mode=mode, gate_per_head=per_head)
+        for i in range(warmup):
+            fn(i)
+        barrier(world)
+        torch.cuda.synchronize()
+        evs = time_region(fn, steps, stream)
+        torch.cuda.synchronize()
+        ms = reduce_max(statistics.fmean(a.elapsed_time(b) for a, b in evs), world)
+        th = w.T * w.H
+        gate_bytes = (w.dk if not per_head else 1) * 2
+        nbytes = th * (BYTES_PER_TOKEN_HEAD - D * 2 + gate_bytes) + w.H * w.dk * w.dv * 4
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"ms": ms, "tokens_per_s": w.T / (ms * 1e-3),
+                     "kernel": "prefill_simt_kernel", "achieved_gbs": gbs, "frac": gbs / hbm_peak,
+                     "peak_source": peak_src}
+    del inp, out, fin
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_prepost(kda, dev, world, steps, warmup, hbm_peak, peak_src):
