@@ -19,7 +19,7 @@ prep / post: the passes around the operator on the same 237,568 tokens x 96
 gate_variants: the 8192-token x 96-head prefill under Kimi Linear's
              unbounded negative-softplus gate (fp32 prefill, position-pair
              in-tile path) and under one bounded gate per head (gated
-             delta), timed after the main region.
+             delta, tensor-core prefill), timed after the main region.
 spec_replay: speculative replay (kda_decode_steps) of 256 sequences x 8
              verified tokens with 1..8 accepted, timed after the main region:
              algorithmic GB/s (state once in and out + the applied tokens'
@@ -529,7 +529,8 @@ def run_gate_variants(kda, dev, world, steps, warmup, hbm_peak, peak_src):
         nbytes = th * (BYTES_PER_TOKEN_HEAD - D * 2 + gate_bytes) + w.H * w.dk * w.dv * 4
         gbs = nbytes / (ms * 1e-3) / 1e9
         res[name] = {"ms": ms, "tokens_per_s": w.T / (ms * 1e-3),
-                     "kernel": "prefill_simt_kernel", "achieved_gbs": gbs, "frac": gbs / hbm_peak,
+                     "kernel": "prefill_tc_kernel" if mode == "bounded" else "prefill_simt_kernel",
+                     "achieved_gbs": gbs, "frac": gbs / hbm_peak,
                      "peak_source": peak_src}
     del inp, out, fin
     torch.cuda.empty_cache()

@@ -124,7 +124,8 @@ constexpr int SMEM_BYTES = SMEM_USED + 1024;      // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 static_assert(STAGE_BYTES % 1024 == 0 && ST_WQ % 1024 == 0 && ST_KD % 1024 == 0,
               "128B-swizzled operands need 1024-byte alignment");
-constexpr uint32_t TX_BYTES = 4 * C * D * 2;
+constexpr uint32_t TX_BYTES = 4 * C * D * 2;        // q, k, g_raw, v tiles
+constexpr uint32_t TX_BYTES_NOZ = 3 * C * D * 2;    // q, k, v (gate per head or none)
 
 __device__ __forceinline__ float bf16_at(const uint8_t *p) {
     return __bfloat162float(__ushort_as_bfloat16(*reinterpret_cast<const uint16_t *>(p)));
@@ -189,6 +190,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     seq_span(a, n, bos, eos);
     const int ntiles = (eos - bos + C - 1) / C;
     const size_t state_off = static_cast<size_t>(chain) * D * D;
+    // gate source: a TMA tile of per-channel inputs (eq. (5)), one input per
+    // (token, head) shared by the channels, or none (alpha = 1)
+    const bool gate_none = a.gate_mode == KDA_GATE_NONE;
+    const bool z_tile = !gate_none && !a.gate_scalar;
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -204,7 +209,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (tid == 0) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
-        prefetch_tmap(&tm_z);
+        if (a.gate_mode == KDA_GATE_BOUNDED && !a.gate_scalar) prefetch_tmap(&tm_z);
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_o);
     }
@@ -238,6 +243,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                        ? __bfloat162float(gbeta[static_cast<size_t>(tok) * a.H + h]) : 0.f;
         };
         float bt_next = load_beta(pg);
+        // per-head gate: lane l < 16 of every producer warp holds row l's input, a tile ahead
+        const __nv_bfloat16 *gzs = static_cast<const __nv_bfloat16 *>(a.g);
+        auto load_zs = [&](int tt) {
+            const int tok = bos + tt * C + lane;
+            return (!z_tile && !gate_none && lane < C && tt < ntiles && tok < eos)
+                       ? __bfloat162float(gzs[static_cast<size_t>(tok) * a.H + h]) : 0.f;
+        };
+        float zs_next = load_zs(pg);
         for (int t = pg; t < ntiles; t += NPROD) {
             const int s = t % NS;
             uint8_t *st = base + s * STAGE_BYTES;
@@ -245,6 +258,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const int nv = min(C, eos - t0);
             const float bt = bt_next;
             bt_next = load_beta(t + NPROD);
+            const float zs = zs_next;
+            zs_next = load_zs(t + NPROD);
             if (!mbar_wait(&bars[B_RAW + s], (t / NS) & 1, kWaitLimitNs)) note_timeout(abort_flag);
 
             // Gate and decays in log2 units, branch-free: the retention
@@ -255,20 +270,39 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const int cp = lane & 15, hh = lane >> 4;
             const int c0 = 32 * pw + 2 * cp;
             float kx[2][8], qx[2][8], pre[2][8], suf[2][8];
+            if (z_tile) {                               // eq. (5) per key channel
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int row = 8 * hh + r;
-                const float m = row < nv ? 1.f : 0.f;
-                const uint32_t zz = *reinterpret_cast<const uint32_t *>(st + ST_Z + row * 256 + c0 * 2);
-                const uint32_t kk = *reinterpret_cast<const uint32_t *>(st + ST_K + row * 256 + c0 * 2);
-                const uint32_t qq = *reinterpret_cast<const uint32_t *>(st + ST_Q + row * 256 + c0 * 2);
+                for (int r = 0; r < 8; ++r) {
+                    const int row = 8 * hh + r;
+                    const float m = row < nv ? 1.f : 0.f;
+                    const uint32_t zz = *reinterpret_cast<const uint32_t *>(st + ST_Z + row * 256 + c0 * 2);
+                    const uint32_t kk = *reinterpret_cast<const uint32_t *>(st + ST_K + row * 256 + c0 * 2);
+                    const uint32_t qq = *reinterpret_cast<const uint32_t *>(st + ST_Q + row * 256 + c0 * 2);
 #pragma unroll
-                for (int ch = 0; ch < 2; ++ch) {
-                    const float z = bf16_half(zz, ch);
-                    kx[ch][r] = m * bf16_half(kk, ch);
-                    qx[ch][r] = m * bf16_half(qq, ch);
+                    for (int ch = 0; ch < 2; ++ch) {
+                        const float z = bf16_half(zz, ch);
+                        kx[ch][r] = m * bf16_half(kk, ch);
+                        qx[ch][r] = m * bf16_half(qq, ch);
+                        const float sig = rcp_approx(1.f + ex2_approx(-kLog2e * escale * z));
+                        suf[ch][r] = ex2_approx(m * (kLog2e * a.g_min) * sig);   // a_r (1 past the end)
+                    }
+                }
+            } else {                                    // one gate per (token, head), or none
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int row = 8 * hh + r;
+                    const float m = row < nv ? 1.f : 0.f;
+                    const uint32_t kk = *reinterpret_cast<const uint32_t *>(st + ST_K + row * 256 + c0 * 2);
+                    const uint32_t qq = *reinterpret_cast<const uint32_t *>(st + ST_Q + row * 256 + c0 * 2);
+                    const float z = __shfl_sync(0xffffffffu, zs, row);
                     const float sig = rcp_approx(1.f + ex2_approx(-kLog2e * escale * z));
-                    suf[ch][r] = ex2_approx(m * (kLog2e * a.g_min) * sig);   // a_r (1 past the end)
+                    const float a_r = ex2_approx(gate_none ? 0.f : m * (kLog2e * a.g_min) * sig);
+#pragma unroll
+                    for (int ch = 0; ch < 2; ++ch) {
+                        kx[ch][r] = m * bf16_half(kk, ch);
+                        qx[ch][r] = m * bf16_half(qq, ch);
+                        suf[ch][r] = a_r;
+                    }
                 }
             }
             float gC[2], inv_gC[2];
@@ -461,10 +495,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const int ss = tt % NS;
             uint8_t *stg = base + ss * STAGE_BYTES;
             const int tok = bos + tt * C;
-            mbar_arrive_expect_tx(&bars[B_RAW + ss], TX_BYTES);
+            mbar_arrive_expect_tx(&bars[B_RAW + ss], z_tile ? TX_BYTES : TX_BYTES_NOZ);
             tma_load_3d(stg + ST_Q, &tm_q, &bars[B_RAW + ss], 0, h, tok);
             tma_load_3d(stg + ST_K, &tm_k, &bars[B_RAW + ss], 0, h, tok);
-            tma_load_3d(stg + ST_Z, &tm_z, &bars[B_RAW + ss], 0, h, tok);
+            if (z_tile) tma_load_3d(stg + ST_Z, &tm_z, &bars[B_RAW + ss], 0, h, tok);
             tma_load_3d(stg + ST_V, &tm_v, &bars[B_RAW + ss], 0, h, tok);
         };
         constexpr int TMA_TID = 160, OST_TID = 192;  // lane 0 of chain warps 5 and 6
@@ -678,9 +712,11 @@ bool prefill_tc_supported(kda_dtype dt, int dk, int dv) { return dt == KDA_BF16 
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     CUtensorMap tq, tk, tz, tv, to;
+    // the gate tile map exists only for per-channel gates (a per-head g_raw is [T, H])
+    const bool z_tile = a.gate_mode == KDA_GATE_BOUNDED && !a.gate_scalar;
     if (!make_map(&tq, a.q, a.H, a.T_total, D, false) || !make_map(&tk, a.k, a.H, a.T_total, D, false) ||
-        !make_map(&tz, a.g, a.H, a.T_total, D, false) || !make_map(&tv, a.v, a.H, a.T_total, D, false) ||
-        !make_map(&to, a.out, a.H, a.T_total, D, false))
+        !make_map(&tz, z_tile ? a.g : a.q, a.H, a.T_total, D, false) ||
+        !make_map(&tv, a.v, a.H, a.T_total, D, false) || !make_map(&to, a.out, a.H, a.T_total, D, false))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SMEM_BYTES);

@@ -83,8 +83,9 @@ typedef enum {
  *   gate_per_head : 0 = one gate per key channel (KDA, g_raw [.., H, dk]);
  *           1 = one gate per token and head shared by every key channel
  *           (gated delta, g_raw [.., H]).
- * Only the default gate (bounded, per channel) runs on the tensor-core
- * prefill; the others run on the fp32 prefill kernel.  The unbounded modes
+ * The bounded gates (eq. (5) per channel or per head) and KDA_GATE_NONE run
+ * on the tensor-core prefill (bf16, dk = dv = 128); the unbounded modes run
+ * on the fp32 prefill kernel.  The unbounded modes
  * (LOG_DECAY, NEG_SOFTPLUS) evaluate the in-tile products with one
  * exponential per position pair instead of dividing by the cumulative
  * decay, which a 16-token tile can drive past fp32's range.
