@@ -93,7 +93,8 @@ kda_status kda_check_device_status(void) {
         g_last_cuda_error = static_cast<int>(e);
         return KDA_ERR_LAUNCH;
     }
-    return kda::take_tc_timeouts() ? KDA_ERR_TIMEOUT : KDA_OK;
+    const unsigned int waits = kda::take_tc_timeouts() + kda::take_prep_timeouts();
+    return waits ? KDA_ERR_TIMEOUT : KDA_OK;
 }
 
 long long kda_checkpoint_rows(int B, int T, const int32_t *cu_seqlens_host, int N,

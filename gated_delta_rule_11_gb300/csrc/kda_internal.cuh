@@ -160,5 +160,6 @@ bool prefill_tc_supported(kda_dtype dt, int dk, int dv);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 // Number of bounded device waits that gave up since the last call (syncs the device).
 unsigned int take_tc_timeouts();
+unsigned int take_prep_timeouts();
 
 }  // namespace kda

@@ -677,22 +677,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
 // [T_total, H, 128] bf16 viewed as a 3-D tensor (d, head, token).
 bool make_map(CUtensorMap *m, const void *ptr, int H, int T_total, int box_d, bool swizzle128) {
-    auto enc = get_encode();
+    auto enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
                                 static_cast<cuuint64_t>(T_total)};
@@ -709,6 +696,19 @@ bool make_map(CUtensorMap *m, const void *ptr, int H, int T_total, int box_d, bo
 }  // namespace
 
 bool prefill_tc_supported(kda_dtype dt, int dk, int dv) { return dt == KDA_BF16 && dk == D && dv == D; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     CUtensorMap tq, tk, tz, tv, to;

@@ -16,21 +16,28 @@
 // sqrt(mean x^2 + eps) and multiplies by a per-channel weight shared by the
 // heads.
 //
-// Both passes are HBM-bound streams.  prep: one warp owns a run of up to
-// 64 consecutive tokens of one (tensor, head); each lane holds d / 32
-// channels and keeps the three previous inputs of its channels in registers,
-// so every input element is read once (plus a three-token halo per run);
-// the L2 norm is a warp reduction.  Loads are issued four tokens at a time;
-// the register budget keeps three CTAs (24 warps) per SM, which measured
-// faster than deeper per-warp prefetch at two CTAs per SM.
+// Both passes are HBM-bound streams.  prep: one CTA owns a run of 64
+// consecutive tokens of one (tensor, head): one TMA copy brings the run and
+// the three tokens before it ([67, d], rows before the first token read as
+// zero) into shared memory, so many runs are in flight per SM without
+// holding registers; each of four warps then walks 16 tokens with the
+// three previous inputs of its lane's d/32 channels in registers, the L2
+// norm as a warp reduction.  Inputs before a sequence's first token come
+// from the caller's conv state (or zero), never from the previous sequence.
 // post: one warp per (token, head) row, four rows per warp in flight.
 #include "kda_internal.cuh"
+#include "kda_sm100.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int kRun = 64;          // tokens per prep warp task
-constexpr int kWarps = 8;         // warps per CTA
+constexpr int kRun = 64;          // tokens per prep CTA
+constexpr int kHalo = 3;          // inputs before the run that ShortConv reads
+constexpr int kPrepWarps = 4;     // prep warps, kRun / kPrepWarps tokens each
+constexpr int kWarps = 8;         // warps per output-gate CTA
+constexpr uint64_t kPrepWaitNs = 1000000000ull;   // bounded wait for the TMA tile (1 s)
+
+__device__ unsigned int g_prep_timeouts = 0;
 
 template <typename T, int CPL> struct Lanes;
 template <> struct Lanes<__nv_bfloat16, 4> {
@@ -57,6 +64,26 @@ template <> struct Lanes<float, 4> {
         *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
     }
 };
+// A lane's CPL channels of one token row in shared memory.
+template <typename T, int CPL>
+__device__ __forceinline__ void load_row(const T *p, float (&x)[CPL]) {
+    if constexpr (CPL == 4 && sizeof(T) == 2) {
+        const uint2 w = *reinterpret_cast<const uint2 *>(p);
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&w.x);
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&w.y);
+        x[0] = __low2float(a); x[1] = __high2float(a); x[2] = __low2float(b); x[3] = __high2float(b);
+    } else if constexpr (CPL == 4) {
+        const float4 w = *reinterpret_cast<const float4 *>(p);
+        x[0] = w.x; x[1] = w.y; x[2] = w.z; x[3] = w.w;
+    } else {
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+            if constexpr (sizeof(T) == 2) x[i] = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[i]);
+            else x[i] = reinterpret_cast<const float *>(p)[i];
+        }
+    }
+}
+
 template <typename T, int CPL> struct LanesScalar {
     static __device__ __forceinline__ void load(const T *p, float (&x)[CPL]) {
 #pragma unroll
@@ -72,8 +99,13 @@ template <> struct Lanes<__nv_bfloat16, 1> : LanesScalar<__nv_bfloat16, 1> {};
 template <> struct Lanes<float, 2> : LanesScalar<float, 2> {};
 template <> struct Lanes<float, 1> : LanesScalar<float, 1> {};
 
-__device__ __forceinline__ float swish(float x) { return x / (1.0f + expf(-x)); }
-__device__ __forceinline__ float sigmoid(float x) { return 1.0f / (1.0f + expf(-x)); }
+// Sigmoid from the hardware exponential and the fast division (relative
+// error ~1e-7, far inside the outputs' rounding): the prep pass issues about
+// 150 instructions per token and head, so the ~20 of an accurate expf and
+// an IEEE division per element would bound it.  For x < -88, e^{-x}
+// overflows and Sigmoid returns 0, its limit.
+__device__ __forceinline__ float sigmoid(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float swish(float x) { return x * sigmoid(x); }
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -104,13 +136,26 @@ __device__ __forceinline__ void span_of(const PrepArgs &a, int n, int &bos, int 
 }
 
 template <typename Tin, int D>
-__global__ void __launch_bounds__(kWarps * 32) prep_kernel(PrepArgs a) {
+constexpr int prep_smem_bytes() {
+    return (((kRun + kHalo) * D * static_cast<int>(sizeof(Tin)) + 15) & ~15) + 16;   // tile + mbarrier
+}
+
+template <typename Tin, int D>
+__global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(const __grid_constant__ CUtensorMap tm_x,
+                                                               PrepArgs a) {
+    using namespace sm100;
     constexpr int CPL = D / 32;                 // channels per lane
-    const int lane = threadIdx.x & 31;
-    const long long task = static_cast<long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    constexpr int TILE_BYTES = (kRun + kHalo) * D * static_cast<int>(sizeof(Tin));
+    constexpr int PER_WARP = kRun / kPrepWarps;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const Tin *tile = reinterpret_cast<const Tin *>(smem_raw);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem_raw + ((TILE_BYTES + 15) & ~15));
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H;
     const long long row_tasks = static_cast<long long>(3) * H;     // (tensor, head) pairs
     const long long run_tasks = static_cast<long long>((a.T_total + kRun - 1) / kRun) * row_tasks;
+    const long long task = blockIdx.x;
     const Tin *x = static_cast<const Tin *>(a.x);
     const Tin *sin = static_cast<const Tin *>(a.state_in);
     Tin *sout = static_cast<Tin *>(a.state_out);
@@ -119,7 +164,7 @@ __global__ void __launch_bounds__(kWarps * 32) prep_kernel(PrepArgs a) {
     if (task >= run_tasks) {
         // conv state of an empty sequence passes through (or becomes zero)
         const long long et = task - run_tasks;
-        if (et >= static_cast<long long>(a.N) * row_tasks || !sout) return;
+        if (warp != 0 || et >= static_cast<long long>(a.N) * row_tasks || !sout) return;
         const int n = static_cast<int>(et / row_tasks);
         const int mh = static_cast<int>(et % row_tasks);
         int bos, eos;
@@ -142,9 +187,18 @@ __global__ void __launch_bounds__(kWarps * 32) prep_kernel(PrepArgs a) {
     const int mh = static_cast<int>(task % row_tasks);     // m * H + h
     const int m = mh / H, h = mh % H;
     const int t_begin = run * kRun, t_end = min(t_begin + kRun, a.T_total);
-    const size_t col = static_cast<size_t>(mh) * D + lane * CPL;   // this lane's channels in a token of x
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {      // rows t_begin - 3 .. t_begin + 63 of this (tensor, head); out of range -> 0
+        mbar_arrive_expect_tx(bar, TILE_BYTES);
+        tma_load_3d(smem_raw, &tm_x, bar, 0, mh, t_begin - kHalo);
+    }
 
     // conv taps of this lane's channels: w[ch][0..3], tap 3 = current token
+    const size_t col = static_cast<size_t>(mh) * D + lane * CPL;   // this lane's channels in a token of x
     float wt[CPL][4];
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
@@ -153,13 +207,22 @@ __global__ void __launch_bounds__(kWarps * 32) prep_kernel(PrepArgs a) {
     }
     Tin *dst = static_cast<Tin *>(m == 0 ? a.q : (m == 1 ? a.k : a.v));
     const size_t tok_o = static_cast<size_t>(H) * D;
-
-    int n = seq_of(a, t_begin), bos, eos;
-    span_of(a, n, bos, eos);
-    while (eos <= t_begin && n + 1 < a.N) {      // empty sequences at t_begin
-        ++n;
+    const int w_begin = t_begin + warp * PER_WARP, w_end = min(w_begin + PER_WARP, t_end);
+    int n = 0, bos = 0, eos = 0;
+    if (w_begin < w_end) {
+        n = seq_of(a, w_begin);
         span_of(a, n, bos, eos);
+        while (eos <= w_begin && n + 1 < a.N) {      // empty sequences at w_begin
+            ++n;
+            span_of(a, n, bos, eos);
+        }
     }
+    if (!mbar_wait(bar, 0, kPrepWaitNs)) {
+        if (lane == 0) atomicAdd(&g_prep_timeouts, 1u);
+        return;
+    }
+    auto row_ptr = [&](int t) { return tile + static_cast<size_t>(t - t_begin + kHalo) * D + lane * CPL; };
+
     // window: x of the three tokens before the current one (win[0] oldest)
     float win[3][CPL];
     auto fill_window = [&](int t) {              // window for token t of sequence n (bos <= t)
@@ -167,7 +230,7 @@ __global__ void __launch_bounds__(kWarps * 32) prep_kernel(PrepArgs a) {
         for (int j = 0; j < 3; ++j) {
             const int p = t - 3 + j;
             if (p >= bos) {
-                Lanes<Tin, CPL>::load(x + static_cast<size_t>(p) * tok_x + col, win[j]);
+                load_row<Tin, CPL>(row_ptr(p), win[j]);
             } else if (sin) {
                 const int tap = p - bos + 3;     // 0..2: state token bos - 3 + tap
                 Lanes<Tin, CPL>::load(sin + (static_cast<size_t>(n) * 3 + tap) * tok_x + col, win[j]);
@@ -177,54 +240,46 @@ __global__ void __launch_bounds__(kWarps * 32) prep_kernel(PrepArgs a) {
             }
         }
     };
-    fill_window(t_begin);
-
-    for (int t0 = t_begin; t0 < t_end; t0 += 4) {
-        float xs[4][CPL];                         // this batch's inputs
+    if (w_begin < w_end) fill_window(w_begin);
+#pragma unroll 2
+    for (int t = w_begin; t < w_end; ++t) {
+        if (t >= eos) {                           // next sequence: restart the window
+            do {
+                ++n;
+                span_of(a, n, bos, eos);
+            } while (eos <= t && n + 1 < a.N);
+            fill_window(t);
+        }
+        float xt[CPL];
+        load_row<Tin, CPL>(row_ptr(t), xt);
+        float y[CPL];
+        float ss = 0.f;
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (t0 + u < t_end) Lanes<Tin, CPL>::load(x + static_cast<size_t>(t0 + u) * tok_x + col, xs[u]);
+        for (int i = 0; i < CPL; ++i) {
+            const float c = wt[i][0] * win[0][i] + wt[i][1] * win[1][i] + wt[i][2] * win[2][i] + wt[i][3] * xt[i];
+            y[i] = swish(c);
+            ss += y[i] * y[i];
+            win[0][i] = win[1][i];
+            win[1][i] = win[2][i];
+            win[2][i] = xt[i];
+        }
+        if (m < 2) {                              // q, k: L2Norm over the head's d channels
+            const float r = rsqrtf(warp_sum(ss) + a.l2_eps);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int t = t0 + u;
-            if (t >= t_end) break;
-            if (t >= eos) {                       // next sequence: restart the window
-                do {
-                    ++n;
-                    span_of(a, n, bos, eos);
-                } while (eos <= t && n + 1 < a.N);
-                fill_window(t);
-            }
-            float y[CPL];
-            float ss = 0.f;
+            for (int i = 0; i < CPL; ++i) y[i] *= r;
+        }
+        Lanes<Tin, CPL>::store(dst + static_cast<size_t>(t) * tok_o + static_cast<size_t>(h) * D + lane * CPL, y);
+        if (t == eos - 1 && sout) {               // last token: save the window as conv state
 #pragma unroll
-            for (int i = 0; i < CPL; ++i) {
-                const float c = wt[i][0] * win[0][i] + wt[i][1] * win[1][i] + wt[i][2] * win[2][i] +
-                                wt[i][3] * xs[u][i];
-                y[i] = swish(c);
-                ss += y[i] * y[i];
-                win[0][i] = win[1][i];
-                win[1][i] = win[2][i];
-                win[2][i] = xs[u][i];
-            }
-            if (m < 2) {                          // q, k: L2Norm over the head's d channels
-                const float r = rsqrtf(warp_sum(ss) + a.l2_eps);
-#pragma unroll
-                for (int i = 0; i < CPL; ++i) y[i] *= r;
-            }
-            Lanes<Tin, CPL>::store(dst + static_cast<size_t>(t) * tok_o + static_cast<size_t>(h) * D + lane * CPL, y);
-            if (t == eos - 1 && sout) {           // last token: save the window as conv state
-#pragma unroll
-                for (int j = 0; j < 3; ++j)
-                    Lanes<Tin, CPL>::store(sout + (static_cast<size_t>(n) * 3 + j) * tok_x + col, win[j]);
-            }
+            for (int j = 0; j < 3; ++j)
+                Lanes<Tin, CPL>::store(sout + (static_cast<size_t>(n) * 3 + j) * tok_x + col, win[j]);
         }
     }
-    // beta = Sigmoid(logit) for this run's tokens and head h (the q-tensor warps)
+    // beta = Sigmoid(logit) for this run's tokens and head h (the q-tensor CTAs)
     if (m == 0 && a.beta_logit) {
         const Tin *bl = static_cast<const Tin *>(a.beta_logit);
         Tin *bo = static_cast<Tin *>(a.beta);
-        for (int t = t_begin + lane; t < t_end; t += 32)
+        for (int t = t_begin + tid; t < t_end; t += kPrepWarps * 32)
             st_out(bo + static_cast<size_t>(t) * H + h, sigmoid(ld_in(bl + static_cast<size_t>(t) * H + h)));
     }
 }
@@ -263,21 +318,40 @@ __global__ void __launch_bounds__(kWarps * 32) output_gate_kernel(PostArgs a) {
     }
 }
 
-template <typename Tin>
-cudaError_t launch_prep_t(int d, const PrepArgs &a, cudaStream_t s) {
+// x_qkv [T, 3, H, d] viewed as the 3-D tensor (channel, tensor-head, token).
+template <typename Tin, int D>
+cudaError_t launch_prep_d(const PrepArgs &a, cudaStream_t s) {
     const long long tasks = static_cast<long long>((a.T_total + kRun - 1) / kRun) * 3 * a.H +
                             static_cast<long long>(a.N) * 3 * a.H;
-    const long long blocks = (tasks + kWarps - 1) / kWarps;
-    if (blocks <= 0) return cudaSuccess;
-    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    const dim3 grid(static_cast<unsigned>(blocks));
-    if (d == 128) prep_kernel<Tin, 128><<<grid, kWarps * 32, 0, s>>>(a);
-    else if (d == 64) prep_kernel<Tin, 64><<<grid, kWarps * 32, 0, s>>>(a);
-    else if (d == 32) prep_kernel<Tin, 32><<<grid, kWarps * 32, 0, s>>>(a);
-    else return cudaErrorInvalidValue;
+    if (tasks <= 0) return cudaSuccess;
+    if (tasks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    auto enc = tensor_map_encoder();
+    if (!enc) return cudaErrorInvalidValue;
+    CUtensorMap tm;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(3) * a.H,
+                                static_cast<cuuint64_t>(a.T_total > 0 ? a.T_total : 1)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * sizeof(Tin),
+                                   static_cast<cuuint64_t>(3) * a.H * D * sizeof(Tin)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 1, static_cast<cuuint32_t>(kRun + kHalo)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(&tm, sizeof(Tin) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                           3, const_cast<void *>(a.x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    constexpr int smem = prep_smem_bytes<Tin, D>();
+    prep_kernel<Tin, D><<<static_cast<unsigned>(tasks), kPrepWarps * 32, smem, s>>>(tm, a);
     const cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;
+}
+
+template <typename Tin>
+cudaError_t launch_prep_t(int d, const PrepArgs &a, cudaStream_t s) {
+    if (d == 128) return launch_prep_d<Tin, 128>(a, s);
+    if (d == 64) return launch_prep_d<Tin, 64>(a, s);
+    if (d == 32) return launch_prep_d<Tin, 32>(a, s);
+    return cudaErrorInvalidValue;
 }
 
 template <typename Tin>
@@ -305,6 +379,13 @@ cudaError_t launch_prep(kda_dtype dt, int d, const PrepArgs &a, cudaStream_t s) 
 cudaError_t launch_output_gate(kda_dtype dt, int d, const PostArgs &a, cudaStream_t s) {
     if (dt == KDA_BF16) return launch_post_t<__nv_bfloat16>(d, a, s);
     return launch_post_t<float>(d, a, s);
+}
+
+unsigned int take_prep_timeouts() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_prep_timeouts, sizeof(v)) != cudaSuccess) return 0;
+    cudaMemcpyToSymbol(g_prep_timeouts, &zero, sizeof(zero));
+    return v;
 }
 
 }  // namespace kda

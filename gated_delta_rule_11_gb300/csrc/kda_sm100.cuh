@@ -5,9 +5,14 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 namespace kda {
+
+// The driver's cuTensorMapEncodeTiled, looked up once (nullptr if missing).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
 namespace sm100 {
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
