@@ -67,7 +67,9 @@ __device__ __forceinline__ f32x2 fmul2(f32x2 a, f32x2 b) {
 // Single-token step with whole rows per warp (a warp instruction touches one
 // 512-byte row of S): rows row0 + m * RPP per thread, the reductions over c
 // combined across warps through shared memory.  K = 1, every token applied.
-template <typename Tin, int DK, int DV>
+// GenericGate = false compiles the default gate (eq. (5), per channel) with
+// its input load issued beside the others; true takes any kda_gate_mode.
+template <typename Tin, int DK, int DV, bool GenericGate>
 __global__ void __launch_bounds__(kDecodeThreads, 2) decode1_kernel(DecodeArgs a) {
     constexpr int V4 = DV / 4;                       // float4 per state row
     constexpr int RPP = kDecodeThreads / V4;         // rows per pass
@@ -102,8 +104,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode1_kernel(DecodeArgs a
 
     if (tid < DK) {
         const float kc = ld_in(k + tid), qc = ld_in(q + tid);
-        const float zc = a.gate_mode == KDA_GATE_NONE ? 0.f : ld_in(z + (a.gate_scalar ? 0 : tid));
-        const float alpha = expf(gate_log_decay(a.gate_mode, zc, escale, a.g_min));
+        float alpha;
+        if constexpr (GenericGate) {
+            const float zc = a.gate_mode == KDA_GATE_NONE ? 0.f : ld_in(z + (a.gate_scalar ? 0 : tid));
+            alpha = expf(gate_log_decay(a.gate_mode, zc, escale, a.g_min));
+        } else {
+            alpha = expf(log_decay(ld_in(z + tid), escale, a.g_min));
+        }
         s_alpha[tid] = alpha;
         s_k[tid] = kc;
         s_ak[tid] = alpha * kc;
@@ -159,13 +166,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode1_kernel(DecodeArgs a
     }
 }
 
-template <int DK, int DV>
+template <int DK, int DVS>
 struct DecodeSmem {
     ulonglong2 akq[kTokBlock][DK];     // pairs (alpha k, alpha k), (alpha q, alpha q) per token and channel
     ulonglong2 alk[kTokBlock][DK];     // pairs (alpha, alpha), (k, k)
-    float red[2][kDecodeThreads / (DV / 4)][DV];      // [a|b][row group][column]
-    float4 u[DV / 4];
-    float v[kTokBlock][DV];
+    float red[2][kDecodeThreads / (DVS / 4)][DVS];    // [a|b][row group][slab column]
+    float4 u[DVS / 4];
+    float v[kTokBlock][DVS];
     float kq[kTokBlock][DK / 32];      // per-warp partial sums of k.q
     float beta[kTokBlock];
 };
@@ -179,33 +186,39 @@ __device__ __forceinline__ float4 ld_state(const float4 *p) {
     return v;
 }
 
-// Multi-token replay, same row layout as the single step: RPP row groups x
-// V4 float4 columns; thread (rg, c4) holds rows rg + m RPP of column c4.  Per
-// token: in-thread partial sums over its rows; barrier; dv threads add the
-// RPP partials of one column each, form u_j and o_j; barrier; every thread
-// applies u to its rows.  The second barrier also orders the partials' reads
-// before the next token's writes, so one buffer serves all tokens.
-template <typename Tin, int DK, int DV>
-__global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(DecodeArgs a) {
-    constexpr int V4 = DV / 4;                       // float4 per state row
+// Multi-token replay.  The value columns of the state never interact, so a
+// (sequence, head) is split into CS slabs of DV / CS columns, one CTA each:
+// half the registers per thread, so four CTAs share an SM and one CTA's
+// state streaming overlaps another's token arithmetic.  Inside a slab, the
+// single step's row layout: RPP row groups x V4 float4 columns; thread
+// (rg, c4) holds rows rg + m RPP of slab column c4.  Per token: in-thread
+// partial sums over its rows; barrier; the slab's threads add the RPP
+// partials of one column each, form u_j and o_j; barrier; every thread
+// applies u to its rows.  The second barrier also orders the partials'
+// reads before the next token's writes, so one buffer serves all tokens.
+template <typename Tin, int DK, int DV, int CS>
+__global__ void __launch_bounds__(kDecodeThreads, 2 * CS) decode_kernel(DecodeArgs a) {
+    constexpr int DVS = DV / CS;                     // slab columns
+    constexpr int V4 = DVS / 4;                      // float4 per slab row
     constexpr int RPP = kDecodeThreads / V4;         // row groups
     constexpr int RPL = DK / RPP;                    // rows per thread
     static_assert(RPL >= 1 && DK % RPP == 0, "tiling");
 
-    __shared__ __align__(16) DecodeSmem<DK, DV> sm;
+    __shared__ __align__(16) DecodeSmem<DK, DVS> sm;
 
     const int tid = threadIdx.x, lane = tid & 31;
     const int c4 = tid % V4, rg = tid / V4;
-    const int nh = blockIdx.x;                       // n * H + h
+    const int nh = blockIdx.x / CS;                  // n * H + h
+    const int slab = blockIdx.x % CS;
     const int n = nh / a.H, h = nh % a.H;
 
     const int acc_raw = a.accepted ? __ldg(a.accepted + n) : a.K;
     // Issue the state loads first: they dominate the kernel's time.
-    float4 *S = reinterpret_cast<float4 *>(a.state) + static_cast<size_t>(nh) * (DK * V4);
+    float4 *S = reinterpret_cast<float4 *>(a.state) + static_cast<size_t>(nh) * (DK * (DV / 4)) + slab * V4;
     f32x2 st[RPL][2];
 #pragma unroll
     for (int m = 0; m < RPL; ++m) {
-        const float4 x = ld_state(S + (rg + m * RPP) * V4 + c4);
+        const float4 x = ld_state(S + (rg + m * RPP) * (DV / 4) + c4);
         st[m][0] = pack2(x.x, x.y);
         st[m][1] = pack2(x.z, x.w);
     }
@@ -236,9 +249,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(DecodeArgs a)
             for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
             if (lane == 0) sm.kq[i][c / 32] = kq;
         }
-        for (int idx = tid; idx < nb * DV; idx += kDecodeThreads)
-            sm.v[idx / DV][idx % DV] =
-                ld_in(gv + (static_cast<size_t>(n) * a.K + i0 + idx / DV) * tok_v + static_cast<size_t>(h) * DV + idx % DV);
+        for (int idx = tid; idx < nb * DVS; idx += kDecodeThreads)
+            sm.v[idx / DVS][idx % DVS] =
+                ld_in(gv + (static_cast<size_t>(n) * a.K + i0 + idx / DVS) * tok_v + static_cast<size_t>(h) * DV +
+                      slab * DVS + idx % DVS);
         if (tid < nb) sm.beta[tid] = ld_in(gb + (static_cast<size_t>(n) * a.K + i0 + tid) * a.H + h);
     };
     // The first block is prepared for every drafted token, before the accepted
@@ -272,7 +286,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(DecodeArgs a)
                 *reinterpret_cast<float4 *>(&sm.red[1][rg][4 * c4]) = make_float4(b0.x, b0.y, b1.x, b1.y);
             }
             __syncthreads();
-            if (tid < DV) {
+            if (tid < DVS) {
                 float av = 0.f, bv = 0.f;
 #pragma unroll
                 for (int r = 0; r < RPP; ++r) {
@@ -284,7 +298,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(DecodeArgs a)
                 for (int w = 0; w < DK / 32; ++w) kq += sm.kq[i][w];
                 const float u = sm.beta[i] * (sm.v[i][tid] - av);
                 reinterpret_cast<float *>(sm.u)[tid] = u;
-                st_out(go + (static_cast<size_t>(n) * a.K + i0 + i) * tok_v + static_cast<size_t>(h) * DV + tid,
+                st_out(go + (static_cast<size_t>(n) * a.K + i0 + i) * tok_v + static_cast<size_t>(h) * DV +
+                           slab * DVS + tid,
                        a.scale * fmaf(kq, u, bv));
             }
             __syncthreads();
@@ -302,7 +317,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(DecodeArgs a)
 #pragma unroll
     for (int m = 0; m < RPL; ++m) {
         const float2 x = unpack2(st[m][0]), y = unpack2(st[m][1]);
-        st_stream(S + (rg + m * RPP) * V4 + c4, make_float4(x.x, x.y, y.x, y.y));
+        st_stream(S + (rg + m * RPP) * (DV / 4) + c4, make_float4(x.x, x.y, y.x, y.y));
     }
 }
 
@@ -311,10 +326,15 @@ cudaError_t launch_t(int dk, int dv, const DecodeArgs &a, cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>(a.N) * static_cast<unsigned>(a.H));
     const dim3 block(kDecodeThreads);
     const bool single = a.K == 1 && !a.accepted;
+    const bool default_gate = a.gate_mode == KDA_GATE_BOUNDED && !a.gate_scalar;
 #define KDA_DEC_CASE(DK_, DV_)                                            \
     if (dk == DK_ && dv == DV_) {                                         \
-        if (single) decode1_kernel<Tin, DK_, DV_><<<grid, block, 0, s>>>(a); \
-        else decode_kernel<Tin, DK_, DV_><<<grid, block, 0, s>>>(a);      \
+        if (single && default_gate)                                       \
+            decode1_kernel<Tin, DK_, DV_, false><<<grid, block, 0, s>>>(a); \
+        else if (single) decode1_kernel<Tin, DK_, DV_, true><<<grid, block, 0, s>>>(a); \
+        else if constexpr (DV_ >= 64)                                     \
+            decode_kernel<Tin, DK_, DV_, 2><<<dim3(grid.x * 2), block, 0, s>>>(a); \
+        else decode_kernel<Tin, DK_, DV_, 1><<<grid, block, 0, s>>>(a);   \
         const cudaError_t e = cudaGetLastError();                         \
         if (e == cudaSuccess) count_launches(1);                          \
         return e;                                                         \

@@ -91,24 +91,35 @@ def test_accepted_zero_and_out_of_range_counts_are_clamped():
     assert torch.equal(S[0], S0[0]) and torch.equal(S[1], S0[1])
 
 
-def test_replay_equals_single_steps_bit_for_bit():
-    """Replaying a accepted tokens in one launch is the same arithmetic as a
-    single-token steps: identical bits for state and outputs."""
+def test_replay_split_is_bit_exact_and_matches_single_steps():
+    """Replaying a prefix in two launches (the state carried in fp32 between
+    them) is bit-identical to one launch; single-token steps agree to fp32
+    rounding (their reduction order over the key channels differs)."""
     w = _w("bf16", 4, 128, 128, N=5, K=6, seed=22)
     S1 = inputs.make_decode_state(w, device="cuda")
-    S2 = S1.clone()
+    S2, S3 = S1.clone(), S1.clone()
     tok = inputs.make_decode_drafts(w, 0, device="cuda", min_accepted=0)
     acc = tok["accepted"].cpu().tolist()
-    out = kda.kda_decode_steps(tok["q"], tok["k"], tok["v"], tok["g_raw"], tok["beta"], S1,
-                               tok["accepted"])
-    for n in range(5):
-        for i in range(acc[n]):
-            t = {x: tok[x][n:n + 1, i] for x in ("q", "k", "v", "g_raw", "beta")}
-            o = kda.kda_decode_step(t["q"], t["k"], t["v"], t["g_raw"], t["beta"], S2[n:n + 1])
-            torch.cuda.synchronize()
-            assert torch.equal(o[0], out[n, i]), (n, i)
+    names = ("q", "k", "v", "g_raw", "beta")
+    out = kda.kda_decode_steps(*(tok[x] for x in names), S1, tok["accepted"])
+    first = torch.tensor([min(a, 2) for a in acc], dtype=torch.int32, device="cuda")
+    rest = torch.tensor([max(a - 2, 0) for a in acc], dtype=torch.int32, device="cuda")
+    o_a = kda.kda_decode_steps(*(tok[x][:, :2].contiguous() for x in names), S2, first)
+    o_b = kda.kda_decode_steps(*(tok[x][:, 2:].contiguous() for x in names), S2, rest)
     torch.cuda.synchronize()
     assert torch.equal(S1, S2)
+    for n in range(5):
+        a = acc[n]
+        assert torch.equal(out[n, :min(a, 2)], o_a[n, :min(a, 2)])
+        assert torch.equal(out[n, 2:a], o_b[n, :max(a - 2, 0)])
+    for n in range(5):
+        for i in range(acc[n]):
+            t = {x: tok[x][n:n + 1, i] for x in names}
+            o = kda.kda_decode_step(t["q"], t["k"], t["v"], t["g_raw"], t["beta"], S3[n:n + 1])
+            torch.cuda.synchronize()
+            torch.testing.assert_close(o[0].float(), out[n, i].float(), rtol=0, atol=2 ** -7)
+    torch.cuda.synchronize()
+    torch.testing.assert_close(S3, S1, rtol=1e-5, atol=1e-6)
 
 
 def test_all_accepted_by_default():
