@@ -29,40 +29,21 @@
 // and (alpha, k), v, beta and k.q are computed for a block of up to 8 tokens at
 // once into shared memory, with their loads in flight beside the state's.
 #include "kda_internal.cuh"
+#include "kda_sm100.cuh"
 
 namespace kda {
 namespace {
+using sm100::f32x2;
+using sm100::pack2;
+using sm100::unpack2;
+using sm100::ffma2;
+using sm100::fmul2;
 
 constexpr int kDecodeThreads = 256;
 constexpr int kTokBlock = 8;                         // tokens prepared per barrier
 
 __device__ __forceinline__ float4 ld_stream(const float4 *p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(float4 *p, float4 v) { __stcs(p, v); }
-
-// Packed two-lane fp32 arithmetic on 64-bit register pairs (fma.rn.f32x2 /
-// mul.rn.f32x2): each lane rounds exactly like fmaf / __fmul_rn, at half the
-// instruction count.  A pair (lo, hi) is kept as one 64-bit value.
-typedef unsigned long long f32x2;
-__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
-    f32x2 r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ float2 unpack2(f32x2 r) {
-    float2 v;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
-    return v;
-}
-__device__ __forceinline__ f32x2 ffma2(f32x2 a, f32x2 b, f32x2 c) {
-    f32x2 d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ f32x2 fmul2(f32x2 a, f32x2 b) {
-    f32x2 d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
 
 // Single-token step with whole rows per warp (a warp instruction touches one
 // 512-byte row of S): rows row0 + m * RPP per thread, the reductions over c

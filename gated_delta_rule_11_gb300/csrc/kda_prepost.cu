@@ -107,6 +107,18 @@ template <> struct Lanes<float, 1> : LanesScalar<float, 1> {};
 __device__ __forceinline__ float sigmoid(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 __device__ __forceinline__ float swish(float x) { return x * sigmoid(x); }
 
+// Swish of a channel pair: the exponentials and reciprocals stay per lane
+// (MUFU), the rest is packed.  Same arithmetic as swish() per element.
+__device__ __forceinline__ sm100::f32x2 swish2(sm100::f32x2 c) {
+    using namespace sm100;
+    const float2 m = unpack2(fmul2(c, pack2(-1.4426950408889634f, -1.4426950408889634f)));
+    float ex, ey;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ex) : "f"(m.x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ey) : "f"(m.y));
+    const float2 den = unpack2(fadd2(pack2(ex, ey), pack2(1.f, 1.f)));
+    return fmul2(c, pack2(__fdividef(1.0f, den.x), __fdividef(1.0f, den.y)));
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -254,14 +266,41 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(const __grid_cons
         load_row<Tin, CPL>(row_ptr(t), xt);
         float y[CPL];
         float ss = 0.f;
+        if constexpr (CPL == 4) {                 // channel pairs in f32x2
+            using namespace sm100;
+            f32x2 ss2 = 0ull;
 #pragma unroll
-        for (int i = 0; i < CPL; ++i) {
-            const float c = wt[i][0] * win[0][i] + wt[i][1] * win[1][i] + wt[i][2] * win[2][i] + wt[i][3] * xt[i];
-            y[i] = swish(c);
-            ss += y[i] * y[i];
-            win[0][i] = win[1][i];
-            win[1][i] = win[2][i];
-            win[2][i] = xt[i];
+            for (int p2 = 0; p2 < 2; ++p2) {
+                const int i0 = 2 * p2, i1 = i0 + 1;
+                const f32x2 x2 = pack2(xt[i0], xt[i1]);
+                f32x2 c = fmul2(pack2(wt[i0][0], wt[i1][0]), pack2(win[0][i0], win[0][i1]));
+                c = ffma2(pack2(wt[i0][1], wt[i1][1]), pack2(win[1][i0], win[1][i1]), c);
+                c = ffma2(pack2(wt[i0][2], wt[i1][2]), pack2(win[2][i0], win[2][i1]), c);
+                c = ffma2(pack2(wt[i0][3], wt[i1][3]), x2, c);
+                const f32x2 yy = swish2(c);
+                ss2 = ffma2(yy, yy, ss2);
+                const float2 yv = unpack2(yy);
+                y[i0] = yv.x;
+                y[i1] = yv.y;
+            }
+            const float2 s2 = unpack2(ss2);
+            ss = s2.x + s2.y;
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) {
+                win[0][i] = win[1][i];
+                win[1][i] = win[2][i];
+                win[2][i] = xt[i];
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) {
+                const float c = wt[i][0] * win[0][i] + wt[i][1] * win[1][i] + wt[i][2] * win[2][i] + wt[i][3] * xt[i];
+                y[i] = swish(c);
+                ss += y[i] * y[i];
+                win[0][i] = win[1][i];
+                win[1][i] = win[2][i];
+                win[2][i] = xt[i];
+            }
         }
         if (m < 2) {                              // q, k: L2Norm over the head's d channels
             const float r = rsqrtf(warp_sum(ss) + a.l2_eps);
