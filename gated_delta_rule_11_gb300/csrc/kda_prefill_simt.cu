@@ -137,35 +137,41 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
         if (tid < C) sm.beta[tid] = tid < nv ? ld_in(gb + static_cast<size_t>(t0 + tid) * a.H + h) : 0.f;
         __syncthreads();
 
-        // L (strictly lower) and A (lower, diagonal kept): warp-cooperative dots.
-        for (int r = warp; r < C; r += NW) {
-            for (int i = 0; i < C; ++i) {
-                float l = 0.f, aa = 0.f;
-                if (i <= r) {
-                    if (pairs) {
-                        for (int c = lane; c < DK; c += 32) {
-                            const float ki = pp.k[i][c] * expf(pp.b[r][c] - pp.b[i][c]);
-                            l += pp.k[r][c] * ki;
-                            aa += pp.q[r][c] * ki;
-                        }
-                    } else {
-                        for (int c = lane; c < DK; c += 32) {
-                            const float ki = sm.kinv[i][c];
-                            l += sm.kg[r][c] * ki;
-                            aa += sm.qg[r][c] * ki;
-                        }
-                    }
+        // L (strictly lower) and A (lower, diagonal kept): one entry (r, i)
+        // per thread and pass, the whole dot product over c in-thread (no
+        // shuffle chains on the critical path); each lane starts at its own
+        // channel, so the 32 lanes' row reads hit 32 different banks.
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        l += __shfl_xor_sync(0xffffffffu, l, o);
-                        aa += __shfl_xor_sync(0xffffffffu, aa, o);
+        for (int pass = 0; pass < (C * C) / NT; ++pass) {
+            const int e = tid + pass * NT;
+            const int r = e / C, i = e % C;
+            float l0 = 0.f, l1 = 0.f, a0 = 0.f, a1 = 0.f;
+            if (i <= r) {
+                if (pairs) {
+#pragma unroll 4
+                    for (int j = 0; j < DK; j += 2) {
+                        const int c0 = (lane + j) & (DK - 1), c1 = (lane + j + 1) & (DK - 1);
+                        const float k0 = pp.k[i][c0] * expf(pp.b[r][c0] - pp.b[i][c0]);
+                        const float k1 = pp.k[i][c1] * expf(pp.b[r][c1] - pp.b[i][c1]);
+                        l0 = fmaf(pp.k[r][c0], k0, l0);
+                        a0 = fmaf(pp.q[r][c0], k0, a0);
+                        l1 = fmaf(pp.k[r][c1], k1, l1);
+                        a1 = fmaf(pp.q[r][c1], k1, a1);
                     }
-                }
-                if (lane == 0) {
-                    sm.L[r][i] = i < r ? l : 0.f;
-                    sm.A[r][i] = i <= r ? aa : 0.f;
+                } else {
+#pragma unroll 4
+                    for (int j = 0; j < DK; j += 2) {
+                        const int c0 = (lane + j) & (DK - 1), c1 = (lane + j + 1) & (DK - 1);
+                        const float k0 = sm.kinv[i][c0], k1 = sm.kinv[i][c1];
+                        l0 = fmaf(sm.kg[r][c0], k0, l0);
+                        a0 = fmaf(sm.qg[r][c0], k0, a0);
+                        l1 = fmaf(sm.kg[r][c1], k1, l1);
+                        a1 = fmaf(sm.qg[r][c1], k1, a1);
+                    }
                 }
             }
+            sm.L[r][i] = i < r ? l0 + l1 : 0.f;
+            sm.A[r][i] = i <= r ? a0 + a1 : 0.f;
         }
         __syncthreads();
 
