@@ -17,9 +17,10 @@ prep / post: the passes around the operator on the same 237,568 tokens x 96
              each timed after the main region: HBM GB/s of the bytes each
              pass must move.
 gate_variants: the 8192-token x 96-head prefill under Kimi Linear's
-             unbounded negative-softplus gate (fp32 prefill, position-pair
-             in-tile path) and under one bounded gate per head (gated
-             delta, tensor-core prefill), timed after the main region.
+             unbounded negative-softplus gate and under one bounded gate per
+             head (gated delta), both on the tensor-core prefill (tiles past
+             fp32's range for e^{-b} take its position-pair path), timed
+             after the main region.
 spec_replay: speculative replay (kda_decode_steps) of 256 sequences x 8
              verified tokens with 1..8 accepted, timed after the main region:
              algorithmic GB/s (state once in and out + the applied tokens'
@@ -529,7 +530,7 @@ def run_gate_variants(kda, dev, world, steps, warmup, hbm_peak, peak_src):
         nbytes = th * (BYTES_PER_TOKEN_HEAD - D * 2 + gate_bytes) + w.H * w.dk * w.dv * 4
         gbs = nbytes / (ms * 1e-3) / 1e9
         res[name] = {"ms": ms, "tokens_per_s": w.T / (ms * 1e-3),
-                     "kernel": "prefill_tc_kernel" if mode == "bounded" else "prefill_simt_kernel",
+                     "kernel": kda.chunk_fwd_kernel(torch.bfloat16, w.dk, w.dv),
                      "achieved_gbs": gbs, "frac": gbs / hbm_peak,
                      "peak_source": peak_src}
     del inp, out, fin

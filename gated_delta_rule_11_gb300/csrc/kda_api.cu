@@ -160,10 +160,9 @@ kda_status kda_chunk_fwd_checkpointed(kda_dtype dt, int B, int T, int H, int dk,
     a.T_total = static_cast<int>(total);
     a.T_seq = T;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // bounded gates (eq. (5), per channel or per head) and no gate run on the
-    // tensor cores; the unbounded maps need the fp32 kernel's pair path
-    const bool bounded = a.gate_mode == KDA_GATE_BOUNDED || a.gate_mode == KDA_GATE_NONE;
-    if (bounded && kda::prefill_tc_supported(dt, dk, dv) && a.T_total > 0)
+    // every gate map runs on the tensor cores (an unbounded map's tiles past
+    // fp32's range take the kernel's position-pair path for L and A)
+    if (kda::prefill_tc_supported(dt, dk, dv) && a.T_total > 0)
         return from_cuda(kda::launch_prefill_tc(a, s));
     return from_cuda(kda::launch_prefill_simt(dt, dk, dv, a, s));
 }

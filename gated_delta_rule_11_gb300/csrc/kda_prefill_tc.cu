@@ -168,11 +168,28 @@ __device__ __forceinline__ void mma_1688_tf32(float (&d)[4], uint32_t a0, uint32
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// log2 of the retention under an unbounded gate map: the gate itself, or
+// -softplus(e^A z) = -(max(x, 0) + log(1 + e^-|x|)), in log2 units.
+__device__ __forceinline__ float unbounded_lg(int mode, float z, float escale) {
+    if (mode == KDA_GATE_LOG_DECAY) return kLog2e * z;
+    const float x = escale * z;
+    return -(fmaxf(x, 0.f) * kLog2e + lg2_approx(1.f + ex2_approx(-fabsf(x) * kLog2e)));
+}
+constexpr float kPairThreshold = 7.5e-37f;   // 2^-120: below it, e^{-b} nears fp32's limit
+
 __device__ __forceinline__ void note_timeout(volatile int *flag) {
     *flag = 1;
     atomicAdd(&g_tc_timeouts, 1u);
 }
 
+// Unbounded: the launch's gate map is unbounded (the per-tile pair path is
+// compiled in); the bounded instance carries none of that code.
+template <bool Unbounded>
 __global__ void __launch_bounds__(NTHREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_v,
@@ -194,6 +211,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // (token, head) shared by the channels, or none (alpha = 1)
     const bool gate_none = a.gate_mode == KDA_GATE_NONE;
     const bool z_tile = !gate_none && !a.gate_scalar;
+    // unbounded maps (the gate as the log-decay, Kimi Linear's -softplus):
+    // a tile whose cumulative decay leaves fp32's range for e^{-b} takes the
+    // position-pair path for L and A
+    constexpr bool unbounded = Unbounded;
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -209,7 +230,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (tid == 0) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
-        if (a.gate_mode == KDA_GATE_BOUNDED && !a.gate_scalar) prefetch_tmap(&tm_z);
+        if (a.gate_mode != KDA_GATE_NONE && !a.gate_scalar) prefetch_tmap(&tm_z);
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_o);
     }
@@ -270,7 +291,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const int cp = lane & 15, hh = lane >> 4;
             const int c0 = 32 * pw + 2 * cp;
             float kx[2][8], qx[2][8], pre[2][8], suf[2][8];
-            if (z_tile) {                               // eq. (5) per key channel
+            if (z_tile && !unbounded) {                 // eq. (5) per key channel
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
                     const int row = 8 * hh + r;
@@ -287,6 +308,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         suf[ch][r] = ex2_approx(m * (kLog2e * a.g_min) * sig);   // a_r (1 past the end)
                     }
                 }
+            } else if (z_tile) {                        // unbounded map per key channel
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int row = 8 * hh + r;
+                    const float m = row < nv ? 1.f : 0.f;
+                    const uint32_t zz = *reinterpret_cast<const uint32_t *>(st + ST_Z + row * 256 + c0 * 2);
+                    const uint32_t kk = *reinterpret_cast<const uint32_t *>(st + ST_K + row * 256 + c0 * 2);
+                    const uint32_t qq = *reinterpret_cast<const uint32_t *>(st + ST_Q + row * 256 + c0 * 2);
+#pragma unroll
+                    for (int ch = 0; ch < 2; ++ch) {
+                        kx[ch][r] = m * bf16_half(kk, ch);
+                        qx[ch][r] = m * bf16_half(qq, ch);
+                        suf[ch][r] = ex2_approx(m * unbounded_lg(a.gate_mode, bf16_half(zz, ch), escale));
+                    }
+                }
             } else {                                    // one gate per (token, head), or none
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
@@ -295,8 +331,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     const uint32_t kk = *reinterpret_cast<const uint32_t *>(st + ST_K + row * 256 + c0 * 2);
                     const uint32_t qq = *reinterpret_cast<const uint32_t *>(st + ST_Q + row * 256 + c0 * 2);
                     const float z = __shfl_sync(0xffffffffu, zs, row);
-                    const float sig = rcp_approx(1.f + ex2_approx(-kLog2e * escale * z));
-                    const float a_r = ex2_approx(gate_none ? 0.f : m * (kLog2e * a.g_min) * sig);
+                    float lg;
+                    if (unbounded) {
+                        lg = unbounded_lg(a.gate_mode, z, escale);
+                    } else {
+                        const float sig = rcp_approx(1.f + ex2_approx(-kLog2e * escale * z));
+                        lg = gate_none ? 0.f : (kLog2e * a.g_min) * sig;
+                    }
+                    const float a_r = ex2_approx(m * lg);
 #pragma unroll
                     for (int ch = 0; ch < 2; ++ch) {
                         kx[ch][r] = m * bf16_half(kk, ch);
@@ -344,8 +386,54 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     make_float2(to_tf32(kd0 * inv_gC[0]), to_tf32(kd1 * inv_gC[1]));
             }
             if (named_bar_or(pbar, 128, *abort_flag != 0)) break;   // uniform across the warpgroup
+            const bool pair_tile =
+                unbounded && named_bar_or(pbar, 128, gC[0] < kPairThreshold || gC[1] < kPairThreshold);
 
-            {
+            if constexpr (Unbounded) if (pair_tile) {
+                // L_ri = sum_c k_rc k_ic 2^{B_rc - B_ic}, A_ri = sum_c q_rc k_ic 2^{B_rc - B_ic}
+                // (i <= r, so every exponent is <= 0), B the in-tile cumulative
+                // log2-decay, stored in the K e^-b operand's place.
+                float bv[2][8], cum[2] = {0.f, 0.f};
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int row = 8 * hh + r;
+                    const float m = row < nv ? 1.f : 0.f;
+                    const uint32_t zz = z_tile ? *reinterpret_cast<const uint32_t *>(st + ST_Z + row * 256 + c0 * 2) : 0u;
+                    const float zr = __shfl_sync(0xffffffffu, zs, row);
+#pragma unroll
+                    for (int ch = 0; ch < 2; ++ch) {
+                        cum[ch] += m * unbounded_lg(a.gate_mode, z_tile ? bf16_half(zz, ch) : zr, escale);
+                        bv[ch][r] = cum[ch];
+                    }
+                }
+#pragma unroll
+                for (int ch = 0; ch < 2; ++ch) {
+                    const float other = __shfl_xor_sync(0xffffffffu, cum[ch], 16);
+                    const float lead = hh ? other : 0.f;
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) kim[(8 * hh + r) * PADF + c0 + ch] = bv[ch][r] + lead;
+                }
+                named_bar_sync(pbar, 128);
+#pragma unroll 1
+                for (int pass = 0; pass < 2; ++pass) {
+                    const int e = c + 128 * pass;
+                    const int r = e >> 4, i = e & 15;
+                    float l = 0.f, aa = 0.f;
+                    if (i <= r && r < nv) {
+                        const float *br = kim + r * PADF, *bi = kim + i * PADF;
+#pragma unroll 4
+                        for (int jj = 0; jj < D; ++jj) {
+                            const int ch = (lane + jj) & (D - 1);   // rotated start: distinct banks
+                            const float ki = bf16_at(st + ST_K + i * 256 + ch * 2) * ex2_approx(br[ch] - bi[ch]);
+                            l = fmaf(bf16_at(st + ST_K + r * 256 + ch * 2), ki, l);
+                            aa = fmaf(bf16_at(st + ST_Q + r * 256 + ch * 2), ki, aa);
+                        }
+                    }
+                    ls[r * LSS + i] = i < r ? l : 0.f;
+                    st_h(st + ST_AT + off_kmajor_none(r, i, C), i <= r ? aa : 0.f);
+                }
+            }
+            if (!pair_tile) {
                 // one 16x8 block per warp: pw 0/1 -> L columns 0-7/8-15, pw 2/3 -> A
                 const int g = lane >> 2, tq = lane & 3;
                 const float *lhs = pw < 2 ? kgm : qgm;
@@ -712,17 +800,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     CUtensorMap tq, tk, tz, tv, to;
-    // the gate tile map exists only for per-channel gates (a per-head g_raw is [T, H])
-    const bool z_tile = a.gate_mode == KDA_GATE_BOUNDED && !a.gate_scalar;
+    // the gate tile map exists only for per-channel gates (a per-head g_raw is
+    // [T, H]; with no gate it may be NULL) -- the same test as the kernel's
+    const bool z_tile = a.gate_mode != KDA_GATE_NONE && !a.gate_scalar;
     if (!make_map(&tq, a.q, a.H, a.T_total, D, false) || !make_map(&tk, a.k, a.H, a.T_total, D, false) ||
         !make_map(&tz, z_tile ? a.g : a.q, a.H, a.T_total, D, false) ||
         !make_map(&tv, a.v, a.H, a.T_total, D, false) || !make_map(&to, a.out, a.H, a.T_total, D, false))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SMEM_BYTES);
+    const bool unbounded = a.gate_mode == KDA_GATE_LOG_DECAY || a.gate_mode == KDA_GATE_NEG_SOFTPLUS;
+    auto kern = unbounded ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(a.N) * static_cast<unsigned>(a.H));
-    prefill_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, s>>>(tq, tk, tz, tv, to, a);
+    kern<<<grid, NTHREADS, SMEM_BYTES, s>>>(tq, tk, tz, tv, to, a);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;

@@ -83,12 +83,12 @@ typedef enum {
  *   gate_per_head : 0 = one gate per key channel (KDA, g_raw [.., H, dk]);
  *           1 = one gate per token and head shared by every key channel
  *           (gated delta, g_raw [.., H]).
- * The bounded gates (eq. (5) per channel or per head) and KDA_GATE_NONE run
- * on the tensor-core prefill (bf16, dk = dv = 128); the unbounded modes run
- * on the fp32 prefill kernel.  The unbounded modes
- * (LOG_DECAY, NEG_SOFTPLUS) evaluate the in-tile products with one
- * exponential per position pair instead of dividing by the cumulative
- * decay, which a 16-token tile can drive past fp32's range.
+ * Every gate runs on the tensor-core prefill for bf16 with dk = dv = 128
+ * and on the fp32 prefill otherwise.  Under the unbounded modes (LOG_DECAY,
+ * NEG_SOFTPLUS), a 16-token tile whose cumulative decay would take e^{-b}
+ * past fp32's range computes its in-tile products with one exponential per
+ * position pair instead of dividing by the cumulative decay (the fp32
+ * prefill always does so under these modes).
  */
 typedef struct {
     float g_min;
