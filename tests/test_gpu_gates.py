@@ -131,6 +131,41 @@ def test_replay_gate_variants(mode, per_head):
     assert_close(f"{mode} replay state", S, rf, tol)
 
 
+@pytest.mark.parametrize("mode", ["log_decay", "neg_softplus"])
+def test_unbounded_gate_mixes_factored_and_pair_tiles(mode):
+    """Moderate gates keep most 16-token tiles inside fp32's range for
+    e^{-b} (factored form); a few tokens with a huge decay push their tiles
+    past it (position-pair form).  Both kinds in one launch on the
+    tensor-core prefill, against the oracle."""
+    seqlens = (160, 77, 16)
+    w = inputs.Workload("test", "prefill", H=2, dk=128, dv=128, dtype="bf16", z_std=1.0,
+                        s0_std=0.1, seed=95, seqlens=seqlens)
+    inp = inputs.make_prefill_inputs(w, device="cuda")
+    T = sum(seqlens)
+    g = torch.Generator().manual_seed(96)
+    if mode == "log_decay":
+        z = -torch.rand((1, T, 2, 128), generator=g) * 2.0                 # |g| < 2 per token
+        big = -200.0
+    else:
+        z = torch.randn((1, T, 2, 128), generator=g) - 1.0                 # softplus ~ 0.3
+        big = 200.0
+    spikes = torch.tensor([5, 40, 170, 200])                               # a few tiles only
+    z[:, spikes] = big
+    inp["g_raw"] = z.to(torch.bfloat16).cuda()
+    out, fin = kda.kda_chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta"],
+                                 inp["init_state"], inp["cu_seqlens"], gate_mode=mode)
+    torch.cuda.synchronize()
+    assert kda.chunk_fwd_kernel(torch.bfloat16, 128, 128) == "prefill_tc_kernel"
+    ro, rf = oracle_heads(inp, [0, 1], gate_mode=mode)
+    tol = TOL[torch.bfloat16]
+    assert_close(f"{mode} mixed out", out, ro, tol)
+    assert_close(f"{mode} mixed final_state", fin, rf, tol)
+    # the spikes really make pair tiles and the rest factored ones
+    gl = oracle.kda_oracle_log_decay(inp["g_raw"].float().cpu().numpy()[0, :, 0], mode)
+    bc = [gl[t0:t0 + 16].sum(0).min() for t0 in range(0, T, 16)]
+    assert min(bc) < -85 and max(bc) > -40
+
+
 def test_default_gate_still_on_tensor_cores_and_variants_reject_bad_args():
     assert kda.chunk_fwd_kernel(torch.bfloat16, 128, 128) == "prefill_tc_kernel"
     w = inputs.Workload("test", "prefill", H=1, dk=128, dv=128, dtype="bf16", z_std=1.0,
