@@ -290,46 +290,47 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             // the two row halves (lanes l, l ^ 16) join their products by shuffle.
             const int cp = lane & 15, hh = lane >> 4;
             const int c0 = 32 * pw + 2 * cp;
-            float kx[2][8], qx[2][8], pre[2][8], suf[2][8];
+            // (channel c0, channel c0 + 1) pairs, packed for the f32x2 pipe
+            f32x2 kx[8], qx[8], pre[8], suf[8];
             if (z_tile && !unbounded) {                 // eq. (5) per key channel
+                const f32x2 zc = pack2(-kLog2e * escale, -kLog2e * escale);
+                const f32x2 lc = pack2(kLog2e * a.g_min, kLog2e * a.g_min);
+                const f32x2 one = pack2(1.f, 1.f);
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
                     const int row = 8 * hh + r;
-                    const float m = row < nv ? 1.f : 0.f;
+                    const bool in = row < nv;
                     const uint32_t zz = *reinterpret_cast<const uint32_t *>(st + ST_Z + row * 256 + c0 * 2);
-                    const uint32_t kk = *reinterpret_cast<const uint32_t *>(st + ST_K + row * 256 + c0 * 2);
-                    const uint32_t qq = *reinterpret_cast<const uint32_t *>(st + ST_Q + row * 256 + c0 * 2);
-#pragma unroll
-                    for (int ch = 0; ch < 2; ++ch) {
-                        const float z = bf16_half(zz, ch);
-                        kx[ch][r] = m * bf16_half(kk, ch);
-                        qx[ch][r] = m * bf16_half(qq, ch);
-                        const float sig = rcp_approx(1.f + ex2_approx(-kLog2e * escale * z));
-                        suf[ch][r] = ex2_approx(m * (kLog2e * a.g_min) * sig);   // a_r (1 past the end)
-                    }
+                    const uint32_t kk = in ? *reinterpret_cast<const uint32_t *>(st + ST_K + row * 256 + c0 * 2) : 0u;
+                    const uint32_t qq = in ? *reinterpret_cast<const uint32_t *>(st + ST_Q + row * 256 + c0 * 2) : 0u;
+                    kx[r] = pack2(bf16_half(kk, 0), bf16_half(kk, 1));
+                    qx[r] = pack2(bf16_half(qq, 0), bf16_half(qq, 1));
+                    const float2 e = unpack2(fmul2(zc, pack2(bf16_half(zz, 0), bf16_half(zz, 1))));
+                    const f32x2 den = fadd2(one, pack2(ex2_approx(e.x), ex2_approx(e.y)));
+                    const float2 lg = unpack2(fmul2(lc, pack2(rcp_approx(unpack2(den).x), rcp_approx(unpack2(den).y))));
+                    suf[r] = in ? pack2(ex2_approx(lg.x), ex2_approx(lg.y)) : one;   // a_r (1 past the end)
                 }
             } else if (z_tile) {                        // unbounded map per key channel
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
                     const int row = 8 * hh + r;
-                    const float m = row < nv ? 1.f : 0.f;
+                    const bool in = row < nv;
                     const uint32_t zz = *reinterpret_cast<const uint32_t *>(st + ST_Z + row * 256 + c0 * 2);
-                    const uint32_t kk = *reinterpret_cast<const uint32_t *>(st + ST_K + row * 256 + c0 * 2);
-                    const uint32_t qq = *reinterpret_cast<const uint32_t *>(st + ST_Q + row * 256 + c0 * 2);
-#pragma unroll
-                    for (int ch = 0; ch < 2; ++ch) {
-                        kx[ch][r] = m * bf16_half(kk, ch);
-                        qx[ch][r] = m * bf16_half(qq, ch);
-                        suf[ch][r] = ex2_approx(m * unbounded_lg(a.gate_mode, bf16_half(zz, ch), escale));
-                    }
+                    const uint32_t kk = in ? *reinterpret_cast<const uint32_t *>(st + ST_K + row * 256 + c0 * 2) : 0u;
+                    const uint32_t qq = in ? *reinterpret_cast<const uint32_t *>(st + ST_Q + row * 256 + c0 * 2) : 0u;
+                    kx[r] = pack2(bf16_half(kk, 0), bf16_half(kk, 1));
+                    qx[r] = pack2(bf16_half(qq, 0), bf16_half(qq, 1));
+                    suf[r] = in ? pack2(ex2_approx(unbounded_lg(a.gate_mode, bf16_half(zz, 0), escale)),
+                                        ex2_approx(unbounded_lg(a.gate_mode, bf16_half(zz, 1), escale)))
+                                : pack2(1.f, 1.f);
                 }
             } else {                                    // one gate per (token, head), or none
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
                     const int row = 8 * hh + r;
-                    const float m = row < nv ? 1.f : 0.f;
-                    const uint32_t kk = *reinterpret_cast<const uint32_t *>(st + ST_K + row * 256 + c0 * 2);
-                    const uint32_t qq = *reinterpret_cast<const uint32_t *>(st + ST_Q + row * 256 + c0 * 2);
+                    const bool in = row < nv;
+                    const uint32_t kk = in ? *reinterpret_cast<const uint32_t *>(st + ST_K + row * 256 + c0 * 2) : 0u;
+                    const uint32_t qq = in ? *reinterpret_cast<const uint32_t *>(st + ST_Q + row * 256 + c0 * 2) : 0u;
                     const float z = __shfl_sync(0xffffffffu, zs, row);
                     float lg;
                     if (unbounded) {
@@ -338,52 +339,55 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         const float sig = rcp_approx(1.f + ex2_approx(-kLog2e * escale * z));
                         lg = gate_none ? 0.f : (kLog2e * a.g_min) * sig;
                     }
-                    const float a_r = ex2_approx(m * lg);
-#pragma unroll
-                    for (int ch = 0; ch < 2; ++ch) {
-                        kx[ch][r] = m * bf16_half(kk, ch);
-                        qx[ch][r] = m * bf16_half(qq, ch);
-                        suf[ch][r] = a_r;
-                    }
+                    const float a_r = in ? ex2_approx(lg) : 1.f;
+                    kx[r] = pack2(bf16_half(kk, 0), bf16_half(kk, 1));
+                    qx[r] = pack2(bf16_half(qq, 0), bf16_half(qq, 1));
+                    suf[r] = pack2(a_r, a_r);
                 }
             }
             float gC[2], inv_gC[2];
-#pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                float run = 1.f;
+            {
+                f32x2 run = pack2(1.f, 1.f);
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
-                    run *= suf[ch][r];
-                    pre[ch][r] = run;
+                    run = fmul2(run, suf[r]);
+                    pre[r] = run;
                 }
-                const float other = __shfl_xor_sync(0xffffffffu, run, 16);   // the other half's product
-                gC[ch] = run * other;                                       // e^{b_C}
-                const float lead = hh ? other : 1.f;                        // decay before this half
-                const float tail = hh ? 1.f : other;                        // decay after this half
-                float back = tail;
+                const float2 rr = unpack2(run);
+                const float2 other = make_float2(__shfl_xor_sync(0xffffffffu, rr.x, 16),   // the other half's
+                                                 __shfl_xor_sync(0xffffffffu, rr.y, 16));  // products
+                const f32x2 oth = pack2(other.x, other.y);
+                const float2 g2 = unpack2(fmul2(run, oth));                             // e^{b_C}
+                gC[0] = g2.x; gC[1] = g2.y;
+                const f32x2 one = pack2(1.f, 1.f);
+                const f32x2 lead = hh ? oth : one;                                       // decay before this half
+                f32x2 back = hh ? one : oth;                                             // decay after this half
 #pragma unroll
                 for (int r = 7; r >= 0; --r) {
-                    const float a_r = suf[ch][r];
-                    suf[ch][r] = back;                                      // e^{b_C - b_r}
-                    back *= a_r;
-                    pre[ch][r] *= lead;                                     // e^{b_r}
+                    const f32x2 a_r = suf[r];
+                    suf[r] = back;                                                       // e^{b_C - b_r}
+                    back = fmul2(back, a_r);
+                    pre[r] = fmul2(pre[r], lead);                                        // e^{b_r}
                 }
-                inv_gC[ch] = rcp_approx(gC[ch]);
+                inv_gC[0] = rcp_approx(gC[0]);
+                inv_gC[1] = rcp_approx(gC[1]);
             }
             if (hh == 0) *reinterpret_cast<float2 *>(st + ST_GC + c0 * 4) = make_float2(gC[0], gC[1]);
             if (c < C) reinterpret_cast<float *>(st + ST_BETA)[c] = bt;
+            const f32x2 igc = pack2(inv_gC[0], inv_gC[1]);
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const int row = 8 * hh + r;
-                const float kg0 = kx[0][r] * pre[0][r], kg1 = kx[1][r] * pre[1][r];
-                const float qg0 = qx[0][r] * pre[0][r], qg1 = qx[1][r] * pre[1][r];
-                const float kd0 = kx[0][r] * suf[0][r], kd1 = kx[1][r] * suf[1][r];
-                *reinterpret_cast<uint32_t *>(st + ST_WQ + off_kmajor_sw128(16 + row, c0, 32)) = pack_h2(qg0, qg1);
-                *reinterpret_cast<uint32_t *>(st + ST_KD + off_mnmajor_sw128(c0, row, C)) = pack_h2(kd0, kd1);
-                *reinterpret_cast<float2 *>(qgm + row * PADF + c0) = make_float2(to_tf32(qg0), to_tf32(qg1));
-                *reinterpret_cast<float2 *>(kgm + row * PADF + c0) = make_float2(to_tf32(kg0), to_tf32(kg1));
-                *reinterpret_cast<float2 *>(kim + row * PADF + c0) =
-                    make_float2(to_tf32(kd0 * inv_gC[0]), to_tf32(kd1 * inv_gC[1]));
+                const float2 kg = unpack2(fmul2(kx[r], pre[r]));
+                const float2 qg = unpack2(fmul2(qx[r], pre[r]));
+                const f32x2 kd2 = fmul2(kx[r], suf[r]);
+                const float2 kd = unpack2(kd2);
+                const float2 ki = unpack2(fmul2(kd2, igc));
+                *reinterpret_cast<uint32_t *>(st + ST_WQ + off_kmajor_sw128(16 + row, c0, 32)) = pack_h2(qg.x, qg.y);
+                *reinterpret_cast<uint32_t *>(st + ST_KD + off_mnmajor_sw128(c0, row, C)) = pack_h2(kd.x, kd.y);
+                *reinterpret_cast<float2 *>(qgm + row * PADF + c0) = make_float2(to_tf32(qg.x), to_tf32(qg.y));
+                *reinterpret_cast<float2 *>(kgm + row * PADF + c0) = make_float2(to_tf32(kg.x), to_tf32(kg.y));
+                *reinterpret_cast<float2 *>(kim + row * PADF + c0) = make_float2(to_tf32(ki.x), to_tf32(ki.y));
             }
             if (named_bar_or(pbar, 128, *abort_flag != 0)) break;   // uniform across the warpgroup
             const bool pair_tile =
@@ -645,7 +649,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
             for (int p = 1; p < NACC; ++p)
 #pragma unroll
-                for (int r = 0; r < 8; ++r) o[r] += x[p - 1][r];
+                for (int r = 0; r < 8; r += 2) {
+                    const float2 y = unpack2(fadd2(pack2(o[r], o[r + 1]), pack2(x[p - 1][r], x[p - 1][r + 1])));
+                    o[r] = y.x; o[r + 1] = y.y;
+                }
             const int tt0 = bos + tt * C;
             const int nvv = min(C, eos - tt0);
             if (nvv == C) {
@@ -689,7 +696,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
                 for (int p = 0; p < NACC; ++p)
 #pragma unroll
-                    for (int r = 0; r < 8; ++r) uj[r] += v[p][r];
+                    for (int r = 0; r < 8; r += 2) {
+                        const float2 x = unpack2(fadd2(pack2(uj[r], uj[r + 1]), pack2(v[p][r], v[p][r + 1])));
+                        uj[r] = x.x; uj[r + 1] = x.y;
+                    }
                 uint32_t p[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) p[i] = pack_h2(uj[2 * i], uj[2 * i + 1]);
@@ -726,8 +736,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         const float4 g4 = *reinterpret_cast<const float4 *>(gc + (cb + b2) * 16 + q4 * 4);
                         float *sp = S + (cb + b2) * 16 + q4 * 4;
                         const float *ip = inc[b2] + q4 * 4;
-                        sp[0] = fmaf(g4.x, sp[0], ip[0]); sp[1] = fmaf(g4.y, sp[1], ip[1]);
-                        sp[2] = fmaf(g4.z, sp[2], ip[2]); sp[3] = fmaf(g4.w, sp[3], ip[3]);
+                        const float2 lo = unpack2(ffma2(pack2(g4.x, g4.y), pack2(sp[0], sp[1]), pack2(ip[0], ip[1])));
+                        const float2 hi = unpack2(ffma2(pack2(g4.z, g4.w), pack2(sp[2], sp[3]), pack2(ip[2], ip[3])));
+                        sp[0] = lo.x; sp[1] = lo.y; sp[2] = hi.x; sp[3] = hi.y;
                     }
                 }
             }
