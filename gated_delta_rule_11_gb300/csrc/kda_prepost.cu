@@ -20,11 +20,16 @@
 // consecutive tokens of one (tensor, head): one TMA copy brings the run and
 // the three tokens before it ([67, d], rows before the first token read as
 // zero) into shared memory, so many runs are in flight per SM without
-// holding registers; each of four warps then walks 16 tokens with the
-// three previous inputs of its lane's d/32 channels in registers, the L2
-// norm as a warp reduction.  Inputs before a sequence's first token come
-// from the caller's conv state (or zero), never from the previous sequence.
+// holding registers; in each of four warps a group of d/8 lanes owns a
+// token (8 channels per lane, 16-byte loads and stores) and walks its
+// share of the warp's 16 tokens with the three previous inputs in
+// registers, the L2 norm as a group reduction.  A run that stays inside one
+// sequence takes straight-line code; inputs before a sequence's first token
+// come from the caller's conv state (or zero), never from the previous
+// sequence.
 // post: one warp per (token, head) row, four rows per warp in flight.
+#include <type_traits>
+
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
 
@@ -65,25 +70,6 @@ template <> struct Lanes<float, 4> {
     }
 };
 // A lane's CPL channels of one token row in shared memory.
-template <typename T, int CPL>
-__device__ __forceinline__ void load_row(const T *p, float (&x)[CPL]) {
-    if constexpr (CPL == 4 && sizeof(T) == 2) {
-        const uint2 w = *reinterpret_cast<const uint2 *>(p);
-        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&w.x);
-        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&w.y);
-        x[0] = __low2float(a); x[1] = __high2float(a); x[2] = __low2float(b); x[3] = __high2float(b);
-    } else if constexpr (CPL == 4) {
-        const float4 w = *reinterpret_cast<const float4 *>(p);
-        x[0] = w.x; x[1] = w.y; x[2] = w.z; x[3] = w.w;
-    } else {
-#pragma unroll
-        for (int i = 0; i < CPL; ++i) {
-            if constexpr (sizeof(T) == 2) x[i] = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[i]);
-            else x[i] = reinterpret_cast<const float *>(p)[i];
-        }
-    }
-}
-
 template <typename T, int CPL> struct LanesScalar {
     static __device__ __forceinline__ void load(const T *p, float (&x)[CPL]) {
 #pragma unroll
@@ -105,20 +91,9 @@ template <> struct Lanes<float, 1> : LanesScalar<float, 1> {};
 // an IEEE division per element would bound it.  For x < -88, e^{-x}
 // overflows and Sigmoid returns 0, its limit.
 __device__ __forceinline__ float sigmoid(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
-__device__ __forceinline__ float swish(float x) { return x * sigmoid(x); }
 
 // Swish of a channel pair: the exponentials and reciprocals stay per lane
 // (MUFU), the rest is packed.  Same arithmetic as swish() per element.
-__device__ __forceinline__ sm100::f32x2 swish2(sm100::f32x2 c) {
-    using namespace sm100;
-    const float2 m = unpack2(fmul2(c, pack2(-1.4426950408889634f, -1.4426950408889634f)));
-    float ex, ey;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ex) : "f"(m.x));
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ey) : "f"(m.y));
-    const float2 den = unpack2(fadd2(pack2(ex, ey), pack2(1.f, 1.f)));
-    return fmul2(c, pack2(__fdividef(1.0f, den.x), __fdividef(1.0f, den.y)));
-}
-
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -152,51 +127,105 @@ constexpr int prep_smem_bytes() {
     return (((kRun + kHalo) * D * static_cast<int>(sizeof(Tin)) + 15) & ~15) + 16;   // tile + mbarrier
 }
 
+// Eight consecutive channels as four (even, odd) f32x2 pairs: global and
+// shared-memory rows (16-byte aligned) of bf16 or fp32.
+template <typename T> struct Oct;
+template <> struct Oct<__nv_bfloat16> {
+    static __device__ __forceinline__ void unpack(const uint4 w, sm100::f32x2 (&x)[4]) {
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) x[p] = sm100::pack2(__uint_as_float(u[p] << 16), __uint_as_float(u[p] & 0xffff0000u));
+    }
+    static __device__ __forceinline__ void ld_global(const __nv_bfloat16 *p, sm100::f32x2 (&x)[4]) {
+        unpack(__ldg(reinterpret_cast<const uint4 *>(p)), x);
+    }
+    static __device__ __forceinline__ void ld_shared(const __nv_bfloat16 *p, sm100::f32x2 (&x)[4]) {
+        unpack(*reinterpret_cast<const uint4 *>(p), x);
+    }
+    static __device__ __forceinline__ void st_global(__nv_bfloat16 *p, const sm100::f32x2 (&x)[4]) {
+        uint32_t u[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 f = sm100::unpack2(x[q]);
+            const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+            u[q] = *reinterpret_cast<const uint32_t *>(&b);
+        }
+        *reinterpret_cast<uint4 *>(p) = make_uint4(u[0], u[1], u[2], u[3]);
+    }
+};
+template <> struct Oct<float> {
+    static __device__ __forceinline__ void from4(const float4 a, const float4 b, sm100::f32x2 (&x)[4]) {
+        x[0] = sm100::pack2(a.x, a.y); x[1] = sm100::pack2(a.z, a.w);
+        x[2] = sm100::pack2(b.x, b.y); x[3] = sm100::pack2(b.z, b.w);
+    }
+    static __device__ __forceinline__ void ld_global(const float *p, sm100::f32x2 (&x)[4]) {
+        from4(__ldg(reinterpret_cast<const float4 *>(p)), __ldg(reinterpret_cast<const float4 *>(p) + 1), x);
+    }
+    static __device__ __forceinline__ void ld_shared(const float *p, sm100::f32x2 (&x)[4]) {
+        from4(reinterpret_cast<const float4 *>(p)[0], reinterpret_cast<const float4 *>(p)[1], x);
+    }
+    static __device__ __forceinline__ void st_global(float *p, const sm100::f32x2 (&x)[4]) {
+        const float2 a = sm100::unpack2(x[0]), b = sm100::unpack2(x[1]), c = sm100::unpack2(x[2]),
+                     e = sm100::unpack2(x[3]);
+        reinterpret_cast<float4 *>(p)[0] = make_float4(a.x, a.y, b.x, b.y);
+        reinterpret_cast<float4 *>(p)[1] = make_float4(c.x, c.y, e.x, e.y);
+    }
+};
+
+// One CTA per run of kRun tokens of one (tensor, head).  A group of D / 8
+// lanes owns a token (8 channels per lane), so a warp works on 32 * 8 / D
+// tokens at once; each group walks its own consecutive tokens with the three
+// previous inputs in registers.
 template <typename Tin, int D>
 __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                                PrepArgs a) {
     using namespace sm100;
-    constexpr int CPL = D / 32;                 // channels per lane
-    constexpr int TILE_BYTES = (kRun + kHalo) * D * static_cast<int>(sizeof(Tin));
+    constexpr int CPL = 8;                       // channels per lane
+    constexpr int LPT = D / CPL;                 // lanes per token
+    constexpr int SLOTS = 32 / LPT;              // tokens per warp step
     constexpr int PER_WARP = kRun / kPrepWarps;
+    constexpr int PER_SLOT = PER_WARP / SLOTS;   // consecutive tokens per lane group
+    static_assert(PER_SLOT >= 1 && PER_WARP % SLOTS == 0, "run split");
+    constexpr int TILE_BYTES = (kRun + kHalo) * D * static_cast<int>(sizeof(Tin));
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const Tin *tile = reinterpret_cast<const Tin *>(smem_raw);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem_raw + ((TILE_BYTES + 15) & ~15));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H;
-    const long long row_tasks = static_cast<long long>(3) * H;     // (tensor, head) pairs
-    const long long run_tasks = static_cast<long long>((a.T_total + kRun - 1) / kRun) * row_tasks;
-    const long long task = blockIdx.x;
-    const Tin *x = static_cast<const Tin *>(a.x);
+    // task counts fit in 32 bits (the launcher checks)
+    const int row_tasks = 3 * H;                                   // (tensor, head) pairs
+    const int run_tasks = (a.T_total + kRun - 1) / kRun * row_tasks;
+    const int task = static_cast<int>(blockIdx.x);
     const Tin *sin = static_cast<const Tin *>(a.state_in);
     Tin *sout = static_cast<Tin *>(a.state_out);
     const size_t tok_x = static_cast<size_t>(3) * H * D;             // one token of x_qkv
 
     if (task >= run_tasks) {
         // conv state of an empty sequence passes through (or becomes zero)
-        const long long et = task - run_tasks;
-        if (warp != 0 || et >= static_cast<long long>(a.N) * row_tasks || !sout) return;
-        const int n = static_cast<int>(et / row_tasks);
-        const int mh = static_cast<int>(et % row_tasks);
+        constexpr int CPE = D / 32;
+        const int et = task - run_tasks;
+        if (warp != 0 || et >= a.N * row_tasks || !sout) return;
+        const int n = et / row_tasks;
+        const int mh = et % row_tasks;
         int bos, eos;
         span_of(a, n, bos, eos);
         if (eos > bos) return;
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
-            const size_t o = (static_cast<size_t>(n) * 3 + j) * tok_x + static_cast<size_t>(mh) * D + lane * CPL;
-            float w[CPL];
-            if (sin) Lanes<Tin, CPL>::load(sin + o, w);
+            const size_t o = (static_cast<size_t>(n) * 3 + j) * tok_x + static_cast<size_t>(mh) * D + lane * CPE;
+            float w[CPE];
+            if (sin) Lanes<Tin, CPE>::load(sin + o, w);
             else
 #pragma unroll
-                for (int i = 0; i < CPL; ++i) w[i] = 0.f;
-            Lanes<Tin, CPL>::store(sout + o, w);
+                for (int i = 0; i < CPE; ++i) w[i] = 0.f;
+            Lanes<Tin, CPE>::store(sout + o, w);
         }
         return;
     }
 
-    const int run = static_cast<int>(task / row_tasks);
-    const int mh = static_cast<int>(task % row_tasks);     // m * H + h
+    const int run = task / row_tasks;
+    const int mh = task % row_tasks;                       // m * H + h
     const int m = mh / H, h = mh % H;
     const int t_begin = run * kRun, t_end = min(t_begin + kRun, a.T_total);
     if (tid == 0) {
@@ -209,110 +238,122 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(const __grid_cons
         tma_load_3d(smem_raw, &tm_x, bar, 0, mh, t_begin - kHalo);
     }
 
-    // conv taps of this lane's channels: w[ch][0..3], tap 3 = current token
-    const size_t col = static_cast<size_t>(mh) * D + lane * CPL;   // this lane's channels in a token of x
-    float wt[CPL][4];
+    const int slot = lane / LPT, sl = lane % LPT;
+    // conv taps of this lane's channels as (even, odd) pairs: wt[tap][pair], tap 3 = current token
+    const int c0 = sl * CPL;
+    f32x2 wt[4][4];
 #pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-        const float4 w4 = __ldg(reinterpret_cast<const float4 *>(a.conv_w) + static_cast<size_t>(mh) * D + lane * CPL + i);
-        wt[i][0] = w4.x; wt[i][1] = w4.y; wt[i][2] = w4.z; wt[i][3] = w4.w;
+    for (int p = 0; p < 4; ++p) {
+        const float4 e = __ldg(reinterpret_cast<const float4 *>(a.conv_w) + static_cast<size_t>(mh) * D + c0 + 2 * p);
+        const float4 o = __ldg(reinterpret_cast<const float4 *>(a.conv_w) + static_cast<size_t>(mh) * D + c0 + 2 * p + 1);
+        wt[0][p] = pack2(e.x, o.x); wt[1][p] = pack2(e.y, o.y);
+        wt[2][p] = pack2(e.z, o.z); wt[3][p] = pack2(e.w, o.w);
     }
-    Tin *dst = static_cast<Tin *>(m == 0 ? a.q : (m == 1 ? a.k : a.v));
+    const size_t col = static_cast<size_t>(mh) * D + c0;            // this lane's channels in a token of x
+    Tin *dst = static_cast<Tin *>(m == 0 ? a.q : (m == 1 ? a.k : a.v)) + static_cast<size_t>(h) * D + c0;
     const size_t tok_o = static_cast<size_t>(H) * D;
-    const int w_begin = t_begin + warp * PER_WARP, w_end = min(w_begin + PER_WARP, t_end);
+    const int s_begin = t_begin + warp * PER_WARP + slot * PER_SLOT;
+    const int s_end = min(s_begin + PER_SLOT, t_end);
     int n = 0, bos = 0, eos = 0;
-    if (w_begin < w_end) {
-        n = seq_of(a, w_begin);
+    if (s_begin < s_end) {
+        n = seq_of(a, s_begin);
         span_of(a, n, bos, eos);
-        while (eos <= w_begin && n + 1 < a.N) {      // empty sequences at w_begin
+        while (eos <= s_begin && n + 1 < a.N) {      // empty sequences at s_begin
             ++n;
             span_of(a, n, bos, eos);
         }
     }
-    if (!mbar_wait(bar, 0, kPrepWaitNs)) {
+    // warp-uniform: every lane of a warp takes part in the group reductions below
+    if (!__all_sync(0xffffffffu, mbar_wait(bar, 0, kPrepWaitNs))) {
         if (lane == 0) atomicAdd(&g_prep_timeouts, 1u);
         return;
     }
-    auto row_ptr = [&](int t) { return tile + static_cast<size_t>(t - t_begin + kHalo) * D + lane * CPL; };
+    auto row_ptr = [&](int t) { return tile + static_cast<size_t>(t - t_begin + kHalo) * D + c0; };
 
     // window: x of the three tokens before the current one (win[0] oldest)
-    float win[3][CPL];
+    f32x2 win[3][4] = {};
     auto fill_window = [&](int t) {              // window for token t of sequence n (bos <= t)
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
             const int p = t - 3 + j;
             if (p >= bos) {
-                load_row<Tin, CPL>(row_ptr(p), win[j]);
+                Oct<Tin>::ld_shared(row_ptr(p), win[j]);
             } else if (sin) {
                 const int tap = p - bos + 3;     // 0..2: state token bos - 3 + tap
-                Lanes<Tin, CPL>::load(sin + (static_cast<size_t>(n) * 3 + tap) * tok_x + col, win[j]);
+                Oct<Tin>::ld_global(sin + (static_cast<size_t>(n) * 3 + tap) * tok_x + col, win[j]);
             } else {
 #pragma unroll
-                for (int i = 0; i < CPL; ++i) win[j][i] = 0.f;
+                for (int q = 0; q < 4; ++q) win[j][q] = 0ull;
             }
         }
     };
-    if (w_begin < w_end) fill_window(w_begin);
-#pragma unroll 2
-    for (int t = w_begin; t < w_end; ++t) {
-        if (t >= eos) {                           // next sequence: restart the window
+    if (s_begin < s_end) fill_window(s_begin);
+    const f32x2 nl2e = pack2(-1.4426950408889634f, -1.4426950408889634f), one = pack2(1.f, 1.f);
+    // one token; Boundary: the run may cross a sequence end (else straight-line code)
+    auto token = [&](int t, bool act, auto boundary) {
+        if (decltype(boundary)::value && act && t >= eos) {                    // next sequence: restart the window
             do {
                 ++n;
                 span_of(a, n, bos, eos);
             } while (eos <= t && n + 1 < a.N);
             fill_window(t);
         }
-        float xt[CPL];
-        load_row<Tin, CPL>(row_ptr(t), xt);
-        float y[CPL];
-        float ss = 0.f;
-        if constexpr (CPL == 4) {                 // channel pairs in f32x2
-            using namespace sm100;
-            f32x2 ss2 = 0ull;
+        f32x2 xt[4], y[4], ss2 = 0ull;
+        if (act) Oct<Tin>::ld_shared(row_ptr(t), xt);
+        else
 #pragma unroll
-            for (int p2 = 0; p2 < 2; ++p2) {
-                const int i0 = 2 * p2, i1 = i0 + 1;
-                const f32x2 x2 = pack2(xt[i0], xt[i1]);
-                f32x2 c = fmul2(pack2(wt[i0][0], wt[i1][0]), pack2(win[0][i0], win[0][i1]));
-                c = ffma2(pack2(wt[i0][1], wt[i1][1]), pack2(win[1][i0], win[1][i1]), c);
-                c = ffma2(pack2(wt[i0][2], wt[i1][2]), pack2(win[2][i0], win[2][i1]), c);
-                c = ffma2(pack2(wt[i0][3], wt[i1][3]), x2, c);
-                const f32x2 yy = swish2(c);
-                ss2 = ffma2(yy, yy, ss2);
-                const float2 yv = unpack2(yy);
-                y[i0] = yv.x;
-                y[i1] = yv.y;
-            }
-            const float2 s2 = unpack2(ss2);
-            ss = s2.x + s2.y;
+            for (int q = 0; q < 4; ++q) xt[q] = 0ull;
 #pragma unroll
-            for (int i = 0; i < CPL; ++i) {
-                win[0][i] = win[1][i];
-                win[1][i] = win[2][i];
-                win[2][i] = xt[i];
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < CPL; ++i) {
-                const float c = wt[i][0] * win[0][i] + wt[i][1] * win[1][i] + wt[i][2] * win[2][i] + wt[i][3] * xt[i];
-                y[i] = swish(c);
-                ss += y[i] * y[i];
-                win[0][i] = win[1][i];
-                win[1][i] = win[2][i];
-                win[2][i] = xt[i];
-            }
+        for (int q = 0; q < 4; ++q) {
+            f32x2 c = fmul2(wt[0][q], win[0][q]);
+            c = ffma2(wt[1][q], win[1][q], c);
+            c = ffma2(wt[2][q], win[2][q], c);
+            c = ffma2(wt[3][q], xt[q], c);
+            // Swish(c) = c / (1 + e^{-c})
+            const float2 e = unpack2(fmul2(c, nl2e));
+            float ex, ey;
+            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ex) : "f"(e.x));
+            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ey) : "f"(e.y));
+            const float2 den = unpack2(fadd2(pack2(ex, ey), one));
+            y[q] = fmul2(c, pack2(__fdividef(1.0f, den.x), __fdividef(1.0f, den.y)));
+            ss2 = ffma2(y[q], y[q], ss2);
+            win[0][q] = win[1][q];
+            win[1][q] = win[2][q];
+            win[2][q] = xt[q];
         }
         if (m < 2) {                              // q, k: L2Norm over the head's d channels
-            const float r = rsqrtf(warp_sum(ss) + a.l2_eps);
+            const float2 s2 = unpack2(ss2);
+            float ss = s2.x + s2.y;
 #pragma unroll
-            for (int i = 0; i < CPL; ++i) y[i] *= r;
+            for (int o = LPT / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            const float r = rsqrtf(ss + a.l2_eps);
+            const f32x2 r2 = pack2(r, r);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) y[q] = fmul2(y[q], r2);
         }
-        Lanes<Tin, CPL>::store(dst + static_cast<size_t>(t) * tok_o + static_cast<size_t>(h) * D + lane * CPL, y);
-        if (t == eos - 1 && sout) {               // last token: save the window as conv state
+        if (act) {
+            Oct<Tin>::st_global(dst + static_cast<size_t>(t) * tok_o, y);
+            if (decltype(boundary)::value && t == eos - 1 && sout) {           // last token: save the window as conv state
 #pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    Tin *sp = sout + (static_cast<size_t>(n) * 3 + j) * tok_x + col;
+                    Oct<Tin>::st_global(sp, win[j]);
+                }
+            }
+        }
+    };
+    // fast path: every group's tokens are PER_SLOT tokens of one sequence
+    const bool inside = s_end - s_begin == PER_SLOT && eos >= s_end;
+    if (__all_sync(0xffffffffu, inside)) {
+    #pragma unroll
+        for (int u2 = 0; u2 < PER_SLOT; ++u2) token(s_begin + u2, true, std::false_type{});
+        if (eos == s_end && sout) {           // the group ends its sequence: save the window
+    #pragma unroll
             for (int j = 0; j < 3; ++j)
-                Lanes<Tin, CPL>::store(sout + (static_cast<size_t>(n) * 3 + j) * tok_x + col, win[j]);
+                Oct<Tin>::st_global(sout + (static_cast<size_t>(n) * 3 + j) * tok_x + col, win[j]);
         }
+    } else {
+        for (int u2 = 0; u2 < PER_SLOT; ++u2) token(s_begin + u2, s_begin + u2 < s_end, std::true_type{});
     }
     // beta = Sigmoid(logit) for this run's tokens and head h (the q-tensor CTAs)
     if (m == 0 && a.beta_logit) {
