@@ -367,7 +367,10 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(const __grid_cons
 template <typename Tin, int D>
 __global__ void __launch_bounds__(kWarps * 32) output_gate_kernel(PostArgs a) {
     constexpr int CPL = D / 32;
-    constexpr int RPW = 4;                       // rows per warp
+    // bf16 rows are held as the loaded words and widened only when used, so
+    // every row's loads are issued before the first one is waited on
+    constexpr bool RAW = sizeof(Tin) == 2 && CPL == 4;
+    constexpr int RPW = 4;                               // rows per warp
     const int lane = threadIdx.x & 31;
     const long long row0 = (static_cast<long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5)) * RPW;
     const Tin *o = static_cast<const Tin *>(a.o);
@@ -376,25 +379,52 @@ __global__ void __launch_bounds__(kWarps * 32) output_gate_kernel(PostArgs a) {
     float w[CPL];
 #pragma unroll
     for (int i = 0; i < CPL; ++i) w[i] = a.norm_w ? __ldg(a.norm_w + lane * CPL + i) : 1.f;
-    float ov[RPW][CPL], gv[RPW][CPL];
+    if constexpr (RAW) {
+        uint2 ow[RPW], gw[RPW];
 #pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-        if (row0 + r >= a.rows) break;
-        const size_t off = static_cast<size_t>(row0 + r) * D + lane * CPL;
-        Lanes<Tin, CPL>::load(o + off, ov[r]);
-        Lanes<Tin, CPL>::load(g + off, gv[r]);
-    }
+        for (int r = 0; r < RPW; ++r) {
+            if (row0 + r >= a.rows) break;
+            const size_t off = static_cast<size_t>(row0 + r) * D + lane * CPL;
+            ow[r] = __ldg(reinterpret_cast<const uint2 *>(o + off));
+            gw[r] = __ldg(reinterpret_cast<const uint2 *>(g + off));
+        }
 #pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-        if (row0 + r >= a.rows) break;
-        float ss = 0.f;
+        for (int r = 0; r < RPW; ++r) {
+            if (row0 + r >= a.rows) break;
+            const float ov[4] = {__uint_as_float(ow[r].x << 16), __uint_as_float(ow[r].x & 0xffff0000u),
+                                  __uint_as_float(ow[r].y << 16), __uint_as_float(ow[r].y & 0xffff0000u)};
+            const float gv[4] = {__uint_as_float(gw[r].x << 16), __uint_as_float(gw[r].x & 0xffff0000u),
+                                  __uint_as_float(gw[r].y << 16), __uint_as_float(gw[r].y & 0xffff0000u)};
+            float ss = 0.f;
 #pragma unroll
-        for (int i = 0; i < CPL; ++i) ss += ov[r][i] * ov[r][i];
-        const float inv = rsqrtf(warp_sum(ss) / D + a.eps);
-        float out[CPL];
+            for (int i = 0; i < 4; ++i) ss += ov[i] * ov[i];
+            const float inv = rsqrtf(warp_sum(ss) / D + a.eps);
+            float out[4];
 #pragma unroll
-        for (int i = 0; i < CPL; ++i) out[i] = sigmoid(gv[r][i]) * (ov[r][i] * inv * w[i]);
-        Lanes<Tin, CPL>::store(y + static_cast<size_t>(row0 + r) * D + lane * CPL, out);
+            for (int i = 0; i < 4; ++i) out[i] = sigmoid(gv[i]) * (ov[i] * inv * w[i]);
+            Lanes<Tin, CPL>::store(y + static_cast<size_t>(row0 + r) * D + lane * CPL, out);
+        }
+    } else {
+        float ov[RPW][CPL], gv[RPW][CPL];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            if (row0 + r >= a.rows) break;
+            const size_t off = static_cast<size_t>(row0 + r) * D + lane * CPL;
+            Lanes<Tin, CPL>::load(o + off, ov[r]);
+            Lanes<Tin, CPL>::load(g + off, gv[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            if (row0 + r >= a.rows) break;
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) ss += ov[r][i] * ov[r][i];
+            const float inv = rsqrtf(warp_sum(ss) / D + a.eps);
+            float out[CPL];
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) out[i] = sigmoid(gv[r][i]) * (ov[r][i] * inv * w[i]);
+            Lanes<Tin, CPL>::store(y + static_cast<size_t>(row0 + r) * D + lane * CPL, out);
+        }
     }
 }
 
@@ -436,7 +466,8 @@ cudaError_t launch_prep_t(int d, const PrepArgs &a, cudaStream_t s) {
 
 template <typename Tin>
 cudaError_t launch_post_t(int d, const PostArgs &a, cudaStream_t s) {
-    const long long blocks = (a.rows + kWarps * 4 - 1) / (kWarps * 4);
+    constexpr int rpw = 4;                       // the kernel's rows per warp
+    const long long blocks = (a.rows + kWarps * rpw - 1) / (kWarps * rpw);
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>(blocks));
