@@ -20,6 +20,8 @@
 // of S, W, Q e^b, Vt, A, K e^{b_C-b} is bounded well inside fp16's range),
 // L and A come from tf32 mma.sync on fp32 operands (K e^-b reaches e^80, out
 // of fp16 range), and U, W, T, the gates and the state master are fp32.
+// U is a bf16 product: v is bf16 already, and T Diag(beta) (tf32-rounded,
+// 11 significant bits) is split exactly into bf16 hi + lo parts.
 //
 // Every tensor-core product is computed transposed so that its M side is a
 // 128-wide head dimension (tcgen05 M = 128, TMEM lane j = value channel j):
@@ -35,6 +37,9 @@
 //       -> E[:, 16:32] = O^T / scale
 //   (h) H[:, 0:128]  = Vt^T (K e^{b_C - b})              M128 N128 K16
 //       -> the state increment, transposed
+//   (u) U^T = V^T (T Diag(beta))^T, hi + lo               M128 N16  K16 (x2)
+//       -> read by the chain from TMEM (two slots, tile parity); V comes
+//          from TMA in the 128B-swizzled MN-major operand layout
 // E is double-buffered in TMEM (tile parity), so tile t's O is read out
 // while tile t+1's (g)/(h) run, off the serial path; full tiles of O are
 // staged in shared memory and written with one TMA store.
@@ -46,17 +51,19 @@
 //                          Vt^T = U^T + D[:,0:16] as the fp16 operand of
 //                          (g)/(h), store O, apply S = Diag(e^{b_C}) S +
 //                          increment and write the fp16 copy of S^T (into
-//                          TMEM) that the next tile's (e) reads.  One elected chain thread
-//                          issues the tcgen05 products and commits them, and
+//                          TMEM) that the next tile's (e) reads.  Elected chain threads
+//                          issue the tcgen05 products ((u) for the next tile by
+//                          a thread idle while (e) runs) and commit them, and
 //                          the TMA loads of the q, k, g_raw, v tiles (16
-//                          tokens each) into a 3-stage ring, refilling a
+//                          tokens each) into a 4-stage ring, refilling a
 //                          stage as soon as the chain has finished with it.
 //   warps 8-15 producer  : two warpgroups taking alternate tiles, each with
 //                          its own scratch; thread c owns key channel c: gate (eq. 5) and
 //                          in-tile decays as running products of the
 //                          retentions, decay-scaled operands, L and A (one
 //                          16x8 block per warp), the triangular solve
-//                          (first warp), W and U (tf32 mma.sync).
+//                          (first warp), W (tf32 mma.sync) and the bf16
+//                          hi/lo operand of (u).
 // The chain is serial per tile; the producer and TMA run up to 3 tiles ahead.
 // Tokens past a sequence's end are masked in the producer (k = q = 0, g = 0,
 // beta = 0), which makes U, W, A and the increment vanish for them.
@@ -88,11 +95,11 @@ constexpr int PADF = 132;        // fp32 row stride of the mma.sync operand tile
 constexpr int ST_Q = 0;          // [16][128] bf16 (TMA, unswizzled)
 constexpr int ST_K = 4096;
 constexpr int ST_Z = 8192;
-constexpr int ST_V = 12288;
+constexpr int ST_V = 12288;      // A of U^T: bf16 MN-major SW128 (TMA, two 64-channel boxes)
 constexpr int ST_WQ = 16384;     // B of (e): fp16 K-major SW128, 32 rows x 128 (rows 0-15 -W, 16-31 Q e^b)
 constexpr int ST_KD = 24576;     // B of (h): fp16 MN-major SW128, mn = c, k = s
 constexpr int ST_AT = 28672;     // B of (g): fp16 K-major none, 16 rows x 16
-constexpr int ST_U = 29696;      // fp32 [16][128] U
+constexpr int ST_TB = 29696;     // B of U^T: bf16 K-major none, T Diag(beta) split hi | lo (16 x 16 each)
 constexpr int ST_GC = 37888;     // fp32 [128] e^{b_C}
 constexpr int ST_BETA = 38400;   // fp32 [16]
 constexpr int STAGE_BYTES = 38912;
@@ -116,6 +123,7 @@ constexpr uint32_t TM_E = 0;     // two E buffers of NACC x 32 columns
 constexpr uint32_t TM_H = 256;   // 128-column H
 constexpr uint32_t TM_ST = 384;  // S^T fp16, 128 K values packed in 64 columns
 constexpr uint32_t TM_VT = 448;  // Vt^T fp16, 16 K values packed in 8 columns
+constexpr uint32_t TM_U = 464;   // two U^T slots of 16 columns (tile parity)
 constexpr uint32_t E_BUF = NACC * 32;
 constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_FLAG = OFF_SLOT + 4;
@@ -221,7 +229,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             mbar_init(&bars[B_RAW + s], 1);
             mbar_init(&bars[B_FULL + s], 128);
         }
-        mbar_init(&bars[B_VT], NACC);     // one commit per (e) issuer
+        mbar_init(&bars[B_VT], NACC + 1); // one commit per (e) issuer and the U^T issuer
         mbar_init(&bars[B_UPD], 2);       // commits of the (g) and (h) issuers
         *abort_flag = 0;
         fence_mbar_init();
@@ -524,9 +532,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tbf[(8 + bi) * TBS + bj8] = to_tf32(-acc * betas[bj8]);
             }
             named_bar_sync(pbar, 128);
-            // W = T Diag(beta) (K e^b) -> rows 0..15 of the (e) B operand hold -W;
-            // U = T Diag(beta) V (fp32) for the chain.  16 x 16 x 128 each, tf32
-            // mma.sync; warp pw covers channels [32 pw, 32 pw + 32).
+            // T Diag(beta) as the bf16 B operand of U^T = V^T (T Diag(beta))^T
+            // (a tcgen05 product the chain issues): hi + lo reproduce the
+            // tf32-rounded values exactly (at most 11 significant bits).
+            {
+                const int r = c >> 3, i0 = 2 * (c & 7);
+                const uint32_t off = (r >> 3) * 256 + (i0 >> 3) * 128 + (r & 7) * 16 + (i0 & 7) * 2;
+                const float x0 = tbf[r * TBS + i0], x1 = tbf[r * TBS + i0 + 1];
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(x0, x1);
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(x0 - __low2float(hi), x1 - __high2float(hi));
+                *reinterpret_cast<__nv_bfloat162 *>(st + ST_TB + off) = hi;
+                *reinterpret_cast<__nv_bfloat162 *>(st + ST_TB + 512 + off) = lo;
+            }
+            // W = T Diag(beta) (K e^b) -> rows 0..15 of the (e) B operand hold -W.
+            // 16 x 16 x 128, tf32 mma.sync; warp pw covers channels [32 pw, 32 pw + 32).
             {
                 const int g = lane >> 2, tq = lane & 3;
                 uint32_t ta[2][4];
@@ -538,23 +557,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     ta[ks][2] = __float_as_uint(tbf[g * TBS + k0 + tq + 4]);
                     ta[ks][3] = __float_as_uint(tbf[(g + 8) * TBS + k0 + tq + 4]);
                 }
-                float *u = reinterpret_cast<float *>(st + ST_U);
-                // all fragment loads and MMAs first, then the stores (which may alias)
-                float dw[4][4], du[4][4];
+                float dw[4][4];
 #pragma unroll
                 for (int nb = 0; nb < 4; ++nb) {
                     const int cn = pw * 32 + nb * 8 + g;          // B-fragment column (channel)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) dw[nb][e] = du[nb][e] = 0.f;
+                    for (int e = 0; e < 4; ++e) dw[nb][e] = 0.f;
 #pragma unroll
                     for (int ks = 0; ks < 2; ++ks) {
                         const int s0 = ks * 8 + tq;
                         const uint32_t bw0 = __float_as_uint(kgm[s0 * PADF + cn]);
                         const uint32_t bw1 = __float_as_uint(kgm[(s0 + 4) * PADF + cn]);
-                        const uint32_t bu0 = __float_as_uint(bf16_at(st + ST_V + s0 * 256 + cn * 2));
-                        const uint32_t bu1 = __float_as_uint(bf16_at(st + ST_V + (s0 + 4) * 256 + cn * 2));
                         mma_1688_tf32(dw[nb], ta[ks][0], ta[ks][1], ta[ks][2], ta[ks][3], bw0, bw1);
-                        mma_1688_tf32(du[nb], ta[ks][0], ta[ks][1], ta[ks][2], ta[ks][3], bu0, bu1);
                     }
                 }
 #pragma unroll
@@ -564,8 +578,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         pack_h2(-dw[nb][0], -dw[nb][1]);
                     *reinterpret_cast<uint32_t *>(st + ST_WQ + off_kmajor_sw128(g + 8, c0, 32)) =
                         pack_h2(-dw[nb][2], -dw[nb][3]);
-                    *reinterpret_cast<float2 *>(u + g * D + c0) = make_float2(du[nb][0], du[nb][1]);
-                    *reinterpret_cast<float2 *>(u + (g + 8) * D + c0) = make_float2(du[nb][2], du[nb][3]);
                 }
             }
             fence_proxy_async_smem();
@@ -591,7 +603,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tma_load_3d(stg + ST_Q, &tm_q, &bars[B_RAW + ss], 0, h, tok);
             tma_load_3d(stg + ST_K, &tm_k, &bars[B_RAW + ss], 0, h, tok);
             if (z_tile) tma_load_3d(stg + ST_Z, &tm_z, &bars[B_RAW + ss], 0, h, tok);
-            tma_load_3d(stg + ST_V, &tm_v, &bars[B_RAW + ss], 0, h, tok);
+            tma_load_3d(stg + ST_V, &tm_v, &bars[B_RAW + ss], 0, h, tok);          // channels 0-63
+            tma_load_3d(stg + ST_V + 2048, &tm_v, &bars[B_RAW + ss], 64, h, tok);  // channels 64-127
         };
         constexpr int TMA_TID = 160, OST_TID = 192;  // lane 0 of chain warps 5 and 6
         if (tid == TMA_TID)
@@ -616,6 +629,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             return true;
         };
         const bool e_issuer = lane == 0 && warp < NACC;   // chain warps 0..3, lane 0
+        // U^T = V^T (T Diag(beta))^T for tile tt into slot tt & 1 (two bf16
+        // products, hi then lo part of T Diag(beta)), committed with (e).
+        constexpr int U_TID = 224;                        // lane 0 of chain warp 7
+        constexpr uint32_t id_u = idesc_f16kind(kTypeBF16, 128, 16, 1, 0);
+        auto issue_u = [&](int tt) -> bool {
+            const int ss = tt % NS;
+            if (!mbar_wait(&bars[B_FULL + ss], (tt / NS) & 1, kWaitLimitNs)) return false;
+            tc_fence_after();
+            const uint32_t st = sb + ss * STAGE_BYTES;
+            const uint64_t av = smem_desc(st + ST_V, 2048, 1024, kLayoutSW128);
+            const uint32_t d = tmem + TM_U + 16u * static_cast<uint32_t>(tt & 1);
+            mma_f16kind(d, av, smem_desc(st + ST_TB, 128, 256, kLayoutNone), id_u, 0);
+            mma_f16kind(d, av, smem_desc(st + ST_TB + 512, 128, 256, kLayoutNone), id_u, 1);
+            mma_commit(&bars[B_VT]);
+            return true;
+        };
 
         float S[HR];
 #pragma unroll
@@ -633,6 +662,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tc_fence_before();
         named_bar_sync(2, NCHAIN);
         if (e_issuer && ntiles > 0 && !issue_e(0, warp)) note_timeout(abort_flag);
+        if (tid == U_TID && ntiles > 0 && !issue_u(0)) note_timeout(abort_flag);
 
         __nv_bfloat16 *gout = static_cast<__nv_bfloat16 *>(a.out);
         uint8_t *ost = base + OFF_OST;
@@ -686,12 +716,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc_fence_after();
             {
                 // tile columns [8 hf, 8 hf + 8) of Vt^T = U^T - (W S)^T
-                const float *u = reinterpret_cast<const float *>(st + ST_U);
                 float uj[8], v[NACC][8];
 #pragma unroll
                 for (int p = 0; p < NACC; ++p) tmem_ld8(e_acc + 32u * p + lane_base + 8 * hf, v[p]);
-#pragma unroll
-                for (int r = 0; r < 8; ++r) uj[r] = u[(8 * hf + r) * D + j];
+                tmem_ld8(tmem + TM_U + 16u * static_cast<uint32_t>(t & 1) + lane_base + 8 * hf, uj);
                 tmem_ld_wait();
 #pragma unroll
                 for (int p = 0; p < NACC; ++p)
@@ -747,6 +775,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (named_bar_or(2, NCHAIN, *abort_flag != 0)) break;   // uniform across the chain
             // every read of this stage (TMA tiles, U, e^{b_C}, MMA operands) is done
             if (e_issuer && t + 1 < ntiles && !issue_e(t + 1, warp)) note_timeout(abort_flag);
+            if (tid == U_TID && t + 1 < ntiles && !issue_u(t + 1)) note_timeout(abort_flag);
             if (tid == TMA_TID && t + NS < ntiles) issue_tma(t + NS);
             if (tid == OST_TID && t > 0) store_out(t - 1);
             // state checkpoint after this tile (off the chain's critical path)
@@ -816,7 +845,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     const bool z_tile = a.gate_mode != KDA_GATE_NONE && !a.gate_scalar;
     if (!make_map(&tq, a.q, a.H, a.T_total, D, false) || !make_map(&tk, a.k, a.H, a.T_total, D, false) ||
         !make_map(&tz, z_tile ? a.g : a.q, a.H, a.T_total, D, false) ||
-        !make_map(&tv, a.v, a.H, a.T_total, D, false) || !make_map(&to, a.out, a.H, a.T_total, D, false))
+        !make_map(&tv, a.v, a.H, a.T_total, D / 2, true) || !make_map(&to, a.out, a.H, a.T_total, D, false))
         return cudaErrorInvalidValue;
     const bool unbounded = a.gate_mode == KDA_GATE_LOG_DECAY || a.gate_mode == KDA_GATE_NEG_SOFTPLUS;
     auto kern = unbounded ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
