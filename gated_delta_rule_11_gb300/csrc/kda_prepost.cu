@@ -124,7 +124,7 @@ __device__ __forceinline__ void span_of(const PrepArgs &a, int n, int &bos, int 
 
 template <typename Tin, int D>
 constexpr int prep_smem_bytes() {
-    return (((kRun + kHalo) * D * static_cast<int>(sizeof(Tin)) + 15) & ~15) + 16;   // tile + mbarrier
+    return (((kRun + kHalo) * D * static_cast<int>(sizeof(Tin)) + 15) & ~15) + D * 16 + 16;   // tile + taps + mbarrier
 }
 
 // Eight consecutive channels as four (even, odd) f32x2 pairs: global and
@@ -176,8 +176,10 @@ template <> struct Oct<float> {
 // lanes owns a token (8 channels per lane), so a warp works on 32 * 8 / D
 // tokens at once; each group walks its own consecutive tokens with the three
 // previous inputs in registers.
+// Registers capped for 7 resident CTAs per SM (7 tiles in flight): with the
+// taps re-read from shared memory the cap costs a few spilled bytes.
 template <typename Tin, int D>
-__global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(const __grid_constant__ CUtensorMap tm_x,
+__global__ void __launch_bounds__(kPrepWarps * 32, 7) prep_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                                PrepArgs a) {
     using namespace sm100;
     constexpr int CPL = 8;                       // channels per lane
@@ -189,7 +191,8 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(const __grid_cons
     constexpr int TILE_BYTES = (kRun + kHalo) * D * static_cast<int>(sizeof(Tin));
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const Tin *tile = reinterpret_cast<const Tin *>(smem_raw);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem_raw + ((TILE_BYTES + 15) & ~15));
+    float *taps_t = reinterpret_cast<float *>(smem_raw + ((TILE_BYTES + 15) & ~15));   // [4][D]: tap-major
+    uint64_t *bar = reinterpret_cast<uint64_t *>(taps_t + 4 * D);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H;
@@ -241,14 +244,25 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(const __grid_cons
     const int slot = lane / LPT, sl = lane % LPT;
     // conv taps of this lane's channels as (even, odd) pairs: wt[tap][pair], tap 3 = current token
     const int c0 = sl * CPL;
-    f32x2 wt[4][4];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const float4 e = __ldg(reinterpret_cast<const float4 *>(a.conv_w) + static_cast<size_t>(mh) * D + c0 + 2 * p);
-        const float4 o = __ldg(reinterpret_cast<const float4 *>(a.conv_w) + static_cast<size_t>(mh) * D + c0 + 2 * p + 1);
-        wt[0][p] = pack2(e.x, o.x); wt[1][p] = pack2(e.y, o.y);
-        wt[2][p] = pack2(e.z, o.z); wt[3][p] = pack2(e.w, o.w);
+    // taps stored tap-major in shared memory, so one 16-byte load gives two (even, odd) channel pairs of
+    // a tap; they are re-read per token rather than held in 32 registers
+    if (tid < D) {
+        const float4 w = __ldg(reinterpret_cast<const float4 *>(a.conv_w) + static_cast<size_t>(mh) * D + tid);
+        taps_t[tid] = w.x; taps_t[D + tid] = w.y; taps_t[2 * D + tid] = w.z; taps_t[3 * D + tid] = w.w;
     }
+    __syncthreads();
+    auto load_taps = [&](f32x2 (&wt)[4][4]) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint64_t lo, hi;
+                asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(lo), "=l"(hi)
+                             : "r"(smem_u32(taps_t + k * D + c0 + 4 * h2)));
+                wt[k][2 * h2] = lo;
+                wt[k][2 * h2 + 1] = hi;
+            }
+    };
     const size_t col = static_cast<size_t>(mh) * D + c0;            // this lane's channels in a token of x
     Tin *dst = static_cast<Tin *>(m == 0 ? a.q : (m == 1 ? a.k : a.v)) + static_cast<size_t>(h) * D + c0;
     const size_t tok_o = static_cast<size_t>(H) * D;
@@ -298,6 +312,8 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(const __grid_cons
             } while (eos <= t && n + 1 < a.N);
             fill_window(t);
         }
+        f32x2 wt[4][4];
+        load_taps(wt);
         f32x2 xt[4], y[4], ss2 = 0ull;
         if (act) Oct<Tin>::ld_shared(row_ptr(t), xt);
         else
