@@ -20,8 +20,6 @@
 // of S, W, Q e^b, Vt, A, K e^{b_C-b} is bounded well inside fp16's range),
 // L and A come from tf32 mma.sync on fp32 operands (K e^-b reaches e^80, out
 // of fp16 range), and U, W, T, the gates and the state master are fp32.
-// U is a bf16 product: v is bf16 already, and T Diag(beta) (tf32-rounded,
-// 11 significant bits) is split exactly into bf16 hi + lo parts.
 //
 // Every tensor-core product is computed transposed so that its M side is a
 // 128-wide head dimension (tcgen05 M = 128, TMEM lane j = value channel j):
@@ -37,9 +35,6 @@
 //       -> E[:, 16:32] = O^T / scale
 //   (h) H[:, 0:128]  = Vt^T (K e^{b_C - b})              M128 N128 K16
 //       -> the state increment, transposed
-//   (u) U^T = V^T (T Diag(beta))^T, hi + lo               M128 N16  K16 (x2)
-//       -> read by the chain from TMEM (two slots, tile parity); V comes
-//          from TMA in the 128B-swizzled MN-major operand layout
 // E is double-buffered in TMEM (tile parity), so tile t's O is read out
 // while tile t+1's (g)/(h) run, off the serial path; full tiles of O are
 // staged in shared memory and written with one TMA store.
@@ -51,19 +46,17 @@
 //                          Vt^T = U^T + D[:,0:16] as the fp16 operand of
 //                          (g)/(h), store O, apply S = Diag(e^{b_C}) S +
 //                          increment and write the fp16 copy of S^T (into
-//                          TMEM) that the next tile's (e) reads.  Elected chain threads
-//                          issue the tcgen05 products ((u) for the next tile by
-//                          a thread idle while (e) runs) and commit them, and
+//                          TMEM) that the next tile's (e) reads.  One elected chain thread
+//                          issues the tcgen05 products and commits them, and
 //                          the TMA loads of the q, k, g_raw, v tiles (16
-//                          tokens each) into a 4-stage ring, refilling a
+//                          tokens each) into a 3-stage ring, refilling a
 //                          stage as soon as the chain has finished with it.
 //   warps 8-15 producer  : two warpgroups taking alternate tiles, each with
 //                          its own scratch; thread c owns key channel c: gate (eq. 5) and
 //                          in-tile decays as running products of the
 //                          retentions, decay-scaled operands, L and A (one
 //                          16x8 block per warp), the triangular solve
-//                          (first warp), W (tf32 mma.sync) and the bf16
-//                          hi/lo operand of (u).
+//                          (first warp), W and U (tf32 mma.sync).
 // The chain is serial per tile; the producer and TMA run up to 3 tiles ahead.
 // Tokens past a sequence's end are masked in the producer (k = q = 0, g = 0,
 // beta = 0), which makes U, W, A and the increment vanish for them.
@@ -383,16 +376,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (hh == 0) *reinterpret_cast<float2 *>(st + ST_GC + c0 * 4) = make_float2(gC[0], gC[1]);
             if (c < C) reinterpret_cast<float *>(st + ST_BETA)[c] = bt;
             const f32x2 igc = pack2(inv_gC[0], inv_gC[1]);
+            // 128B-swizzled offsets of this thread's rows: row 0's offset has
+            // zeros in bits 4-9, so row r's is it XOR (r << 7 | r << 4)
+            const uint32_t wq0 = off_kmajor_sw128(16 + 8 * hh, c0, 32);
+            const uint32_t kd0 = off_mnmajor_sw128(c0, 8 * hh, C);
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const int row = 8 * hh + r;
+                const uint32_t sw = static_cast<uint32_t>((r << 7) | (r << 4));
                 const float2 kg = unpack2(fmul2(kx[r], pre[r]));
                 const float2 qg = unpack2(fmul2(qx[r], pre[r]));
                 const f32x2 kd2 = fmul2(kx[r], suf[r]);
                 const float2 kd = unpack2(kd2);
                 const float2 ki = unpack2(fmul2(kd2, igc));
-                *reinterpret_cast<uint32_t *>(st + ST_WQ + off_kmajor_sw128(16 + row, c0, 32)) = pack_h2(qg.x, qg.y);
-                *reinterpret_cast<uint32_t *>(st + ST_KD + off_mnmajor_sw128(c0, row, C)) = pack_h2(kd.x, kd.y);
+                *reinterpret_cast<uint32_t *>(st + ST_WQ + (wq0 ^ sw)) = pack_h2(qg.x, qg.y);
+                *reinterpret_cast<uint32_t *>(st + ST_KD + (kd0 ^ sw)) = pack_h2(kd.x, kd.y);
                 *reinterpret_cast<float2 *>(qgm + row * PADF + c0) = make_float2(to_tf32(qg.x), to_tf32(qg.y));
                 *reinterpret_cast<float2 *>(kgm + row * PADF + c0) = make_float2(to_tf32(kg.x), to_tf32(kg.y));
                 *reinterpret_cast<float2 *>(kim + row * PADF + c0) = make_float2(to_tf32(ki.x), to_tf32(ki.y));
