@@ -685,8 +685,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const int nvv = min(C, eos - tt0);
             if (nvv == C) {
                 __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(ost + (tt & 1) * (C * D * 2));
+                const f32x2 sc = pack2(a.scale, a.scale);
 #pragma unroll
-                for (int r = 0; r < 8; ++r) stg[(8 * hf + r) * D + j] = __float2bfloat16_rn(a.scale * o[r]);
+                for (int r = 0; r < 8; r += 2) {
+                    const float2 y = unpack2(fmul2(pack2(o[r], o[r + 1]), sc));
+                    stg[(8 * hf + r) * D + j] = __float2bfloat16_rn(y.x);
+                    stg[(8 * hf + r + 1) * D + j] = __float2bfloat16_rn(y.y);
+                }
                 fence_proxy_async_smem();
             } else {
                 __nv_bfloat16 *op = gout + static_cast<size_t>(tt0 + 8 * hf) * a.H * D + static_cast<size_t>(h) * D + j;
@@ -770,7 +775,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             write_sT();
             tc_fence_before();
-            if (named_bar_or(2, NCHAIN, *abort_flag != 0)) break;   // uniform across the chain
+            named_bar_sync(2, NCHAIN);   // (the abort flag is polled once a tile, at the Vt barrier)
             // every read of this stage (TMA tiles, U, e^{b_C}, MMA operands) is done
             if (e_issuer && t + 1 < ntiles && !issue_e(t + 1, warp)) note_timeout(abort_flag);
             if (tid == U_TID && t + 1 < ntiles && !issue_u(t + 1)) note_timeout(abort_flag);
