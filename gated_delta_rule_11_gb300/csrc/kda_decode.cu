@@ -43,6 +43,13 @@ constexpr int kDecodeThreads = 256;
 constexpr int kTokBlock = 8;                         // tokens prepared per barrier
 
 __device__ __forceinline__ float4 ld_stream(const float4 *p) { return __ldcs(p); }
+// 16-byte global -> shared copy that holds no registers while in flight
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sm100::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
+}
 __device__ __forceinline__ void st_stream(float4 *p, float4 v) { __stcs(p, v); }
 
 // Single-token step with whole rows per warp (a warp instruction touches one
@@ -214,14 +221,53 @@ __global__ void __launch_bounds__(kDecodeThreads, 2 * CS) decode_kernel(DecodeAr
     Tin *go = static_cast<Tin *>(a.out);
 
     // Per-token vectors of tokens [i0, i0 + nb) (a warp's 32 channels share a token).
+    // bf16 drafts: the block's q, k, g_raw rows and v slab rows are copied into
+    // shared memory (over the reduction buffer, idle until the token loop) by
+    // 16-byte asynchronous copies, all in flight at once.
+    constexpr bool kStage = sizeof(Tin) == 2;
+    static_assert(!kStage || sizeof(sm.red) >= (3 * kTokBlock * DK + kTokBlock * DVS) * sizeof(Tin), "staging");
+    Tin *kin = reinterpret_cast<Tin *>(&sm.red[0][0][0]);
+    Tin *qin = kin + kTokBlock * DK, *zin = qin + kTokBlock * DK, *vin = zin + kTokBlock * DK;
+    auto stage = [&](int i0, int nb) {
+        constexpr int CH = DK * static_cast<int>(sizeof(Tin)) / 16;    // 16-byte chunks per channel row
+        constexpr int CV = DVS * static_cast<int>(sizeof(Tin)) / 16;   // per value-slab row
+        const int nz = (a.gate_mode != KDA_GATE_NONE && !a.gate_scalar) ? 1 : 0;
+        const int per_tok = CH * (2 + nz) + CV;
+        for (int idx = tid; idx < nb * per_tok; idx += kDecodeThreads) {
+            const int i = idx / per_tok, w = idx % per_tok;
+            const size_t tok = static_cast<size_t>(n) * a.K + i0 + i;
+            if (w < CH * (2 + nz)) {
+                const int m = w / CH, ch = w % CH;
+                const Tin *src = (m == 0 ? gk : (m == 1 ? gq : gz)) + tok * tok_k + static_cast<size_t>(h) * DK;
+                Tin *dst = (m == 0 ? kin : (m == 1 ? qin : zin)) + i * DK;
+                cp_async16(dst + ch * (16 / sizeof(Tin)), src + ch * (16 / sizeof(Tin)));
+            } else {
+                const int ch = w - CH * (2 + nz);
+                cp_async16(vin + i * DVS + ch * (16 / sizeof(Tin)),
+                           gv + tok * tok_v + static_cast<size_t>(h) * DV + slab * DVS + ch * (16 / sizeof(Tin)));
+            }
+        }
+        cp_async_wait_all();
+        __syncthreads();
+    };
     auto prepare = [&](int i0, int nb) {
 #pragma unroll 1
         for (int idx = tid; idx < nb * DK; idx += kDecodeThreads) {
             const int i = idx / DK, c = idx % DK;
             const size_t o = (static_cast<size_t>(n) * a.K + i0 + i) * tok_k + static_cast<size_t>(h) * DK + c;
-            const float kc = ld_in(gk + o), qc = ld_in(gq + o);
-            const size_t og = a.gate_scalar ? (static_cast<size_t>(n) * a.K + i0 + i) * a.H + h : o;
-            const float zc = a.gate_mode == KDA_GATE_NONE ? 0.f : ld_in(gz + og);
+            float kc, qc, zc;
+            if constexpr (kStage) {
+                kc = __bfloat162float(kin[i * DK + c]);
+                qc = __bfloat162float(qin[i * DK + c]);
+                zc = a.gate_mode == KDA_GATE_NONE ? 0.f
+                     : a.gate_scalar ? ld_in(gz + (static_cast<size_t>(n) * a.K + i0 + i) * a.H + h)
+                                     : __bfloat162float(zin[i * DK + c]);
+            } else {
+                kc = ld_in(gk + o);
+                qc = ld_in(gq + o);
+                const size_t og = a.gate_scalar ? (static_cast<size_t>(n) * a.K + i0 + i) * a.H + h : o;
+                zc = a.gate_mode == KDA_GATE_NONE ? 0.f : ld_in(gz + og);
+            }
             const float alpha = expf(gate_log_decay(a.gate_mode, zc, escale, a.g_min));
             sm.akq[i][c] = make_ulonglong2(pack2(alpha * kc, alpha * kc), pack2(alpha * qc, alpha * qc));
             sm.alk[i][c] = make_ulonglong2(pack2(alpha, alpha), pack2(kc, kc));
@@ -230,14 +276,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 2 * CS) decode_kernel(DecodeAr
             for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
             if (lane == 0) sm.kq[i][c / 32] = kq;
         }
-        for (int idx = tid; idx < nb * DVS; idx += kDecodeThreads)
-            sm.v[idx / DVS][idx % DVS] =
-                ld_in(gv + (static_cast<size_t>(n) * a.K + i0 + idx / DVS) * tok_v + static_cast<size_t>(h) * DV +
-                      slab * DVS + idx % DVS);
+        for (int idx = tid; idx < nb * DVS; idx += kDecodeThreads) {
+            if constexpr (kStage) {
+                sm.v[idx / DVS][idx % DVS] = __bfloat162float(vin[idx]);
+            } else {
+                sm.v[idx / DVS][idx % DVS] =
+                    ld_in(gv + (static_cast<size_t>(n) * a.K + i0 + idx / DVS) * tok_v + static_cast<size_t>(h) * DV +
+                          slab * DVS + idx % DVS);
+            }
+        }
         if (tid < nb) sm.beta[tid] = ld_in(gb + (static_cast<size_t>(n) * a.K + i0 + tid) * a.H + h);
     };
     // The first block is prepared for every drafted token, before the accepted
     // count is used, so its loads overlap the state's.
+    if constexpr (kStage) stage(0, min(kTokBlock, a.K));
     prepare(0, min(kTokBlock, a.K));
     __syncthreads();
     const int n_acc = min(max(acc_raw, 0), a.K);
@@ -248,6 +300,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2 * CS) decode_kernel(DecodeAr
         const int nb = min(kTokBlock, n_acc - i0);
         if (i0 > 0) {
             __syncthreads();                         // previous block's vectors are consumed
+            if constexpr (kStage) stage(i0, nb);
             prepare(i0, nb);
             __syncthreads();
         }
