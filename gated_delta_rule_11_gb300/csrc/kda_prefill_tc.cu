@@ -20,6 +20,8 @@
 // of S, W, Q e^b, Vt, A, K e^{b_C-b} is bounded well inside fp16's range),
 // L and A come from tf32 mma.sync on fp32 operands (K e^-b reaches e^80, out
 // of fp16 range), and U, W, T, the gates and the state master are fp32.
+// U is a bf16 product: v is bf16 already, and T Diag(beta) (tf32-rounded,
+// 11 significant bits) is split exactly into bf16 hi + lo parts.
 //
 // Every tensor-core product is computed transposed so that its M side is a
 // 128-wide head dimension (tcgen05 M = 128, TMEM lane j = value channel j):
@@ -35,6 +37,9 @@
 //       -> E[:, 16:32] = O^T / scale
 //   (h) H[:, 0:128]  = Vt^T (K e^{b_C - b})              M128 N128 K16
 //       -> the state increment, transposed
+//   (u) U^T = V^T (T Diag(beta))^T, hi + lo               M128 N16  K16 (x2)
+//       -> read by the chain from TMEM (two slots, tile parity); V comes
+//          from TMA in the 128B-swizzled MN-major operand layout
 // E is double-buffered in TMEM (tile parity), so tile t's O is read out
 // while tile t+1's (g)/(h) run, off the serial path; full tiles of O are
 // staged in shared memory and written with one TMA store.
@@ -46,17 +51,19 @@
 //                          Vt^T = U^T + D[:,0:16] as the fp16 operand of
 //                          (g)/(h), store O, apply S = Diag(e^{b_C}) S +
 //                          increment and write the fp16 copy of S^T (into
-//                          TMEM) that the next tile's (e) reads.  One elected chain thread
-//                          issues the tcgen05 products and commits them, and
+//                          TMEM) that the next tile's (e) reads.  Elected chain threads
+//                          issue the tcgen05 products ((u) for the next tile by
+//                          a thread idle while (e) runs) and commit them, and
 //                          the TMA loads of the q, k, g_raw, v tiles (16
-//                          tokens each) into a 3-stage ring, refilling a
+//                          tokens each) into a 4-stage ring, refilling a
 //                          stage as soon as the chain has finished with it.
 //   warps 8-15 producer  : two warpgroups taking alternate tiles, each with
 //                          its own scratch; thread c owns key channel c: gate (eq. 5) and
 //                          in-tile decays as running products of the
 //                          retentions, decay-scaled operands, L and A (one
 //                          16x8 block per warp), the triangular solve
-//                          (first warp), W and U (tf32 mma.sync).
+//                          (first warp), W (tf32 mma.sync) and the bf16
+//                          hi/lo operand of (u).
 // The chain is serial per tile; the producer and TMA run up to 3 tiles ahead.
 // Tokens past a sequence's end are masked in the producer (k = q = 0, g = 0,
 // beta = 0), which makes U, W, A and the increment vanish for them.
