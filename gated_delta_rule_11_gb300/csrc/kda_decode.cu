@@ -21,13 +21,15 @@
 // so both reductions happen in a single pass over the state.  alpha follows
 // eq. (5) of §下界 log-decay 是一个 kernel 设计.
 //
-// Layout of the work: 256 threads = 8 warps; warp w owns the column slab
-// [w dv/8, (w+1) dv/8) of every row, as CG = dv/32 float4 column groups x
-// RG = 32/CG row groups (lane = rg * CG + cg; rows rg + m RG).  Both
-// reductions over c then stay inside the warp (shuffles), so applying a token
-// needs no block barrier.  The per-token channel vectors (alpha k, alpha q)
-// and (alpha, k), v, beta and k.q are computed for a block of up to 8 tokens at
-// once into shared memory, with their loads in flight beside the state's.
+// Two kernels, both with the state in registers as float4 column groups of
+// whole rows (256 threads): decode1_kernel, the single-token step over all
+// dv columns, combining the two reductions over c across warps through
+// shared memory; decode_kernel, the multi-token replay, over one dv/CS-column
+// slab per CTA with one cross-warp reduction per token.  The replay's
+// per-token channel vectors (alpha k, alpha q) and (alpha, k), v, beta and
+// k.q are computed for a block of up to 8 tokens at once into shared memory,
+// with their loads in flight beside the state's (bf16 drafts are first
+// staged into shared memory by cp.async).
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
 
@@ -220,7 +222,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2 * CS) decode_kernel(DecodeAr
     const Tin *gb = static_cast<const Tin *>(a.beta);
     Tin *go = static_cast<Tin *>(a.out);
 
-    // Per-token vectors of tokens [i0, i0 + nb) (a warp's 32 channels share a token).
     // bf16 drafts: the block's q, k, g_raw rows and v slab rows are copied into
     // shared memory (over the reduction buffer, idle until the token loop) by
     // 16-byte asynchronous copies, all in flight at once.
@@ -250,11 +251,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 2 * CS) decode_kernel(DecodeAr
         cp_async_wait_all();
         __syncthreads();
     };
+    // Per-token vectors of tokens [i0, i0 + nb) (a warp's 32 channels share a token).
     auto prepare = [&](int i0, int nb) {
 #pragma unroll 1
         for (int idx = tid; idx < nb * DK; idx += kDecodeThreads) {
             const int i = idx / DK, c = idx % DK;
-            const size_t o = (static_cast<size_t>(n) * a.K + i0 + i) * tok_k + static_cast<size_t>(h) * DK + c;
             float kc, qc, zc;
             if constexpr (kStage) {
                 kc = __bfloat162float(kin[i * DK + c]);
@@ -263,6 +264,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2 * CS) decode_kernel(DecodeAr
                      : a.gate_scalar ? ld_in(gz + (static_cast<size_t>(n) * a.K + i0 + i) * a.H + h)
                                      : __bfloat162float(zin[i * DK + c]);
             } else {
+                const size_t o = (static_cast<size_t>(n) * a.K + i0 + i) * tok_k + static_cast<size_t>(h) * DK + c;
                 kc = ld_in(gk + o);
                 qc = ld_in(gq + o);
                 const size_t og = a.gate_scalar ? (static_cast<size_t>(n) * a.K + i0 + i) * a.H + h : o;
