@@ -52,7 +52,10 @@ def _applied_rows(out, acc):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("dk,dv,K", [(32, 32, 3), (64, 128, 5), (128, 64, 2), (128, 128, 8),
-                                     (32, 128, 4), (128, 128, 1)])
+                                     (32, 128, 4), (128, 128, 1),
+                                     # more drafts than one 8-token block: later blocks
+                                     # are prepared after the first one's tokens
+                                     (128, 128, 12), (64, 64, 17)])
 def test_small_replay_matches_oracle(dtype, dk, dv, K):
     w = _w(dtype, 3, dk, dv, N=6, K=K, seed=dk + dv + K)
     S = inputs.make_decode_state(w, device="cuda")
