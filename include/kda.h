@@ -124,9 +124,11 @@ typedef struct {
  *   out    [B, T, H, dv]   o_t for every token (dtype dt); required if B*T > 0.
  *   final_state [N, H, dk, dv] fp32, or NULL: the state after each
  *          sequence's last token.
- * Numerics: fp32 state and accumulation.  The bf16 path feeds bf16
- * operands (inputs and a bf16 copy of the state) to the tensor cores; the
- * fp32 path computes in fp32 throughout.
+ * Numerics: fp32 state, gates and accumulation.  On the bf16 path the
+ * tensor-core operands are fp16 (an fp16 copy of the state, the residual and
+ * the decay-scaled q, k; all bounded well inside fp16's range), tf32 for the
+ * in-tile products whose factors span e^{+-80}, and exact bf16 parts for
+ * T Diag(beta) V; the fp32 path computes in fp32 throughout.
  */
 kda_status kda_chunk_fwd(kda_dtype dt, int B, int T, int H, int dk, int dv,
                          const void *q, const void *k, const void *v,
