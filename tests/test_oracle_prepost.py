@@ -106,3 +106,98 @@ def test_output_gate_closed_forms():
     wgt = rng.uniform(0.5, 2.0, 16)
     yw = prepost.output_gate(o, np.full_like(o, 60.0), wgt, eps=1e-5)
     np.testing.assert_allclose(yw, y * wgt, rtol=1e-12)
+
+
+# ----------------------------------------------------------------- planted mistakes
+
+def _prep_mutant(kind):
+    """Plausible wrong restatements of eq. (2)'s tail, to show the pins above
+    catch them (same signature as prepost.qkv_prep)."""
+    def qkv_prep(x_qkv, conv_w, beta_logit=None, cu_seqlens=None, conv_state_in=None, l2_eps=1e-6):
+        x = prepost._f64(x_qkv)
+        w = prepost._f64(conv_w)
+        B, T, _, H, d = x.shape
+        flat = x.reshape(B * T, 3, H, d)
+        cu = np.arange(B + 1) * T if cu_seqlens is None else np.asarray(prepost._f64(cu_seqlens), dtype=np.int64)
+        N = len(cu) - 1
+        st_in = np.zeros((N, 3, 3, H, d)) if conv_state_in is None else prepost._f64(conv_state_in)
+        y = np.zeros((B * T, 3, H, d))
+        st_out = np.zeros((N, 3, 3, H, d))
+        carry = None
+        for n in range(N):
+            bos, eos = int(cu[n]), int(cu[n + 1])
+            hist = [st_in[n, j] for j in range(3)]
+            if kind == "history_across_sequences" and carry is not None:
+                hist = carry
+            for t in range(bos, eos):
+                window = hist[-3:] + [flat[t]]
+                if kind == "taps_reversed":
+                    window = window[::-1]
+                acc = sum(w[..., i] * window[i] for i in range(4))
+                y[t] = acc if kind == "no_swish" else prepost.swish(acc)
+                hist = hist + [flat[t]]
+            carry = hist
+            for j in range(3):
+                st_out[n, j] = hist[-1 - j] if kind == "state_newest_first" else hist[-3 + j]
+        y = y.reshape(B, T, 3, H, d)
+        q, k, v = y[:, :, 0], y[:, :, 1], y[:, :, 2]
+        axis = -2 if kind == "norm_over_heads" else -1
+        q = q / np.sqrt((q * q).sum(axis, keepdims=True) + l2_eps)
+        k = k / np.sqrt((k * k).sum(axis, keepdims=True) + l2_eps)
+        if kind == "norm_v":
+            v = v / np.sqrt((v * v).sum(-1, keepdims=True) + l2_eps)
+        beta = None if beta_logit is None else prepost.sigmoid(prepost._f64(beta_logit))
+        return q, k, v, beta, st_out
+    return qkv_prep
+
+
+def _gate_mutant(kind):
+    def output_gate(o, gate, norm_w=None, eps=1e-5):
+        o = prepost._f64(o)
+        g = prepost._f64(gate)
+        w = np.ones(o.shape[-1]) if norm_w is None else prepost._f64(norm_w)
+        if kind == "mean_not_rms":
+            den = np.abs(o.mean(-1, keepdims=True)) + eps
+        else:
+            den = np.sqrt((o * o).mean(-1, keepdims=True) + eps)
+        act = prepost.swish(g) if kind == "swish_gate" else prepost.sigmoid(g)
+        return act * (o / den * w)
+    return output_gate
+
+
+def _prep_pins_pass():
+    try:
+        test_short_conv_is_causal_convolution()
+        test_identity_taps_and_l2_norm()
+        for cut in (0, 1, 2, 3, 10, 22):
+            test_conv_state_split_invariant(cut)
+        test_conv_state_out_holds_last_three_rows()
+        test_varlen_sequences_are_convolved_separately()
+    except AssertionError:
+        return False
+    return True
+
+
+@pytest.mark.parametrize("kind", ["taps_reversed", "no_swish", "norm_over_heads", "norm_v",
+                                  "state_newest_first", "history_across_sequences"])
+def test_prep_pins_catch_planted_mistakes(kind, monkeypatch):
+    """Every mutant of the prep oracle fails at least one pin above, while the
+    oracle itself passes them all."""
+    assert _prep_pins_pass()
+    monkeypatch.setattr(prepost, "qkv_prep", _prep_mutant(kind))
+    assert not _prep_pins_pass()
+
+
+def test_prep_mutant_without_mistake_passes(monkeypatch):
+    """The mutant factory with no planted mistake is the oracle again (so the
+    failures above come from the planted mistakes alone)."""
+    monkeypatch.setattr(prepost, "qkv_prep", _prep_mutant("none"))
+    assert _prep_pins_pass()
+
+
+@pytest.mark.parametrize("kind", ["mean_not_rms", "swish_gate"])
+def test_gate_pins_catch_planted_mistakes(kind, monkeypatch):
+    test_output_gate_closed_forms()
+    monkeypatch.setattr(prepost, "output_gate", _gate_mutant(kind))
+    with pytest.raises(AssertionError):
+        test_output_gate_closed_forms()
