@@ -2,9 +2,11 @@
 //
 // This kernel serves the fp32 path (whose tolerance the tensor cores' bf16
 // and tf32 operands cannot meet) and every head-dimension combination.  One
-// CTA owns one (sequence, head) chain and one 32-column slab of the value
+// CTA owns one (sequence, head) chain and one dv/4-column slab of the value
 // dimension: the value columns of the state never interact, so slabs are
-// independent (the key-side work of a tile is recomputed per slab).
+// independent (the key-side work of a tile is recomputed per slab), and
+// four CTAs per chain keep several chains' latency-bound tiles in flight
+// per SM at every head size.
 //
 // Per 16-token tile (the tile of "Kimi K3：从三条信息流到完整系统",
 // §下界 log-decay 是一个 kernel 设计, whose bound -80 < sum g < 0 keeps
@@ -37,11 +39,8 @@ namespace {
 
 constexpr int C = 16;      // tile length (tokens)
 constexpr int NT = 128;    // threads per CTA
-constexpr int BV = 32;     // value columns per CTA
-constexpr int NW = NT / 32;
-constexpr int RPT = C / NW;  // tile rows per thread in the value-side products
 
-template <int DK>
+template <int DK, int BV>
 struct SimtSmem {
     float kg[C][DK], kinv[C][DK], qg[C][DK], kdec[C][DK], W[C][DK];
     float S[DK][BV];
@@ -56,14 +55,20 @@ struct SimtPairSmem {
     float k[C][DK], q[C][DK], b[C][DK];
 };
 
-template <typename Tin, int DK, int DV>
+// BV value columns per CTA (a quarter of dv, so every head size has four
+// slabs per chain); value-side thread (j, rg): column j = tid % BV of row
+// group rg = tid / BV, tile rows rg + m * RG.
+template <typename Tin, int DK, int DV, int BV>
 __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
+    constexpr int RG = NT / BV;        // row groups
+    constexpr int RPT = C / RG;        // tile rows per thread in the value-side products
+    static_assert(NT % BV == 0 && C % RG == 0 && DK % RG == 0, "value-side tiling");
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    SimtSmem<DK> &sm = *reinterpret_cast<SimtSmem<DK> *>(smem_raw);
-    SimtPairSmem<DK> &pp = *reinterpret_cast<SimtPairSmem<DK> *>(smem_raw + sizeof(SimtSmem<DK>));
+    SimtSmem<DK, BV> &sm = *reinterpret_cast<SimtSmem<DK, BV> *>(smem_raw);
+    SimtPairSmem<DK> &pp = *reinterpret_cast<SimtPairSmem<DK> *>(smem_raw + sizeof(SimtSmem<DK, BV>));
     const bool pairs = a.gate_mode == KDA_GATE_LOG_DECAY || a.gate_mode == KDA_GATE_NEG_SOFTPLUS;
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31;
     const int chain = blockIdx.x;             // n * H + h
     const int n = chain / a.H, h = chain % a.H;
     const int j0 = blockIdx.y * BV;
@@ -201,7 +206,7 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
         __syncthreads();
 
         // Vt = U - W S_0 and the inter-tile output (Q*e^b) S_0.
-        const int j = lane;
+        const int j = tid % BV, rg = tid / BV;
         float accw[RPT], accq[RPT];
 #pragma unroll
         for (int m = 0; m < RPT; ++m) accw[m] = accq[m] = 0.f;
@@ -209,14 +214,14 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
             const float s = sm.S[c][j];
 #pragma unroll
             for (int m = 0; m < RPT; ++m) {
-                const int r = warp + m * NW;
+                const int r = rg + m * RG;
                 accw[m] += sm.W[r][c] * s;
                 accq[m] += sm.qg[r][c] * s;
             }
         }
 #pragma unroll
         for (int m = 0; m < RPT; ++m) {
-            const int r = warp + m * NW;
+            const int r = rg + m * RG;
             sm.Vt[r][j] = sm.U[r][j] - accw[m];
         }
         __syncthreads();
@@ -224,7 +229,7 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
         // Intra-tile output and the state update.
 #pragma unroll
         for (int m = 0; m < RPT; ++m) {
-            const int r = warp + m * NW;
+            const int r = rg + m * RG;
             float o = accq[m];
             for (int i = 0; i <= r; ++i) o += sm.A[r][i] * sm.Vt[i][j];
             if (r < nv) st_out(go + (t0 + r) * tok_v + h * DV + j0 + j, a.scale * o);
@@ -232,7 +237,7 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
         float vt[C];
 #pragma unroll
         for (int r = 0; r < C; ++r) vt[r] = sm.Vt[r][j];
-        for (int c = warp; c < DK; c += NW) {
+        for (int c = rg; c < DK; c += RG) {
             float acc = sm.ebC[c] * sm.S[c][j];
 #pragma unroll
             for (int r = 0; r < C; ++r) acc += sm.kdec[r][c] * vt[r];
@@ -257,11 +262,12 @@ __global__ void __launch_bounds__(NT) prefill_simt_kernel(PrefillArgs a) {
 
 template <typename Tin, int DK, int DV>
 cudaError_t launch_one(const PrefillArgs &a, cudaStream_t s) {
+    constexpr int BV = DV / 4;         // four value slabs per chain at every head size
     const bool pairs = a.gate_mode == KDA_GATE_LOG_DECAY || a.gate_mode == KDA_GATE_NEG_SOFTPLUS;
-    const size_t smem = sizeof(SimtSmem<DK>) + (pairs ? sizeof(SimtPairSmem<DK>) : 0);
-    auto kern = prefill_simt_kernel<Tin, DK, DV>;
+    const size_t smem = sizeof(SimtSmem<DK, BV>) + (pairs ? sizeof(SimtPairSmem<DK>) : 0);
+    auto kern = prefill_simt_kernel<Tin, DK, DV, BV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(sizeof(SimtSmem<DK>) + sizeof(SimtPairSmem<DK>)));
+                                         static_cast<int>(sizeof(SimtSmem<DK, BV>) + sizeof(SimtPairSmem<DK>)));
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(a.N) * static_cast<unsigned>(a.H), DV / BV);
     kern<<<grid, NT, smem, s>>>(a);
