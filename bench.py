@@ -423,12 +423,7 @@ def run_ours(args, rank, world, local):
 
     e2e = None
     if not args.no_e2e:   # every rank: the timing is reduced over ranks
-        try:
-            e2e = run_e2e(kda, q, k, v, g, b, cu, out, fin, args.e2e_steps, world, T_total)
-        except RuntimeError as exc:   # e.g. the host cannot pin every rank's input set
-            torch.cuda.synchronize()
-            torch.cuda.empty_cache()
-            e2e = {"unavailable": f"end-to-end leg failed on this host: {str(exc).splitlines()[0][:200]}"}
+        e2e = run_e2e(kda, q, k, v, g, b, cu, out, fin, args.e2e_steps, world, T_total)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -593,11 +588,23 @@ def run_e2e(kda, q, k, v, g, b, cu, out, fin, steps, world, T_total):
         h.copy_(t)
         return h
 
-    hin = [pinned_copy(t) for t in (q, k, v, g, b)]
-    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    hfin = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
-    din = [[q, k, v, g, b], [torch.empty_like(t) for t in (q, k, v, g, b)]]
-    dout = [[out, fin], [torch.empty_like(out), torch.empty_like(fin)]]
+    # Allocate first, then agree over the ranks: a host that cannot pin every
+    # rank's buffers (or a device out of memory) skips the leg on all ranks
+    # alike, so no rank waits in a collective that another never reaches.
+    failure = None
+    try:
+        hin = [pinned_copy(t) for t in (q, k, v, g, b)]
+        hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        hfin = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+        din = [[q, k, v, g, b], [torch.empty_like(t) for t in (q, k, v, g, b)]]
+        dout = [[out, fin], [torch.empty_like(out), torch.empty_like(fin)]]
+    except RuntimeError as exc:
+        failure = str(exc).splitlines()[0][:200]
+    if reduce_max(1.0 if failure else 0.0, world) > 0.0:
+        hin = hout = hfin = din = dout = None
+        torch.cuda.empty_cache()
+        return {"unavailable": "end-to-end buffers could not be allocated on "
+                               + ("this rank: " + failure if failure else "another rank")}
     up, comp, down = torch.cuda.Stream(), torch.cuda.current_stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()
     uploaded, computed, downloaded = [ev(), ev()], [ev(), ev()], [ev(), ev()]
