@@ -289,13 +289,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 2 * CS) decode_kernel(DecodeAr
         }
         if (tid < nb) sm.beta[tid] = ld_in(gb + (static_cast<size_t>(n) * a.K + i0 + tid) * a.H + h);
     };
-    // The first block's drafts are staged for every drafted token, before the
-    // accepted count is used, so their loads overlap the state's; the vectors
-    // are then prepared for the accepted tokens only.
+    // The accepted count is read first; the first block's accepted drafts are
+    // staged while the state's loads are in flight, and the vectors are
+    // prepared for the accepted tokens only.
     const int n_acc = min(max(acc_raw, 0), a.K);
     if constexpr (kStage) {
-        stage(0, min(kTokBlock, a.K));
         if (n_acc == 0) return;                      // state and outputs untouched
+        stage(0, min(kTokBlock, n_acc));
         prepare(0, min(kTokBlock, n_acc));
     } else {
         prepare(0, min(kTokBlock, a.K));
