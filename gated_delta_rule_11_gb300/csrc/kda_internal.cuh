@@ -62,12 +62,6 @@ __device__ __forceinline__ float log_decay(float z, float escale, float g_min) {
     return g_min / (1.0f + expf(-escale * z));
 }
 
-// The same gate with hardware exponential and reciprocal (relative error
-// ~1e-6, far below the tensor-core paths' operand rounding).
-__device__ __forceinline__ float log_decay_fast(float z, float escale, float g_min) {
-    return g_min * __frcp_rn(1.0f + __expf(-escale * z));
-}
-
 // Pre/post passes.  prep: x [T, 3, H, d] (q | k | v projections), conv_w
 // [3, H, d, 4] fp32, beta_logit [T, H], conv states [N, 3, 3, H, d] (the
 // last three tokens' x, oldest first); outputs q, k, v [T, H, d], beta
