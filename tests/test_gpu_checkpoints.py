@@ -62,6 +62,9 @@ CASES = [
     ("f32", 2, 64, 128, 1, 0, (40, 96, 15), 32),
     ("f32", 1, 32, 32, 3, 70, (), 16),
     ("bf16", 2, 64, 64, 1, 0, (80, 17), 16),
+    # more sequences than a warp: each chain's first checkpoint row is a
+    # warp-strided count over all the sequences before it
+    ("bf16", 2, 128, 128, 1, 0, tuple((16, 0, 40, 5, 33)[i % 5] for i in range(70)), 16),
 ]
 
 

@@ -63,6 +63,15 @@ def test_small_cases(dtype, H, dk, dv, B, T, seqlens):
     _run_and_compare(_w(dtype, H, dk, dv, B=B, T=T, seqlens=seqlens, seed=H * 7 + dk + T))
 
 
+@pytest.mark.parametrize("dtype,dk", [("bf16", 128), ("f32", 64)])
+def test_many_short_sequences(dtype, dk):
+    """Two hundred packed sequences, many empty or shorter than a tile: every
+    chain's span, the partial last tiles and the states all match."""
+    rng = np.random.default_rng(31)
+    seqlens = tuple(int(x) for x in rng.choice([0, 1, 5, 15, 16, 17, 33], size=200))
+    _run_and_compare(_w(dtype, 2, dk, dk, seqlens=seqlens, seed=31))
+
+
 def test_zero_initial_state_and_scale_and_head_log_scale():
     w = _w("bf16", 3, 128, 128, B=2, T=80, s0_std=0.0, seed=5)
     A_log = torch.tensor([0.0, 0.5, -0.7], device="cuda")
