@@ -97,6 +97,12 @@ kda_status kda_check_device_status(void) {
     return waits ? KDA_ERR_TIMEOUT : KDA_OK;
 }
 
+kda_status kda_selftest_bounded_wait(int limit_us, kda_stream_t stream) {
+    if (limit_us < 1 || limit_us > 100000) return KDA_ERR_ARG;
+    return from_cuda(kda::launch_wait_selftest(static_cast<uint64_t>(limit_us) * 1000u,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
 long long kda_checkpoint_rows(int B, int T, const int32_t *cu_seqlens_host, int N,
                               int checkpoint_every) {
     if (checkpoint_every <= 0 || checkpoint_every % 16 != 0 || B < 0 || T < 0 || N < 0) return -1;

@@ -155,5 +155,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 // Number of bounded device waits that gave up since the last call (syncs the device).
 unsigned int take_tc_timeouts();
 unsigned int take_prep_timeouts();
+// Test hook: one kernel whose bounded wait on a never-arriving barrier gives up.
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace kda

@@ -117,7 +117,7 @@ constexpr int SC_T00 = SC_T11 + 64 * 4;           //   fp32 [8][8]: upper-left b
 constexpr int SC_Y = SC_T00 + 64 * 4;             //   fp32 [8][8]: Diag(beta) L10 T00
 constexpr int SCR_BYTES = (SC_Y + 64 * 4 + 127) & ~127;
 constexpr int OFF_BAR = (OFF_SCR + NPROD * SCR_BYTES + 63) & ~63;
-enum { B_RAW = 0, B_FULL = NS, B_VT = 2 * NS, B_UPD, NUM_BARS };
+enum { B_RAW = 0, B_FULL = NS, B_VT = 2 * NS, B_UPD, B_DRAIN, NUM_BARS };
 constexpr int NACC = 4;          // independent accumulators of (e)
 constexpr uint32_t TM_E = 0;     // two E buffers of NACC x 32 columns
 constexpr uint32_t TM_H = 256;   // 128-column H
@@ -231,6 +231,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         mbar_init(&bars[B_VT], NACC + 1); // one commit per (e) issuer and the U^T issuer
         mbar_init(&bars[B_UPD], 2);       // commits of the (g) and (h) issuers
+        mbar_init(&bars[B_DRAIN], 5);     // abort only: one commit per MMA-issuing thread
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -612,8 +613,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tma_load_3d(stg + ST_V + 2048, &tm_v, &bars[B_RAW + ss], 64, h, tok);  // channels 64-127
         };
         constexpr int TMA_TID = 160, OST_TID = 192;  // lane 0 of chain warps 5 and 6
+        int tma_next = 0;                            // (TMA thread) next tile to load
         if (tid == TMA_TID)
-            for (int tt = 0; tt < NS && tt < ntiles; ++tt) issue_tma(tt);
+            for (; tma_next < NS && tma_next < ntiles; ++tma_next) issue_tma(tma_next);
         // (e) for tile tt: issuer p (lane 0 of chain warp p) issues the K slices
         // p and p + 4 into accumulator p once the tile's operands are ready.
         auto issue_e = [&](int tt, int p) -> bool {
@@ -786,7 +788,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             // every read of this stage (TMA tiles, U, e^{b_C}, MMA operands) is done
             if (e_issuer && t + 1 < ntiles && !issue_e(t + 1, warp)) note_timeout(abort_flag);
             if (tid == U_TID && t + 1 < ntiles && !issue_u(t + 1)) note_timeout(abort_flag);
-            if (tid == TMA_TID && t + NS < ntiles) issue_tma(t + NS);
+            if (tid == TMA_TID && t + NS < ntiles) issue_tma(tma_next++);
             if (tid == OST_TID && t > 0) store_out(t - 1);
             // state checkpoint after this tile (off the chain's critical path)
             if (float *cp = ckpt_slot(a, ck_row0, min((t + 1) * C, eos - bos), h, D * D)) {
@@ -802,6 +804,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (tid == OST_TID) store_out(ntiles - 1);
         }
         if (tid == OST_TID) bulk_wait_all();
+        if (aborted) {
+            // A wait gave up: before the CTA frees its tensor memory and exits,
+            // let the asynchronous work it started finish (bounded waits).
+            //  - TMA loads: the last tile issued into each ring stage.
+            //  - tcgen05 products: every MMA-issuing thread (lane 0 of chain
+            //    warps 0-3: (e), (g), (h); lane 0 of warp 7: U) commits once
+            //    more; the commit arrives when all its earlier products are done.
+            if (tid == TMA_TID)
+                for (int tt = max(0, tma_next - NS); tt < tma_next; ++tt)
+                    mbar_wait(&bars[B_RAW + tt % NS], (tt / NS) & 1, kWaitLimitNs);
+            if (lane == 0 && (warp < NACC || tid == U_TID)) {
+                mma_commit(&bars[B_DRAIN]);
+                mbar_wait(&bars[B_DRAIN], 0, kWaitLimitNs);
+            }
+        }
         if (a.final_state && !aborted) {
 #pragma unroll
             for (int cc = 0; cc < HR; ++cc)
@@ -864,6 +881,26 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>(a.N) * static_cast<unsigned>(a.H));
     kern<<<grid, NTHREADS, SMEM_BYTES, s>>>(tq, tk, tz, tv, to, a);
     e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
+
+namespace {
+// One thread waits on a barrier nothing arrives at; the bounded wait gives
+// up after limit_ns and records the timeout like a real stalled launch.
+__global__ void __launch_bounds__(32) wait_selftest_kernel(uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        sm100::mbar_init(&bar, 1);
+        sm100::fence_mbar_init();
+        if (!sm100::mbar_wait(&bar, 0, limit_ns)) atomicAdd(&g_tc_timeouts, 1u);
+    }
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s) {
+    wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns);
+    const cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;
 }

@@ -280,6 +280,9 @@ __global__ void __launch_bounds__(kPrepWarps * 32, 7) prep_kernel(const __grid_c
     // warp-uniform: every lane of a warp takes part in the group reductions below
     if (!__all_sync(0xffffffffu, mbar_wait(bar, 0, kPrepWaitNs))) {
         if (lane == 0) atomicAdd(&g_prep_timeouts, 1u);
+        // the tile copy may still be in flight into this CTA's shared memory:
+        // give it one more bounded wait before the CTA exits
+        mbar_wait(bar, 0, kPrepWaitNs);
         return;
     }
     auto row_ptr = [&](int t) { return tile + static_cast<size_t>(t - t_begin + kHalo) * D + c0; };

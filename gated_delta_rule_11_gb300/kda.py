@@ -27,7 +27,7 @@ _lock = threading.Lock()
 EXPORTED = ("kda_chunk_fwd", "kda_decode_step", "kda_status_str", "kda_last_cuda_error",
             "kda_version", "kda_launch_count", "kda_check_device_status", "kda_chunk_fwd_kernel",
             "kda_decode_steps", "kda_chunk_fwd_checkpointed", "kda_checkpoint_rows",
-            "kda_qkv_prep", "kda_output_gate")
+            "kda_qkv_prep", "kda_output_gate", "kda_selftest_bounded_wait")
 
 
 class KdaError(RuntimeError):
@@ -95,6 +95,8 @@ def load_library(build_if_missing: bool = False):
         lib.kda_launch_count.argtypes = []
         lib.kda_check_device_status.restype = i
         lib.kda_check_device_status.argtypes = []
+        lib.kda_selftest_bounded_wait.restype = i
+        lib.kda_selftest_bounded_wait.argtypes = [i, vp]
         lib.kda_chunk_fwd_kernel.restype = ctypes.c_char_p
         lib.kda_chunk_fwd_kernel.argtypes = [i, i, i]
         _lib = lib
@@ -119,6 +121,16 @@ def check_device_status() -> None:
     st = lib.kda_check_device_status()
     if st != 0:
         _raise(lib, "kda_check_device_status", st)
+
+
+def selftest_bounded_wait(limit_us: int = 1000, stream=None) -> None:
+    """Enqueue the library's test kernel whose bounded wait gives up after
+    ``limit_us``; the next check_device_status() then raises KDA_ERR_TIMEOUT."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st = lib.kda_selftest_bounded_wait(int(limit_us), _stream_handle(dev, stream))
+    if st != 0:
+        _raise(lib, "kda_selftest_bounded_wait", st)
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -356,6 +368,38 @@ def kda_decode_steps(q, k, v, g_raw, beta, state, accepted=None, *, out=None,
     return out
 
 
+def _prep_outputs(out, B, T, H, d, dt, dev, want_beta):
+    """The (q, k, v, beta) buffers of kda_qkv_prep: allocated when ``out`` is
+    None, else checked like every input (shape, dtype, device, contiguity),
+    so a short or misplaced buffer is refused before any kernel writes it."""
+    if out is None:
+        q, k, v = (torch.empty((B, T, H, d), dtype=dt, device=dev) for _ in range(3))
+        beta = torch.empty((B, T, H), dtype=dt, device=dev) if want_beta else None
+        return q, k, v, beta
+    if not isinstance(out, (tuple, list)) or len(out) != 4:
+        raise TypeError("out must be a tuple (q, k, v, beta)")
+    q, k, v, beta = out
+    for name, t in (("out q", q), ("out k", k), ("out v", v)):
+        if t is None:
+            raise ValueError(f"{name} is missing")
+        _check(t, name, (B, T, H, d), dt, dev)
+    if want_beta:
+        if beta is None:
+            raise ValueError("out beta is missing although beta_logit is given")
+        _check(beta, "out beta", (B, T, H), dt, dev)
+    elif beta is not None:
+        raise ValueError("out beta is given but beta_logit is None")
+    return q, k, v, beta
+
+
+def _gate_output(out, o):
+    """The y buffer of kda_output_gate: new, or checked against o."""
+    if out is None:
+        return torch.empty_like(o)
+    _check(out, "out", tuple(o.shape), o.dtype, o.device)
+    return out
+
+
 def kda_qkv_prep(x_qkv, conv_w, beta_logit=None, cu_seqlens=None, conv_state_in=None, *,
                  conv_state_out=None, output_conv_state: bool = False, l2_eps: float = 0.0,
                  out=None, stream=None):
@@ -393,11 +437,7 @@ def kda_qkv_prep(x_qkv, conv_w, beta_logit=None, cu_seqlens=None, conv_state_in=
         conv_state_out = torch.empty((N, 3, 3, H, d), dtype=dt, device=dev)
     elif conv_state_out is not None:
         _check(conv_state_out, "conv_state_out", (N, 3, 3, H, d), dt, dev)
-    if out is None:
-        q, k, v = (torch.empty((B, T, H, d), dtype=dt, device=dev) for _ in range(3))
-        beta = None if beta_logit is None else torch.empty((B, T, H), dtype=dt, device=dev)
-    else:
-        q, k, v, beta = out
+    q, k, v, beta = _prep_outputs(out, B, T, H, d, dt, dev, beta_logit is not None)
     st = lib.kda_qkv_prep(_dtype_code(x_qkv), B, T, H, d, _ptr(x_qkv), _ptr(conv_w),
                           _ptr(beta_logit), _ptr(cu_seqlens), N, _ptr(conv_state_in),
                           _ptr(conv_state_out), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
@@ -419,7 +459,7 @@ def kda_output_gate(o, gate, norm_w=None, *, eps: float = 0.0, out=None, stream=
     _check(o, "o", tuple(o.shape), o.dtype, dev)
     if norm_w is not None:
         _check(norm_w, "norm_w", (d,), torch.float32, dev)
-    y = torch.empty_like(o) if out is None else out
+    y = _gate_output(out, o)
     st = lib.kda_output_gate(_dtype_code(o), o.numel() // d, d, _ptr(o), _ptr(gate), _ptr(norm_w),
                              float(eps), _ptr(y), _stream_handle(dev, stream))
     if st != 0:

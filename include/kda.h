@@ -283,6 +283,19 @@ int kda_version(void);
  * instead of hanging. */
 kda_status kda_check_device_status(void);
 
+/* Exercises the failure report above without a real fault.  Enqueues one
+ * small kernel on `stream` whose single thread waits, with the same bounded
+ * wait the prefill and prep kernels use, on a shared-memory barrier that
+ * nothing ever arrives at.  After `limit_us` microseconds the wait gives up
+ * and records a timeout exactly as a stalled real launch would, so the next
+ * kda_check_device_status() returns KDA_ERR_TIMEOUT and the one after it
+ * KDA_OK.  The kernel starts no copy, tensor-core product or other
+ * asynchronous work, so giving up leaves nothing in flight and the context
+ * stays usable.  limit_us must be in [1, 100000] (KDA_ERR_ARG otherwise).
+ * The pages define no such call: it is the library's own test hook for its
+ * failure detection. */
+kda_status kda_selftest_bounded_wait(int limit_us, kda_stream_t stream);
+
 /* Number of CUDA kernels this library has enqueued in this process so far
  * (all entry points, all threads).  Lets a caller count launches over a
  * region of its own code. */

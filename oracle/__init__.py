@@ -7,10 +7,11 @@ this package; the CUDA library never does, and the two share no code.
 
 What it computes (from "Kimi K3：从三条信息流到完整系统", wineandchord.com):
 
-* §KDA 是带逐通道遗忘的 delta rule, eq. (1): per (sequence, head), token by
-  token, ``S <- Diag(alpha) S``; ``e = v - S^T k``; ``S <- S + beta k e^T``;
-  ``o = scale * S^T q`` (decay, then delta correction, then the read of the
-  freshly written state, as the kda_step example there fixes).
+* §KDA 是带逐通道遗忘的 delta rule, eq. (1) in its expanded form
+  ``S_t = D + beta_t k_t (v_t - D^T k_t)^T`` with ``D = Diag(alpha_t) S_{t-1}``,
+  and ``o_t = S_t^T q_t``: per (sequence, head), token by token,
+  ``D = Diag(alpha) S``; ``e = v - D^T k``; ``S = D + beta k e^T``;
+  ``o = scale * S^T q`` (the read sees this token's write).
 * §下界 log-decay 是一个 kernel 设计, eq. (5): ``g = g_min *
   sigmoid(e^A z)``, ``alpha = e^g``, ``g_min = -5``.
 * Gate variants ("Kimi K3: Two point eight trillion parameters, open

@@ -12,9 +12,12 @@
  *           S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
  *               = Diag(alpha_t) S_{t-1} + beta_t k_t (v_t^T - k_t^T Diag(alpha_t) S_{t-1})
  *           o_t = S_t^T q_t
- *         and the kda_step example under it, which fixes the order: decay the
- *         key-channel rows first, then the delta correction, then the read
- *         of the freshly written state.
+ *         The steps below are read off this expanded form: D = Diag(alpha_t)
+ *         S_{t-1} scales the key-channel rows and appears in both terms, the
+ *         residual is e = v_t - D^T k_t, the write is S_t = D + beta_t k_t e^T,
+ *         and o_t reads S_t, the state after this token's write.  (The
+ *         worked numbers printed under the equation are a test fixture,
+ *         tests/golden/kda_step_worked_example.json, not a template.)
  *       - §下界 log-decay 是一个 kernel 设计, eq. (5):
  *           g_t = g_min * Sigmoid(e^A z_t),  alpha_t = e^{g_t},  g_min = -5.
  *         and, in the same section, the gate it replaced: Kimi Linear's
@@ -105,28 +108,28 @@ static void chain(int len, int dk, int dv,
         const double *zt = gate ? gate + (ptrdiff_t)t * gate_stride : NULL;
         const double bt = beta[(ptrdiff_t)t * beta_stride];
 
-        /* step 1-2: per-channel retention alpha_c = exp(g_c) */
+        /* eq. (5): per-channel retention alpha_c = exp(g_c) */
         for (int c = 0; c < dk; ++c) {
             double g = zt ? kda_oracle_log_decay(gate_mode, zt[(ptrdiff_t)c * gate_cstride], A_log, g_min)
                           : 0.0;
             alpha[c] = exp(g);
         }
-        /* step 3: decay row c of S (key channel c) by alpha_c */
+        /* D = Diag(alpha) S_{t-1}: row c (key channel c) scaled by alpha_c */
         for (int c = 0; c < dk; ++c)
             for (int j = 0; j < dv; ++j)
                 S[(ptrdiff_t)c * dv + j] *= alpha[c];
-        /* step 4: residual e = v - (Diag(alpha) S)^T k */
+        /* residual of the expanded eq. (1): e = v_t - D^T k_t */
         for (int j = 0; j < dv; ++j) {
             double acc = 0.0;
             for (int c = 0; c < dk; ++c)
                 acc += S[(ptrdiff_t)c * dv + j] * kt[c];
             e[j] = vt[j] - acc;
         }
-        /* step 5: delta write S += beta k e^T */
+        /* S_t = D + beta_t k_t e^T */
         for (int c = 0; c < dk; ++c)
             for (int j = 0; j < dv; ++j)
                 S[(ptrdiff_t)c * dv + j] += bt * kt[c] * e[j];
-        /* step 6: read after write, o = scale * S^T q */
+        /* o_t = scale * S_t^T q_t (the state after this token's write) */
         double *ot = out + (ptrdiff_t)t * tok_stride_v;
         for (int j = 0; j < dv; ++j) {
             double acc = 0.0;

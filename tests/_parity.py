@@ -13,12 +13,12 @@ TOL = {torch.bfloat16: 2e-2, torch.float32: 1e-4}
 
 # A bf16 output cannot be closer to the exact value than its own rounding:
 # on heavy-tailed outputs (max/RMS ~ 13 on the decode workload) rounding the
-# exact fp64 answer to bf16 alone reaches 3.5e-2 x RMS.  So for bf16 outputs
-# the representation error -- up to one bf16 ulp, 2^-8 |ref|, which also
-# covers a result within rounding distance of a boundary landing on either
-# neighbour -- is not counted, just as input rounding is not:
+# exact fp64 answer to bf16 alone reaches 3.5e-2 x RMS.  Where that happens
+# (and only there, see assert_close) the representation error -- up to one
+# bf16 ulp, 2^-8 |ref|, which also covers a result within rounding distance
+# of a boundary landing on either neighbour -- is not counted:
 #     |gpu - ref| <= TOL * RMS(ref) + 2^-8 |ref|      (elementwise)
-# fp32 outputs (the fp32 path and every state) use the plain bound.
+# Everywhere else, and for every fp32 output, the plain bound is asserted.
 BF16_ULP_REL = 2.0 ** -8
 
 
@@ -48,12 +48,56 @@ def compute_err(gpu, ref) -> float:
     return float(np.max(excess)) / rms
 
 
+def rounding_floor(gpu, ref) -> float:
+    """max|round_bf16(ref) - ref| / RMS(ref) for a bf16 output (0 otherwise):
+    how close any output in this format can come to the exact answer."""
+    if getattr(gpu, "dtype", None) != torch.bfloat16:
+        return 0.0
+    r = np.asarray(ref, dtype=np.float64)
+    rb = torch.from_numpy(r).to(torch.bfloat16).double().numpy()
+    return rel_err(rb, r)
+
+
 def assert_close(name, gpu, ref, tol):
-    e = compute_err(gpu, ref)
+    """The literal bound max|gpu - ref| <= tol * RMS(ref) wherever a bf16
+    output can meet it at all (rounding the exact answer to bf16 stays under
+    tol * RMS: every prefill output and every state); the one-ulp allowance
+    above is used only where that rounding alone exceeds the bound (the
+    heavy-tailed decode outputs).  Both numbers are printed."""
+    plain = rel_err(gpu, ref)
+    floor = rounding_floor(gpu, ref)
+    literal = floor <= tol
+    e = plain if literal else compute_err(gpu, ref)
+    print(f"[parity] {name}: plain max|gpu-ref|/RMS = {plain:.3e}, "
+          f"bf16 rounding floor = {floor:.3e}, "
+          f"{'literal bound' if literal else 'beyond one-ulp allowance'} {e:.3e} <= {tol:.1e}")
     assert np.isfinite(e) and e <= tol, (
-        f"{name}: error {e:.3e} x RMS beyond the output format's rounding exceeds {tol:.1e} "
-        f"(plain max-abs/RMS {rel_err(gpu, ref):.3e})")
+        f"{name}: error {e:.3e} x RMS exceeds {tol:.1e} "
+        f"({'plain max-abs/RMS' if literal else 'beyond the bf16 rounding of the exact answer'}; "
+        f"plain {plain:.3e}, rounding floor {floor:.3e})")
     return e
+
+
+def assert_elementwise(name, gpu, ref, ulps=2.0):
+    """Per-element bound for the elementwise passes (no long accumulation):
+    |gpu - ref| <= ulps * ulp(ref) + 1e-6 * RMS(ref), with ulp the output
+    format's spacing at |ref| (bf16: 2^(e-7), fp32: 2^(e-23) for |ref| in
+    [2^e, 2^(e+1))); the small absolute term covers fp32 rounding of terms
+    that cancel to near zero."""
+    g, r = _np(gpu), np.asarray(ref, dtype=np.float64)
+    if not r.size:
+        return 0.0
+    bits = 7 if getattr(gpu, "dtype", None) == torch.bfloat16 else 23
+    e2 = np.floor(np.log2(np.maximum(np.abs(r), 1e-300)))
+    ulp = np.exp2(e2 - bits)
+    rms = float(np.sqrt(np.mean(r * r)))
+    bound = ulps * ulp + 1e-6 * rms
+    worst = float(np.max(np.abs(g - r) / bound))
+    print(f"[parity] {name}: max |gpu-ref| / ({ulps:g} ulp + 1e-6 RMS) = {worst:.3f}, "
+          f"plain max|gpu-ref|/RMS = {rel_err(gpu, ref):.3e}")
+    assert np.isfinite(worst) and worst <= 1.0, (
+        f"{name}: an element is {worst:.2f}x beyond {ulps:g} ulp of the exact value")
+    return worst
 
 
 def oracle_heads(inp, heads, A_log=None, scale=1.0, g_min=-5.0, **gate_kw):

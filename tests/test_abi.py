@@ -130,3 +130,41 @@ def test_checkpointed_validation_rejects_before_launch(lib):
                                 None, None) == 1   # K must be >= 1
     assert lib.kda_decode_steps(1, 4, 3, 2, 128, 128, p0, p0, p0, p0, p0, ctypes.c_void_p(4098),
                                 p0, p0, None, None) == 4   # accepted needs 4-byte alignment
+
+
+def test_prep_and_gate_output_buffers_are_checked():
+    """Caller-supplied output buffers of the pre/post passes get the same
+    shape / dtype / device / contiguity checks as inputs (CPU tensors stand
+    in for device ones: only the host-side checks run)."""
+    import torch
+    B, T, H, d, dt, dev = 1, 8, 2, 32, torch.bfloat16, torch.device("cpu")
+    ok = lambda: torch.empty((B, T, H, d), dtype=dt)
+    beta = torch.empty((B, T, H), dtype=dt)
+    q, k, v, b = kda._prep_outputs((ok(), ok(), ok(), beta), B, T, H, d, dt, dev, True)
+    assert b is beta
+    with pytest.raises(ValueError):          # too short
+        kda._prep_outputs((torch.empty((B, T - 1, H, d), dtype=dt), ok(), ok(), beta),
+                          B, T, H, d, dt, dev, True)
+    with pytest.raises(TypeError):           # wrong dtype
+        kda._prep_outputs((ok(), ok().float(), ok(), beta), B, T, H, d, dt, dev, True)
+    with pytest.raises(ValueError):          # not contiguous
+        kda._prep_outputs((ok(), ok(), torch.empty((B, T, d, H), dtype=dt).transpose(2, 3), beta),
+                          B, T, H, d, dt, dev, True)
+    with pytest.raises(ValueError):          # beta buffer missing while beta_logit is given
+        kda._prep_outputs((ok(), ok(), ok(), None), B, T, H, d, dt, dev, True)
+    with pytest.raises(ValueError):          # beta buffer given without beta_logit
+        kda._prep_outputs((ok(), ok(), ok(), beta), B, T, H, d, dt, dev, False)
+    with pytest.raises(TypeError):
+        kda._prep_outputs((ok(), ok(), ok()), B, T, H, d, dt, dev, False)
+    o = torch.empty((5, d), dtype=dt)
+    assert kda._gate_output(None, o).shape == o.shape
+    with pytest.raises(ValueError):
+        kda._gate_output(torch.empty((4, d), dtype=dt), o)
+    with pytest.raises(TypeError):
+        kda._gate_output(torch.empty((5, d), dtype=torch.float32), o)
+
+
+def test_selftest_wait_limit_is_validated(lib):
+    # out-of-range limits are refused on the host, before any launch
+    assert lib.kda_selftest_bounded_wait(0, None) == 1
+    assert lib.kda_selftest_bounded_wait(100001, None) == 1

@@ -1,9 +1,11 @@
 """Parity of the pre/post passes (kda_qkv_prep, kda_output_gate, through the
 C ABI) with the fp64 oracle in oracle/prepost.py.
 
-Bar: max|gpu - oracle| <= tol * RMS (+ one bf16 ulp of the reference for
-bf16 outputs), tol 2e-2 (bf16) / 1e-4 (fp32) -- the outputs are single
-rounding of a short fp32 computation, so they sit far inside it.
+Bar: per element, |gpu - oracle| <= 2 ulp of the output format at the exact
+value (bf16) or 64 fp32 ulp (the fp32 path's fast sigmoid and reciprocal
+square root), plus 1e-6 RMS for terms that cancel to near zero.  These
+passes are one rounding of a short fp32 computation (no long accumulation),
+so the operator's 2e-2 / 1e-4 RMS bound would be far too loose for them.
 """
 import numpy as np
 import pytest
@@ -12,7 +14,7 @@ import torch
 from gated_delta_rule_11_gb300 import inputs, kda
 from gated_delta_rule_11_gb300 import build as kbuild
 from oracle import prepost
-from tests._parity import TOL, assert_close
+from tests._parity import assert_elementwise
 
 pytestmark = pytest.mark.gpu
 
@@ -21,6 +23,10 @@ pytestmark = pytest.mark.gpu
 def _lib():
     kbuild.build()
     kda.load_library()
+
+
+def _ulps(t):
+    return 2.0 if t.dtype == torch.bfloat16 else 64.0
 
 
 def _cu(seqlens):
@@ -41,11 +47,10 @@ def test_prep_small_varlen(dtype, d, with_state):
     torch.cuda.synchronize()
     rq, rk, rv, rb, rst = prepost.qkv_prep(inp["x_qkv"], inp["conv_w"], inp["beta_logit"],
                                            cu.cpu().numpy(), inp["conv_state"])
-    tol = TOL[q.dtype]
-    assert_close("q", q, rq, tol)
-    assert_close("k", k, rk, tol)
-    assert_close("v", v, rv, tol)
-    assert_close("beta", beta, rb, tol)
+    assert_elementwise("q", q, rq, ulps=_ulps(q))
+    assert_elementwise("k", k, rk, ulps=_ulps(k))
+    assert_elementwise("v", v, rv, ulps=_ulps(v))
+    assert_elementwise("beta", beta, rb, ulps=_ulps(beta))
     assert torch.equal(st.float().cpu(), torch.from_numpy(rst).float())   # states are copies
 
 
@@ -73,7 +78,7 @@ def test_prep_decode_one_token_per_sequence():
     rq, rk, rv, rb, rst = prepost.qkv_prep(inp["x_qkv"], inp["conv_w"], inp["beta_logit"],
                                            np.arange(N + 1), inp["conv_state"])
     for name, g, r in (("q", q, rq), ("k", k, rk), ("v", v, rv), ("beta", beta, rb)):
-        assert_close(name, g, r, TOL[torch.bfloat16])
+        assert_elementwise(name, g, r, ulps=_ulps(g))
     assert torch.equal(st.float().cpu(), torch.from_numpy(rst).float())
 
 
@@ -116,11 +121,10 @@ def test_prep_varlen_workload_sampled():
                 hist[3 - prev.shape[0]:] = prev
             rq, rk, rv, rb, _ = prepost.qkv_prep(x[:, s:e], wt, inp["beta_logit"][:, s:e][:, :, hs],
                                                  None, hist[None])
-            tol = TOL[torch.bfloat16]
-            assert_close(f"q[{s}:{e}]", q[:, s:e][:, :, hs], rq, tol)
-            assert_close(f"k[{s}:{e}]", k[:, s:e][:, :, hs], rk, tol)
-            assert_close(f"v[{s}:{e}]", v[:, s:e][:, :, hs], rv, tol)
-            assert_close(f"beta[{s}:{e}]", beta[:, s:e][:, :, hs], rb, tol)
+            assert_elementwise(f"q[{s}:{e}]", q[:, s:e][:, :, hs], rq, ulps=2.0)
+            assert_elementwise(f"k[{s}:{e}]", k[:, s:e][:, :, hs], rk, ulps=2.0)
+            assert_elementwise(f"v[{s}:{e}]", v[:, s:e][:, :, hs], rv, ulps=2.0)
+            assert_elementwise(f"beta[{s}:{e}]", beta[:, s:e][:, :, hs], rb, ulps=2.0)
         assert torch.equal(st[n], inp["x_qkv"][0, eos - 3:eos])
 
 
@@ -132,10 +136,9 @@ def test_output_gate(dtype, d, rows):
     y = kda.kda_output_gate(inp["o"], inp["gate"], inp["norm_w"])
     y1 = kda.kda_output_gate(inp["o"], inp["gate"], None, eps=1e-3)
     torch.cuda.synchronize()
-    tol = TOL[y.dtype]
-    assert_close("y", y, prepost.output_gate(inp["o"], inp["gate"], inp["norm_w"]), tol)
-    assert_close("y (unit weight, eps 1e-3)", y1,
-                 prepost.output_gate(inp["o"], inp["gate"], None, eps=1e-3), tol)
+    assert_elementwise("y", y, prepost.output_gate(inp["o"], inp["gate"], inp["norm_w"]), ulps=_ulps(y))
+    assert_elementwise("y (unit weight, eps 1e-3)", y1,
+                       prepost.output_gate(inp["o"], inp["gate"], None, eps=1e-3), ulps=_ulps(y1))
 
 
 def test_output_gate_workload_sampled():
@@ -148,7 +151,7 @@ def test_output_gate_workload_sampled():
     idx = torch.tensor(sorted(set(np.random.default_rng(0).integers(0, rows, 4000).tolist()) | {0, rows - 1}),
                        device="cuda")
     ref = prepost.output_gate(inp["o"][idx], inp["gate"][idx], inp["norm_w"])
-    assert_close("y sampled", y[idx], ref, TOL[torch.bfloat16])
+    assert_elementwise("y sampled", y[idx], ref, ulps=_ulps(y[idx]))
 
 
 def test_no_device_wait_gave_up():
