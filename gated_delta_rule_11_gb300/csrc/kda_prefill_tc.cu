@@ -62,8 +62,8 @@
 //                          in-tile decays as running products of the
 //                          retentions, decay-scaled operands, L and A (one
 //                          16x8 block per warp), the triangular solve
-//                          (first warp), W (tf32 mma.sync) and the bf16
-//                          hi/lo operand of (u).
+//                          (first warp only, one barrier), W (tf32 mma.sync)
+//                          and the bf16 hi/lo operand of (u).
 // The chain is serial per tile; the producer and TMA run up to 3 tiles ahead.
 // Tokens past a sequence's end are masked in the producer (k = q = 0, g = 0,
 // beta = 0), which makes U, W, A and the increment vanish for them.
@@ -486,9 +486,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             named_bar_sync(pbar, 128);
             // T = (I + N)^-1, N = Diag(beta) L strictly lower, in 8x8 blocks:
             // T00 = (I + N00)^-1 and T11 = (I + N11)^-1 by forward substitution
-            // (lanes 0-7 / 8-15 of the first warp own one column each), then
-            // T10 = -T11 (N10 T00) as two 8x8 products over 64 threads.  Stored
-            // as T Diag(beta), tf32-rounded.
+            // (lanes 0-7 / 8-15 of the first warp own one column each, right-
+            // looking: once x_m is final every later x_i loses N_im x_m, so the
+            // dependent chain is one FMA per step), then T10 = -T11 (N10 T00) as
+            // two 8x8 products over the same warp.  Stored as T Diag(beta),
+            // tf32-rounded.  Only warp 0 works; one barrier follows.
             const float *betas = reinterpret_cast<const float *>(st + ST_BETA);
             auto row8 = [&](const float *p, float (&x)[8]) {   // 8 floats, two 16-byte loads
                 const float4 lo = *reinterpret_cast<const float4 *>(p);
@@ -496,46 +498,55 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 x[0] = lo.x; x[1] = lo.y; x[2] = lo.z; x[3] = lo.w;
                 x[4] = hi.x; x[5] = hi.y; x[6] = hi.z; x[7] = hi.w;
             };
-            if (pw == 0 && lane < C) {
-                const int j = lane, blk = j >> 3, r0 = 8 * blk;
-                float tb[8];
+            if (pw == 0) {
+                if (lane < C) {
+                    const int j = lane, blk = j >> 3, r0 = 8 * blk;
+                    float br[8], lr[8][8];
+                    row8(betas + r0, br);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int r = r0 + i;
+                    for (int i = 1; i < 8; ++i) row8(ls + (r0 + i) * LSS + r0, lr[i]);
+                    float x[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) x[i] = r0 + i == j ? 1.f : 0.f;
+#pragma unroll
+                    for (int m = 0; m < 7; ++m)
+#pragma unroll
+                        for (int i = m + 1; i < 8; ++i) x[i] = fmaf(-br[i] * lr[i][m], x[m], x[i]);
+                    const float bj = betas[j];
+                    float *tdiag = blk ? t11 : t00;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        tdiag[i * 8 + (j - r0)] = x[i];
+                        tbf[(r0 + i) * TBS + j] = to_tf32(x[i] * bj);
+                        if (blk) tbf[i * TBS + j] = 0.f;           // T01 = 0
+                    }
+                }
+                __syncwarp();
+                // Y = Diag(beta_8..15) L10 T00 and T10 = -T11 Y: two entries per lane
+                float yv[2];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int e = lane + 32 * h2, bi = e >> 3, bj8 = e & 7;
                     float lr[8];
-                    row8(ls + r * LSS + r0, lr);
+                    row8(ls + (8 + bi) * LSS, lr);
                     float acc = 0.f;
 #pragma unroll
-                    for (int i2 = 0; i2 < i; ++i2) acc = fmaf(lr[i2], tb[i2], acc);
-                    tb[i] = (r == j ? 1.f : 0.f) - betas[r] * acc;
+                    for (int m2 = 0; m2 < 8; ++m2) acc = fmaf(lr[m2], t00[m2 * 8 + bj8], acc);
+                    yv[h2] = betas[8 + bi] * acc;
                 }
-                const float bj = betas[j];
-                float *tdiag = blk ? t11 : t00;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    tdiag[i * 8 + (j - r0)] = tb[i];
-                    tbf[(r0 + i) * TBS + j] = to_tf32(tb[i] * bj);
-                    if (blk) tbf[i * TBS + j] = 0.f;           // T01 = 0
+                for (int h2 = 0; h2 < 2; ++h2) ysc[lane + 32 * h2] = yv[h2];
+                __syncwarp();
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int e = lane + 32 * h2, bi = e >> 3, bj8 = e & 7;
+                    float tr[8];
+                    row8(t11 + bi * 8, tr);
+                    float acc = 0.f;
+#pragma unroll
+                    for (int m2 = 0; m2 < 8; ++m2) acc = fmaf(tr[m2], ysc[m2 * 8 + bj8], acc);
+                    tbf[(8 + bi) * TBS + bj8] = to_tf32(-acc * betas[bj8]);
                 }
-            }
-            named_bar_sync(pbar, 128);
-            const int bi = c >> 3, bj8 = c & 7;                 // block entry (bi, bj8) for c < 64
-            if (c < 64) {                                       // Y = Diag(beta_8..15) L10 T00
-                float lr[8];
-                row8(ls + (8 + bi) * LSS, lr);
-                float acc = 0.f;
-#pragma unroll
-                for (int m2 = 0; m2 < 8; ++m2) acc = fmaf(lr[m2], t00[m2 * 8 + bj8], acc);
-                ysc[bi * 8 + bj8] = betas[8 + bi] * acc;
-            }
-            named_bar_sync(pbar, 128);
-            if (c < 64) {                                       // T10 = -T11 Y
-                float tr[8];
-                row8(t11 + bi * 8, tr);
-                float acc = 0.f;
-#pragma unroll
-                for (int m2 = 0; m2 < 8; ++m2) acc = fmaf(tr[m2], ysc[m2 * 8 + bj8], acc);
-                tbf[(8 + bi) * TBS + bj8] = to_tf32(-acc * betas[bj8]);
             }
             named_bar_sync(pbar, 128);
             // T Diag(beta) as the bf16 B operand of U^T = V^T (T Diag(beta))^T
@@ -563,28 +574,33 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     ta[ks][2] = __float_as_uint(tbf[g * TBS + k0 + tq + 4]);
                     ta[ks][3] = __float_as_uint(tbf[(g + 8) * TBS + k0 + tq + 4]);
                 }
+                // n index n of n-block nb is channel 32 pw + 4 n + nb: a lane's B
+                // fragments for the four n-blocks are one float4, and its output
+                // columns (n = 2 tq, 2 tq + 1) are channels 32 pw + 8 tq + 0..7.
                 float dw[4][4];
 #pragma unroll
-                for (int nb = 0; nb < 4; ++nb) {
-                    const int cn = pw * 32 + nb * 8 + g;          // B-fragment column (channel)
+                for (int nb = 0; nb < 4; ++nb)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) dw[nb][e] = 0.f;
 #pragma unroll
-                    for (int ks = 0; ks < 2; ++ks) {
-                        const int s0 = ks * 8 + tq;
-                        const uint32_t bw0 = __float_as_uint(kgm[s0 * PADF + cn]);
-                        const uint32_t bw1 = __float_as_uint(kgm[(s0 + 4) * PADF + cn]);
-                        mma_1688_tf32(dw[nb], ta[ks][0], ta[ks][1], ta[ks][2], ta[ks][3], bw0, bw1);
-                    }
-                }
+                for (int ks = 0; ks < 2; ++ks) {
+                    const int s0 = ks * 8 + tq;
+                    const float4 b0 = *reinterpret_cast<const float4 *>(kgm + s0 * PADF + pw * 32 + 4 * g);
+                    const float4 b1 = *reinterpret_cast<const float4 *>(kgm + (s0 + 4) * PADF + pw * 32 + 4 * g);
+                    const float bl0[4] = {b0.x, b0.y, b0.z, b0.w}, bl1[4] = {b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-                for (int nb = 0; nb < 4; ++nb) {
-                    const int c0 = pw * 32 + nb * 8 + 2 * tq;
-                    *reinterpret_cast<uint32_t *>(st + ST_WQ + off_kmajor_sw128(g, c0, 32)) =
-                        pack_h2(-dw[nb][0], -dw[nb][1]);
-                    *reinterpret_cast<uint32_t *>(st + ST_WQ + off_kmajor_sw128(g + 8, c0, 32)) =
-                        pack_h2(-dw[nb][2], -dw[nb][3]);
+                    for (int nb = 0; nb < 4; ++nb)
+                        mma_1688_tf32(dw[nb], ta[ks][0], ta[ks][1], ta[ks][2], ta[ks][3], __float_as_uint(bl0[nb]),
+                                      __float_as_uint(bl1[nb]));
                 }
+                // channel 32 pw + 8 tq + nb <- dw[nb][0 | 2], + 4 + nb <- dw[nb][1 | 3]
+                const int c0 = pw * 32 + 8 * tq;
+                const uint4 w_lo = make_uint4(pack_h2(-dw[0][0], -dw[1][0]), pack_h2(-dw[2][0], -dw[3][0]),
+                                              pack_h2(-dw[0][1], -dw[1][1]), pack_h2(-dw[2][1], -dw[3][1]));
+                const uint4 w_hi = make_uint4(pack_h2(-dw[0][2], -dw[1][2]), pack_h2(-dw[2][2], -dw[3][2]),
+                                              pack_h2(-dw[0][3], -dw[1][3]), pack_h2(-dw[2][3], -dw[3][3]));
+                *reinterpret_cast<uint4 *>(st + ST_WQ + off_kmajor_sw128(g, c0, 32)) = w_lo;
+                *reinterpret_cast<uint4 *>(st + ST_WQ + off_kmajor_sw128(g + 8, c0, 32)) = w_hi;
             }
             fence_proxy_async_smem();
             mbar_arrive(&bars[B_FULL + s]);

@@ -60,13 +60,16 @@ def rounding_floor(gpu, ref) -> float:
 
 def assert_close(name, gpu, ref, tol):
     """The literal bound max|gpu - ref| <= tol * RMS(ref) wherever a bf16
-    output can meet it at all (rounding the exact answer to bf16 stays under
-    tol * RMS: every prefill output and every state); the one-ulp allowance
-    above is used only where that rounding alone exceeds the bound (the
-    heavy-tailed decode outputs).  Both numbers are printed."""
+    output can meet it with room to spare: rounding the exact answer to bf16
+    costs at most half the tolerance, leaving the other half for the
+    computation (every state, the large prefill outputs).  Where the
+    rounding alone takes more than that (heavy-tailed outputs: decode, and
+    small cases whose few elements make max/RMS large), the one-ulp
+    allowance above is used instead, which still bounds the error beyond
+    the format's own rounding by tol * RMS.  Both numbers are printed."""
     plain = rel_err(gpu, ref)
     floor = rounding_floor(gpu, ref)
-    literal = floor <= tol
+    literal = floor <= 0.5 * tol
     e = plain if literal else compute_err(gpu, ref)
     print(f"[parity] {name}: plain max|gpu-ref|/RMS = {plain:.3e}, "
           f"bf16 rounding floor = {floor:.3e}, "
