@@ -33,10 +33,14 @@ e2e        : prefill tokens/s through the same API with pinned host buffers:
 cpu_baseline / --impl reference : the fp64 CPU oracle on a bounded sample of
              the same workload, on the host's cores.
 
-Multi-GPU (torchrun): every rank runs an independent replica of the
-workload (the (sequence, head) chains share nothing), no collective on the
-data path; the barrier and a max-over-ranks of the timings are the only
-communication.  value = all ranks' tokens / the slowest rank's time.
+Multi-GPU (torchrun): the (sequence, head) chains share nothing, so no
+collective is on the data path; the barrier and a max-over-ranks of the
+timings are the only communication.  --partition replicas (default): every
+rank runs an independent replica of the workload (weak scaling), value = all
+ranks' tokens / the slowest rank's time.  --partition heads: the ranks split
+the one workload's 96 heads ([h0, h1) per rank, partition.head_range; the
+decode state likewise), value = the workload's tokens / the slowest rank's
+time (strong scaling).
 """
 from __future__ import annotations
 
@@ -77,6 +81,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--partition", choices=["replicas", "heads"], default="replicas",
+                    help="multi-GPU: independent replicas, or the ranks split one workload by heads")
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -336,18 +342,28 @@ def run_ours(args, rank, world, local):
 
     # ---- inputs, resident in HBM
     pw = kin.WORKLOADS[args.prefill_workload]
-    inp = kin.make_prefill_inputs(pw, device=dev, seed=pw.seed + 1000 * rank)
+    by_heads = args.partition == "heads" and world > 1
+    if by_heads:      # this rank's heads of the one workload (same shapes per head)
+        from gated_delta_rule_11_gb300.partition import head_range
+        h0, h1 = head_range(rank, world, pw.H)
+        inp = kin.make_prefill_inputs(pw, device=dev, seed=pw.seed + h0, H=h1 - h0)
+    else:
+        h0, h1 = 0, pw.H
+        inp = kin.make_prefill_inputs(pw, device=dev, seed=pw.seed + 1000 * rank)
+    H_rank = h1 - h0
     q, k, v, g, b = (inp[n] for n in ("q", "k", "v", "g_raw", "beta"))
     cu = inp["cu_seqlens"]
     N = pw.n_seqs
     T_total = pw.total_tokens
     out = torch.empty_like(v)
-    fin = torch.empty((N, pw.H, pw.dk, pw.dv), dtype=torch.float32, device=dev)
+    fin = torch.empty((N, H_rank, pw.dk, pw.dv), dtype=torch.float32, device=dev)
 
     dw = DECODE
-    S = kin.make_decode_state(dw, device=dev, seed=dw.seed + 1000 * rank)
-    toks = [kin.make_decode_token(dw, i, device=dev, seed=dw.seed + 1000 * rank) for i in range(4)]
-    dout = torch.empty((dw.N, dw.H, dw.dv), dtype=torch.bfloat16, device=dev)
+    dH = H_rank if by_heads else dw.H
+    dseed = dw.seed + (h0 if by_heads else 1000 * rank)
+    S = kin.make_decode_state(dw, device=dev, seed=dseed, H=dH)
+    toks = [kin.make_decode_token(dw, i, device=dev, seed=dseed, H=dH) for i in range(4)]
+    dout = torch.empty((dw.N, dH, dw.dv), dtype=torch.bfloat16, device=dev)
     torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream(dev)
@@ -399,14 +415,16 @@ def run_ours(args, rank, world, local):
     d_mean = reduce_max(statistics.fmean(decode_ms), world)
     step_ms = reduce_max(total_ms / args.steps, world)
 
-    tokens = T_total * world
+    # whole job: every rank's tokens (replicas), or the one workload's tokens
+    # with its heads split over the ranks
+    tokens = T_total if by_heads else T_total * world
     value = tokens / (p_mean * 1e-3)
-    token_heads = T_total * pw.H
-    alg_bytes = token_heads * BYTES_PER_TOKEN_HEAD + N * pw.H * pw.dk * pw.dv * 4
+    token_heads = T_total * H_rank            # one rank's launch (the roofline is per GPU)
+    alg_bytes = token_heads * BYTES_PER_TOKEN_HEAD + N * H_rank * pw.dk * pw.dv * 4
     alg_flops = token_heads * FLOPS_PER_TOKEN_HEAD
     p_gbs = alg_bytes / (p_mean * 1e-3) / 1e9
     tc_tflops = alg_flops / (p_mean * 1e-3) / 1e12
-    dec_bytes = 2 * dw.N * dw.H * dw.dk * dw.dv * 4
+    dec_bytes = 2 * dw.N * dH * dw.dk * dw.dv * 4
     d_gbs = dec_bytes / (d_mean * 1e-3) / 1e9
     hbm_peak = float(peaks["hbm_gbs"])
     # the prefill launch is timed on its own (CUDA events around it), so the
@@ -427,7 +445,8 @@ def run_ours(args, rank, world, local):
 
     e2e = None
     if not args.no_e2e:   # every rank: the timing is reduced over ranks
-        e2e = run_e2e(kda, q, k, v, g, b, cu, out, fin, args.e2e_steps, world, T_total)
+        e2e = run_e2e(kda, q, k, v, g, b, cu, out, fin, args.e2e_steps, world,
+                      T_total if by_heads else T_total * world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -439,7 +458,7 @@ def run_ours(args, rank, world, local):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "higher_is_better": True, "scaling": "strong" if by_heads else "weak", "vs_baseline": None,
         "dtype": ("f16 tensor-core operands (bf16 inputs; fp32 state, gates and accumulation)"
                   if kernel_name == "prefill_tc_kernel" else "f32 (bf16 inputs)"),
         "data": "synthetic",
@@ -448,7 +467,8 @@ def run_ours(args, rank, world, local):
             "prefill_seqlens": list(pw.seqlens) or [pw.T] * pw.B, "H": pw.H, "dk": pw.dk, "dv": pw.dv,
             "decode_N": dw.N, "l2": "inputs larger than L2 (29 GB prefill inputs, 1.6 GB decode state); no flush",
             "value_counts": "prefill launches only (decode reported under 'decode')",
-            "parallelism": f"replicas x{world}",
+            "parallelism": (f"heads split over {world} ranks ({H_rank} on rank 0)" if by_heads
+                            else f"replicas x{world}"),
         },
         "prefill_ms": p_mean, "decode_ms": d_mean,
         "roofline": {"kernel": kernel_name, "bound": "hbm", "achieved": p_gbs,
@@ -616,7 +636,7 @@ def run_prepost(kda, dev, world, steps, warmup, hbm_peak, peak_src):
     return prep, post
 
 
-def run_e2e(kda, q, k, v, g, b, cu, out, fin, steps, world, T_total):
+def run_e2e(kda, q, k, v, g, b, cu, out, fin, steps, world, job_tokens):
     """Prefill through the public API from pinned host buffers, pipelined:
     every step copies its inputs host->device and its out and final_state
     device->host; step i+1's upload runs while step i computes and downloads
@@ -678,7 +698,7 @@ def run_e2e(kda, q, k, v, g, b, cu, out, fin, steps, world, T_total):
     d2h = hout.numel() * hout.element_size() + hfin.numel() * hfin.element_size()
     del din[1], dout[1]
     torch.cuda.empty_cache()
-    return {"value": T_total * world / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+    return {"value": job_tokens / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "timing": "host wall clock over the steps, device synchronised on both sides",
             "pipelined": "step i+1's host->device copy overlaps step i's kernel and device->host copy"}

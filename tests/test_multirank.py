@@ -2,6 +2,10 @@
 
 * The benchmark's replica timing: every rank reports its time and the
   maximum over ranks is taken (bench.reduce_max / barrier).
+* Head partitioning of one workload (the benchmark's --partition heads):
+  rank r runs heads [h0, h1) of every sequence, no exchange on the data
+  path; gathering the ranks' slices reproduces the unsplit outputs exactly
+  (the oracle stands in for the GPU path on these CPU ranks).
 * Context parallelism over ranks ("Kimi K3：从三条信息流到完整系统",
   §FlashKDA 与 KCP, eq. 17): each rank owns a contiguous segment of one long
   sequence, computes its fragment (M, E) from zero state, one fixed-size
@@ -118,3 +122,59 @@ def test_kcp_composition_over_two_ranks_gloo(cuts):
     got = np.concatenate([res[0][0], res[1][0]], axis=1)
     np.testing.assert_allclose(got, ref_out, rtol=0, atol=1e-11)
     np.testing.assert_allclose(res[1][1], ref_fin, rtol=0, atol=1e-11)
+
+
+def test_head_range_covers_every_head_once():
+    from gated_delta_rule_11_gb300.partition import head_range
+    for H, W in ((96, 1), (96, 2), (96, 8), (7, 3), (5, 5), (130, 8)):
+        ranges = [head_range(r, W, H) for r in range(W)]
+        assert ranges[0][0] == 0 and ranges[-1][1] == H
+        for (a0, a1), (b0, b1) in zip(ranges, ranges[1:]):
+            assert a1 == b0
+        sizes = [b - a for a, b in ranges]
+        assert max(sizes) - min(sizes) <= 1
+    with pytest.raises(ValueError):
+        head_range(0, 4, 3)
+    with pytest.raises(ValueError):
+        head_range(2, 2, 8)
+
+
+def _heads_rank(rank, world, port, q_out):
+    _init(rank, world, port)
+    import oracle
+    from gated_delta_rule_11_gb300 import inputs
+    from gated_delta_rule_11_gb300.partition import shard_heads, unshard_heads
+    w = inputs.Workload("heads", "prefill", H=5, dk=16, dv=8, dtype="f32", z_std=2.0, s0_std=0.1,
+                        seed=11, seqlens=(9, 0, 23, 16))
+    inp = inputs.make_prefill_inputs(w, device="cpu")
+    sl = {n: shard_heads(inp[n], rank, world, axis=2) for n in ("q", "k", "v", "g_raw", "beta")}
+    s0 = shard_heads(inp["init_state"], rank, world, axis=1)
+    out, fin = oracle.kda_oracle_fwd(sl["q"], sl["k"], sl["v"], sl["g_raw"], sl["beta"], s0,
+                                     inp["cu_seqlens"].numpy())
+    outs = [None] * world
+    fins = [None] * world
+    dist.all_gather_object(outs, torch.from_numpy(out))      # reassembly only: no data-path exchange
+    dist.all_gather_object(fins, torch.from_numpy(fin))
+    if rank == 0:
+        ref_out, ref_fin = oracle.kda_oracle_fwd(inp["q"], inp["k"], inp["v"], inp["g_raw"],
+                                                 inp["beta"], inp["init_state"],
+                                                 inp["cu_seqlens"].numpy())
+        got_out = unshard_heads(outs, axis=2).numpy()
+        got_fin = unshard_heads(fins, axis=1).numpy()
+        q_out.put((bool((got_out == ref_out).all()), bool((got_fin == ref_fin).all()),
+                   got_out.shape == ref_out.shape))
+    dist.destroy_process_group()
+
+
+def test_head_partition_reassembles_the_unsplit_run_gloo():
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_heads_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    same_out, same_fin, same_shape = q.get(timeout=180)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert same_shape and same_out and same_fin
