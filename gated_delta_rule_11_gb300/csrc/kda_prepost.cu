@@ -16,11 +16,11 @@
 // sqrt(mean x^2 + eps) and multiplies by a per-channel weight shared by the
 // heads.
 //
-// Both passes are HBM-bound streams.  prep: one CTA owns a run of 64
-// consecutive tokens of one (tensor, head): one TMA copy brings the run and
+// Both passes are HBM-bound streams.  prep: one CTA owns two consecutive
+// runs of 64 tokens of one (tensor, head): a TMA copy per run brings it and
 // the three tokens before it ([67, d], rows before the first token read as
-// zero) into shared memory, so many runs are in flight per SM without
-// holding registers; in each of four warps a group of d/8 lanes owns a
+// zero) into shared memory, both requested up front, so many runs are in
+// flight per SM without holding registers; in each of four warps a group of d/8 lanes owns a
 // token (8 channels per lane, 16-byte loads and stores) and walks its
 // share of the warp's 16 tokens with the three previous inputs in
 // registers, the L2 norm as a group reduction.  A run that stays inside one
@@ -123,8 +123,12 @@ __device__ __forceinline__ void span_of(const PrepArgs &a, int n, int &bos, int 
 }
 
 template <typename Tin, int D>
+__host__ __device__ constexpr int prep_tile_bytes() {
+    return ((kRun + kHalo) * D * static_cast<int>(sizeof(Tin)) + 127) & ~127;
+}
+template <typename Tin, int D>
 constexpr int prep_smem_bytes() {
-    return (((kRun + kHalo) * D * static_cast<int>(sizeof(Tin)) + 15) & ~15) + D * 16 + 16;   // tile + taps + mbarrier
+    return 2 * prep_tile_bytes<Tin, D>() + D * 16 + 16;     // two run tiles + taps + two mbarriers
 }
 
 // Eight consecutive channels as four (even, odd) f32x2 pairs: global and
@@ -172,14 +176,14 @@ template <> struct Oct<float> {
     }
 };
 
-// One CTA per run of kRun tokens of one (tensor, head).  A group of D / 8
-// lanes owns a token (8 channels per lane), so a warp works on 32 * 8 / D
-// tokens at once; each group walks its own consecutive tokens with the three
-// previous inputs in registers.
-// Registers capped for 7 resident CTAs per SM (7 tiles in flight): with the
-// taps re-read from shared memory the cap costs a few spilled bytes.
+// One CTA per two consecutive runs of kRun tokens of one (tensor, head):
+// both runs' TMA tiles are requested at the start, so the second one loads
+// while the first is computed.  A group of D / 8 lanes owns a token (8
+// channels per lane), so a warp works on 32 * 8 / D tokens at once; each
+// group walks its own consecutive tokens with the three previous inputs in
+// registers.  Six resident CTAs per SM keep twelve tiles in flight.
 template <typename Tin, int D>
-__global__ void __launch_bounds__(kPrepWarps * 32, 7) prep_kernel(const __grid_constant__ CUtensorMap tm_x,
+__global__ void __launch_bounds__(kPrepWarps * 32, 6) prep_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                                PrepArgs a) {
     using namespace sm100;
     constexpr int CPL = 8;                       // channels per lane
@@ -189,16 +193,18 @@ __global__ void __launch_bounds__(kPrepWarps * 32, 7) prep_kernel(const __grid_c
     constexpr int PER_SLOT = PER_WARP / SLOTS;   // consecutive tokens per lane group
     static_assert(PER_SLOT >= 1 && PER_WARP % SLOTS == 0, "run split");
     constexpr int TILE_BYTES = (kRun + kHalo) * D * static_cast<int>(sizeof(Tin));
+    constexpr int TILE_STRIDE = prep_tile_bytes<Tin, D>();
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    const Tin *tile = reinterpret_cast<const Tin *>(smem_raw);
-    float *taps_t = reinterpret_cast<float *>(smem_raw + ((TILE_BYTES + 15) & ~15));   // [4][D]: tap-major
-    uint64_t *bar = reinterpret_cast<uint64_t *>(taps_t + 4 * D);
+    float *taps_t = reinterpret_cast<float *>(smem_raw + 2 * TILE_STRIDE);   // [4][D]: tap-major
+    uint64_t *bars = reinterpret_cast<uint64_t *>(taps_t + 4 * D);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H;
-    // task counts fit in 32 bits (the launcher checks)
+    // task counts fit in 32 bits (the launcher checks): a CTA owns the runs
+    // 2 rp, 2 rp + 1 of one (tensor, head) mh, or one empty sequence's state
     const int row_tasks = 3 * H;                                   // (tensor, head) pairs
-    const int run_tasks = (a.T_total + kRun - 1) / kRun * row_tasks;
+    const int n_runs = (a.T_total + kRun - 1) / kRun;
+    const int run_tasks = (n_runs + 1) / 2 * row_tasks;
     const int task = static_cast<int>(blockIdx.x);
     const Tin *sin = static_cast<const Tin *>(a.state_in);
     Tin *sout = static_cast<Tin *>(a.state_out);
@@ -227,19 +233,21 @@ __global__ void __launch_bounds__(kPrepWarps * 32, 7) prep_kernel(const __grid_c
         return;
     }
 
-    const int run = task / row_tasks;
+    const int run0 = task / row_tasks * 2;
     const int mh = task % row_tasks;                       // m * H + h
     const int m = mh / H, h = mh % H;
-    const int t_begin = run * kRun, t_end = min(t_begin + kRun, a.T_total);
+    const int nr = min(2, n_runs - run0);                  // runs of this CTA
     if (tid == 0) {
-        mbar_init(bar, 1);
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
         fence_mbar_init();
     }
     __syncthreads();
-    if (tid == 0) {      // rows t_begin - 3 .. t_begin + 63 of this (tensor, head); out of range -> 0
-        mbar_arrive_expect_tx(bar, TILE_BYTES);
-        tma_load_3d(smem_raw, &tm_x, bar, 0, mh, t_begin - kHalo);
-    }
+    if (tid == 0)        // rows t_begin - 3 .. t_begin + 63 of each run of this (tensor, head); out of range -> 0
+        for (int r = 0; r < nr; ++r) {
+            mbar_arrive_expect_tx(&bars[r], TILE_BYTES);
+            tma_load_3d(smem_raw + r * TILE_STRIDE, &tm_x, &bars[r], 0, mh, (run0 + r) * kRun - kHalo);
+        }
 
     const int slot = lane / LPT, sl = lane % LPT;
     // conv taps of this lane's channels as (even, odd) pairs: wt[tap][pair], tap 3 = current token
@@ -266,120 +274,127 @@ __global__ void __launch_bounds__(kPrepWarps * 32, 7) prep_kernel(const __grid_c
     const size_t col = static_cast<size_t>(mh) * D + c0;            // this lane's channels in a token of x
     Tin *dst = static_cast<Tin *>(m == 0 ? a.q : (m == 1 ? a.k : a.v)) + static_cast<size_t>(h) * D + c0;
     const size_t tok_o = static_cast<size_t>(H) * D;
-    const int s_begin = t_begin + warp * PER_WARP + slot * PER_SLOT;
-    const int s_end = min(s_begin + PER_SLOT, t_end);
-    int n = 0, bos = 0, eos = 0;
-    if (s_begin < s_end) {
-        n = seq_of(a, s_begin);
-        span_of(a, n, bos, eos);
-        while (eos <= s_begin && n + 1 < a.N) {      // empty sequences at s_begin
-            ++n;
+#pragma unroll 1
+    for (int r = 0; r < nr; ++r) {
+        const Tin *tile = reinterpret_cast<const Tin *>(smem_raw + r * TILE_STRIDE);
+        uint64_t *bar = &bars[r];
+        const int t_begin = (run0 + r) * kRun, t_end = min(t_begin + kRun, a.T_total);
+        const int s_begin = t_begin + warp * PER_WARP + slot * PER_SLOT;
+        const int s_end = min(s_begin + PER_SLOT, t_end);
+        int n = 0, bos = 0, eos = 0;
+        if (s_begin < s_end) {
+            n = seq_of(a, s_begin);
             span_of(a, n, bos, eos);
-        }
-    }
-    // warp-uniform: every lane of a warp takes part in the group reductions below
-    if (!__all_sync(0xffffffffu, mbar_wait(bar, 0, kPrepWaitNs))) {
-        if (lane == 0) atomicAdd(&g_prep_timeouts, 1u);
-        // the tile copy may still be in flight into this CTA's shared memory:
-        // give it one more bounded wait before the CTA exits
-        mbar_wait(bar, 0, kPrepWaitNs);
-        return;
-    }
-    auto row_ptr = [&](int t) { return tile + static_cast<size_t>(t - t_begin + kHalo) * D + c0; };
-
-    // window: x of the three tokens before the current one (win[0] oldest)
-    f32x2 win[3][4] = {};
-    auto fill_window = [&](int t) {              // window for token t of sequence n (bos <= t)
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-            const int p = t - 3 + j;
-            if (p >= bos) {
-                Oct<Tin>::ld_shared(row_ptr(p), win[j]);
-            } else if (sin) {
-                const int tap = p - bos + 3;     // 0..2: state token bos - 3 + tap
-                Oct<Tin>::ld_global(sin + (static_cast<size_t>(n) * 3 + tap) * tok_x + col, win[j]);
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) win[j][q] = 0ull;
-            }
-        }
-    };
-    if (s_begin < s_end) fill_window(s_begin);
-    const f32x2 nl2e = pack2(-1.4426950408889634f, -1.4426950408889634f), one = pack2(1.f, 1.f);
-    // one token; Boundary: the run may cross a sequence end (else straight-line code)
-    auto token = [&](int t, bool act, auto boundary) {
-        if (decltype(boundary)::value && act && t >= eos) {                    // next sequence: restart the window
-            do {
+            while (eos <= s_begin && n + 1 < a.N) {      // empty sequences at s_begin
                 ++n;
                 span_of(a, n, bos, eos);
-            } while (eos <= t && n + 1 < a.N);
-            fill_window(t);
-        }
-        f32x2 wt[4][4];
-        load_taps(wt);
-        f32x2 xt[4], y[4], ss2 = 0ull;
-        if (act) Oct<Tin>::ld_shared(row_ptr(t), xt);
-        else
-#pragma unroll
-            for (int q = 0; q < 4; ++q) xt[q] = 0ull;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            f32x2 c = fmul2(wt[0][q], win[0][q]);
-            c = ffma2(wt[1][q], win[1][q], c);
-            c = ffma2(wt[2][q], win[2][q], c);
-            c = ffma2(wt[3][q], xt[q], c);
-            // Swish(c) = c / (1 + e^{-c})
-            const float2 e = unpack2(fmul2(c, nl2e));
-            float ex, ey;
-            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ex) : "f"(e.x));
-            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ey) : "f"(e.y));
-            const float2 den = unpack2(fadd2(pack2(ex, ey), one));
-            y[q] = fmul2(c, pack2(__fdividef(1.0f, den.x), __fdividef(1.0f, den.y)));
-            ss2 = ffma2(y[q], y[q], ss2);
-            win[0][q] = win[1][q];
-            win[1][q] = win[2][q];
-            win[2][q] = xt[q];
-        }
-        if (m < 2) {                              // q, k: L2Norm over the head's d channels
-            const float2 s2 = unpack2(ss2);
-            float ss = s2.x + s2.y;
-#pragma unroll
-            for (int o = LPT / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            const float r = rsqrtf(ss + a.l2_eps);
-            const f32x2 r2 = pack2(r, r);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) y[q] = fmul2(y[q], r2);
-        }
-        if (act) {
-            Oct<Tin>::st_global(dst + static_cast<size_t>(t) * tok_o, y);
-            if (decltype(boundary)::value && t == eos - 1 && sout) {           // last token: save the window as conv state
-#pragma unroll
-                for (int j = 0; j < 3; ++j) {
-                    Tin *sp = sout + (static_cast<size_t>(n) * 3 + j) * tok_x + col;
-                    Oct<Tin>::st_global(sp, win[j]);
-                }
             }
         }
-    };
-    // fast path: every group's tokens are PER_SLOT tokens of one sequence
-    const bool inside = s_end - s_begin == PER_SLOT && eos >= s_end;
-    if (__all_sync(0xffffffffu, inside)) {
-    #pragma unroll
-        for (int u2 = 0; u2 < PER_SLOT; ++u2) token(s_begin + u2, true, std::false_type{});
-        if (eos == s_end && sout) {           // the group ends its sequence: save the window
-    #pragma unroll
-            for (int j = 0; j < 3; ++j)
-                Oct<Tin>::st_global(sout + (static_cast<size_t>(n) * 3 + j) * tok_x + col, win[j]);
+        // warp-uniform: every lane of a warp takes part in the group reductions below
+        if (!__all_sync(0xffffffffu, mbar_wait(bar, 0, kPrepWaitNs))) {
+            if (lane == 0) atomicAdd(&g_prep_timeouts, 1u);
+            // this and the next run's tile copies may still be in flight into
+            // this CTA's shared memory: one more bounded wait each before it exits
+            for (int r2 = r; r2 < nr; ++r2) mbar_wait(&bars[r2], 0, kPrepWaitNs);
+            return;
         }
-    } else {
-        for (int u2 = 0; u2 < PER_SLOT; ++u2) token(s_begin + u2, s_begin + u2 < s_end, std::true_type{});
-    }
-    // beta = Sigmoid(logit) for this run's tokens and head h (the q-tensor CTAs)
-    if (m == 0 && a.beta_logit) {
-        const Tin *bl = static_cast<const Tin *>(a.beta_logit);
-        Tin *bo = static_cast<Tin *>(a.beta);
-        for (int t = t_begin + tid; t < t_end; t += kPrepWarps * 32)
-            st_out(bo + static_cast<size_t>(t) * H + h, sigmoid(ld_in(bl + static_cast<size_t>(t) * H + h)));
+        auto row_ptr = [&](int t) { return tile + static_cast<size_t>(t - t_begin + kHalo) * D + c0; };
+
+        // window: x of the three tokens before the current one (win[0] oldest)
+        f32x2 win[3][4] = {};
+        auto fill_window = [&](int t) {              // window for token t of sequence n (bos <= t)
+    #pragma unroll
+            for (int j = 0; j < 3; ++j) {
+                const int p = t - 3 + j;
+                if (p >= bos) {
+                    Oct<Tin>::ld_shared(row_ptr(p), win[j]);
+                } else if (sin) {
+                    const int tap = p - bos + 3;     // 0..2: state token bos - 3 + tap
+                    Oct<Tin>::ld_global(sin + (static_cast<size_t>(n) * 3 + tap) * tok_x + col, win[j]);
+                } else {
+    #pragma unroll
+                    for (int q = 0; q < 4; ++q) win[j][q] = 0ull;
+                }
+            }
+        };
+        if (s_begin < s_end) fill_window(s_begin);
+        const f32x2 nl2e = pack2(-1.4426950408889634f, -1.4426950408889634f), one = pack2(1.f, 1.f);
+        // one token; Boundary: the run may cross a sequence end (else straight-line code)
+        auto token = [&](int t, bool act, auto boundary) {
+            if (decltype(boundary)::value && act && t >= eos) {                    // next sequence: restart the window
+                do {
+                    ++n;
+                    span_of(a, n, bos, eos);
+                } while (eos <= t && n + 1 < a.N);
+                fill_window(t);
+            }
+            f32x2 wt[4][4];
+            load_taps(wt);
+            f32x2 xt[4], y[4], ss2 = 0ull;
+            if (act) Oct<Tin>::ld_shared(row_ptr(t), xt);
+            else
+    #pragma unroll
+                for (int q = 0; q < 4; ++q) xt[q] = 0ull;
+    #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                f32x2 c = fmul2(wt[0][q], win[0][q]);
+                c = ffma2(wt[1][q], win[1][q], c);
+                c = ffma2(wt[2][q], win[2][q], c);
+                c = ffma2(wt[3][q], xt[q], c);
+                // Swish(c) = c / (1 + e^{-c})
+                const float2 e = unpack2(fmul2(c, nl2e));
+                float ex, ey;
+                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ex) : "f"(e.x));
+                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ey) : "f"(e.y));
+                const float2 den = unpack2(fadd2(pack2(ex, ey), one));
+                y[q] = fmul2(c, pack2(__fdividef(1.0f, den.x), __fdividef(1.0f, den.y)));
+                ss2 = ffma2(y[q], y[q], ss2);
+                win[0][q] = win[1][q];
+                win[1][q] = win[2][q];
+                win[2][q] = xt[q];
+            }
+            if (m < 2) {                              // q, k: L2Norm over the head's d channels
+                const float2 s2 = unpack2(ss2);
+                float ss = s2.x + s2.y;
+    #pragma unroll
+                for (int o = LPT / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                const float r = rsqrtf(ss + a.l2_eps);
+                const f32x2 r2 = pack2(r, r);
+    #pragma unroll
+                for (int q = 0; q < 4; ++q) y[q] = fmul2(y[q], r2);
+            }
+            if (act) {
+                Oct<Tin>::st_global(dst + static_cast<size_t>(t) * tok_o, y);
+                if (decltype(boundary)::value && t == eos - 1 && sout) {           // last token: save the window as conv state
+    #pragma unroll
+                    for (int j = 0; j < 3; ++j) {
+                        Tin *sp = sout + (static_cast<size_t>(n) * 3 + j) * tok_x + col;
+                        Oct<Tin>::st_global(sp, win[j]);
+                    }
+                }
+            }
+        };
+        // fast path: every group's tokens are PER_SLOT tokens of one sequence
+        const bool inside = s_end - s_begin == PER_SLOT && eos >= s_end;
+        if (__all_sync(0xffffffffu, inside)) {
+        #pragma unroll
+            for (int u2 = 0; u2 < PER_SLOT; ++u2) token(s_begin + u2, true, std::false_type{});
+            if (eos == s_end && sout) {           // the group ends its sequence: save the window
+        #pragma unroll
+                for (int j = 0; j < 3; ++j)
+                    Oct<Tin>::st_global(sout + (static_cast<size_t>(n) * 3 + j) * tok_x + col, win[j]);
+            }
+        } else {
+            for (int u2 = 0; u2 < PER_SLOT; ++u2) token(s_begin + u2, s_begin + u2 < s_end, std::true_type{});
+        }
+        // beta = Sigmoid(logit) for this run's tokens and head h (the q-tensor CTAs)
+        if (m == 0 && a.beta_logit) {
+            const Tin *bl = static_cast<const Tin *>(a.beta_logit);
+            Tin *bo = static_cast<Tin *>(a.beta);
+            for (int t = t_begin + tid; t < t_end; t += kPrepWarps * 32)
+                st_out(bo + static_cast<size_t>(t) * H + h, sigmoid(ld_in(bl + static_cast<size_t>(t) * H + h)));
+        }
+
     }
 }
 
@@ -450,7 +465,8 @@ __global__ void __launch_bounds__(kWarps * 32) output_gate_kernel(PostArgs a) {
 // x_qkv [T, 3, H, d] viewed as the 3-D tensor (channel, tensor-head, token).
 template <typename Tin, int D>
 cudaError_t launch_prep_d(const PrepArgs &a, cudaStream_t s) {
-    const long long tasks = static_cast<long long>((a.T_total + kRun - 1) / kRun) * 3 * a.H +
+    // a CTA per pair of runs of each (tensor, head), then one per empty-sequence state
+    const long long tasks = static_cast<long long>(((a.T_total + kRun - 1) / kRun + 1) / 2) * 3 * a.H +
                             static_cast<long long>(a.N) * 3 * a.H;
     if (tasks <= 0) return cudaSuccess;
     if (tasks > 0x7fffffffLL) return cudaErrorInvalidValue;
@@ -469,6 +485,10 @@ cudaError_t launch_prep_d(const PrepArgs &a, cudaStream_t s) {
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     constexpr int smem = prep_smem_bytes<Tin, D>();
+    if (smem > 48 * 1024) {
+        const cudaError_t ea = cudaFuncSetAttribute(prep_kernel<Tin, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (ea != cudaSuccess) return ea;
+    }
     prep_kernel<Tin, D><<<static_cast<unsigned>(tasks), kPrepWarps * 32, smem, s>>>(tm, a);
     const cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
