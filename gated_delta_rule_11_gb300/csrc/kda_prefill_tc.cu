@@ -72,6 +72,7 @@
 
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
+#include "kda_tc_util.cuh"
 
 namespace kda {
 
@@ -79,6 +80,7 @@ __device__ unsigned int g_tc_timeouts = 0;
 
 namespace {
 using namespace sm100;
+using namespace tcu;
 
 constexpr int D = 128;           // dk = dv
 constexpr int C = 16;            // tile tokens
@@ -135,52 +137,6 @@ static_assert(STAGE_BYTES % 1024 == 0 && ST_WQ % 1024 == 0 && ST_KD % 1024 == 0,
 constexpr uint32_t TX_BYTES = 4 * C * D * 2;        // q, k, g_raw, v tiles
 constexpr uint32_t TX_BYTES_NOZ = 3 * C * D * 2;    // q, k, v (gate per head or none)
 
-__device__ __forceinline__ float bf16_at(const uint8_t *p) {
-    return __bfloat162float(__ushort_as_bfloat16(*reinterpret_cast<const uint16_t *>(p)));
-}
-// One of the two bf16 values packed in a 32-bit word (ch 0 = low half).
-__device__ __forceinline__ float bf16_half(uint32_t w, int ch) {
-    return __uint_as_float(ch ? (w & 0xffff0000u) : (w << 16));
-}
-__device__ __forceinline__ void st_h(uint8_t *p, float x) {
-    *reinterpret_cast<uint16_t *>(p) = __half_as_ushort(__float2half_rn(x));
-}
-__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
-    const __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&h);
-}
-constexpr float kLog2e = 1.4426950408889634f;
-// Single-instruction MUFU approximations (rel. error ~2^-22 and 1 ulp).
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float rcp_approx(float x) {
-    float y;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float to_tf32(float x) {
-    uint32_t u;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(u) : "f"(x));
-    return __uint_as_float(u);
-}
-// D (16x8 fp32) += A (16x8 tf32, row) * B (8x8 tf32, col)
-__device__ __forceinline__ void mma_1688_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ float lg2_approx(float x) {
-    float y;
-    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 // log2 of the retention under an unbounded gate map: the gate itself, or
 // -softplus(e^A z) = -(max(x, 0) + log(1 + e^-|x|)), in log2 units.
 __device__ __forceinline__ float unbounded_lg(int mode, float z, float escale) {
