@@ -439,6 +439,8 @@ def run_ours(args, rank, world, local):
 
     layer = run_layer_prefill(kda, dev, rank, world, min(args.steps, 10), args.warmup, hbm_peak,
                               float(peaks["bf16_tflops"]), peak_src)
+    split = run_split_prefill(kda, dev, rank, world, min(args.steps, 10), args.warmup, hbm_peak,
+                              peak_src)
     spec = run_spec(kda, dev, rank, world, args.steps, args.warmup, hbm_peak, peak_src)
     prep, post = run_prepost(kda, dev, world, min(args.steps, 10), args.warmup, hbm_peak, peak_src)
     gates = run_gate_variants(kda, dev, world, min(args.steps, 5), args.warmup, hbm_peak, peak_src)
@@ -484,6 +486,7 @@ def run_ours(args, rank, world, local):
                                 "peak": hbm_peak, "unit": "GB/s", "frac": d_gbs / hbm_peak,
                                 "traffic": d_traffic, "peak_source": peak_src}},
         "layer_prefill": layer,
+        "split_prefill": split,
         "spec_replay": spec, "prep": prep, "post": post, "gate_variants": gates,
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches,
         "clocks": clocks, "wall_s_timed": t_wall,
@@ -521,6 +524,58 @@ def run_layer_prefill(kda, dev, rank, world, steps, warmup, hbm_peak, tc_peak, p
            "tensor": {"achieved_tflops": tfl, "peak_tflops": tc_peak, "frac": tfl / tc_peak,
                       "peak_source": peak_src + " (burst bf16)"}}
     del inp, a, out, fin
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_split_prefill(kda, dev, rank, world, steps, warmup, hbm_peak, peak_src):
+    """One 131,072-token sequence x 12 heads (the 96-head layer sharded 8
+    ways by head): 12 chains on the whole GPU, unsplit and with the segment
+    split (kda_chunk_fwd_split, automatic segment length).  The roofline
+    counts the operator's own bytes (inputs, outputs, final states); the
+    split's workspace traffic is reported beside it."""
+    w = kin.WORKLOADS["tp8_bf16_H12_T131072"]
+    inp = kin.make_prefill_inputs(w, device=dev, seed=w.seed + 1000 * rank)
+    a = [inp[n] for n in ("q", "k", "v", "g_raw", "beta")]
+    out = torch.empty_like(inp["v"])
+    fin = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    tau = kda.split_segment_tokens(w.B, w.T, w.H, w.B, False, sms)
+    ws = torch.empty(max(kda.split_workspace_bytes(w.B, w.T, w.H, w.dk, w.dv, w.B, tau), 1),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    th = w.B * w.T * w.H
+    nbytes = th * BYTES_PER_TOKEN_HEAD + w.B * w.H * w.dk * w.dv * 4
+    res = {"workload": w.name, "chains": w.B * w.H, "sms": sms, "segment_tokens": tau}
+    legs = (("unsplit", lambda i: kda.kda_chunk_fwd(*a, None, None, out=out, final_state=fin)),
+            ("split", lambda i: kda.kda_chunk_fwd_split(*a, None, None, segment_tokens=tau,
+                                                        workspace=ws, out=out, final_state=fin)))
+    for name, fn in legs:
+        for i in range(warmup):
+            fn(i)
+        barrier(world)
+        torch.cuda.synchronize()
+        l0 = kda.launch_count()
+        evs = time_region(fn, steps, stream)
+        torch.cuda.synchronize()
+        ms = reduce_max(statistics.fmean(x.elapsed_time(y) for x, y in evs), world)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"ms": ms, "tokens_per_s": w.B * w.T * world / (ms * 1e-3),
+                     "launches_per_call": (kda.launch_count() - l0) // max(steps, 1),
+                     "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                                  "frac": gbs / hbm_peak, "algorithmic_bytes_per_launch": nbytes,
+                                  "peak_source": peak_src}}
+    P = -(-w.T // tau) if tau else 1
+    # the split's workspace traffic per token and head of segments 1..: the
+    # transition run's q, k, g_raw, beta reads, its fp32 rows written and
+    # read, the zero-state run's fp32 rows (instead of bf16) written and
+    # read; plus the virtual chains' states (written, read, composed)
+    later = w.T - min(tau, w.T) if tau else 0
+    per_tok = (3 * w.dk * 2 + 2) + 2 * w.dk * 4 + (w.dv * 4 - w.dv * 2) + w.dv * 4
+    res["split"]["extra_bytes"] = (w.H * later * per_tok
+                                   + w.H * (2 * P - 1) * w.dk * w.dv * 4 * 3) if tau else 0
+    res["speedup"] = res["unsplit"]["ms"] / res["split"]["ms"]
+    del inp, a, out, fin, ws
     torch.cuda.empty_cache()
     return res
 

@@ -149,7 +149,7 @@ kda_status kda_chunk_fwd_checkpointed(kda_dtype dt, int B, int T, int H, int dk,
     if (const kda_status gs = check_gate(p, dt, g_raw, total > 0)) return gs;
     if (N == 0 || (total == 0 && !final_state)) return KDA_OK;  // nothing to compute
 
-    kda::PrefillArgs a;
+    kda::PrefillArgs a{};
     a.q = q; a.k = k; a.v = v; a.g = g_raw; a.beta = beta;
     a.init_state = init_state;
     a.cu_seqlens = cu_seqlens;
@@ -182,6 +182,133 @@ kda_status kda_chunk_fwd(kda_dtype dt, int B, int T, int H, int dk, int dv,
                          const kda_params *p, kda_stream_t stream) {
     return kda_chunk_fwd_checkpointed(dt, B, T, H, dk, dv, q, k, v, g_raw, beta, init_state,
                                       cu_seqlens, N, out, final_state, 0, nullptr, 0, p, stream);
+}
+
+// ---------------------------------------------------------------- segment split
+namespace {
+constexpr size_t kSplitAlign = 256;
+size_t round_up(size_t x) { return (x + kSplitAlign - 1) / kSplitAlign * kSplitAlign; }
+
+// Upper bound of the virtual sequences: sum over n of (2 P_n - 1) with
+// P_n = max(1, ceil(L_n / tau)) <= L_n / tau + 1.
+long long split_nv_max(long long total, int N, int tau) { return 2 * (total / tau) + 2 + N; }
+
+struct SplitLayout {
+    size_t vseg, seqtab, states, s_in, out_trans, out_zero, bytes;
+};
+SplitLayout split_layout(long long total, int H, int N, int tau) {
+    const long long nv = split_nv_max(total, N, tau);
+    const size_t state_bytes = static_cast<size_t>(nv) * H * 128 * 128 * sizeof(float);
+    SplitLayout l;
+    l.vseg = 0;
+    l.seqtab = round_up(l.vseg + static_cast<size_t>(nv) * 16);
+    l.states = round_up(l.seqtab + static_cast<size_t>(N) * 8);
+    l.s_in = round_up(l.states + state_bytes);
+    const size_t rows = static_cast<size_t>(total) * H * 128 * sizeof(float);
+    l.out_trans = round_up(l.s_in + state_bytes);
+    l.out_zero = round_up(l.out_trans + rows);
+    l.bytes = round_up(l.out_zero + rows);
+    return l;
+}
+}  // namespace
+
+unsigned long long kda_chunk_fwd_split_workspace(int B, int T, int H, int dk, int dv, int N,
+                                                 int segment_tokens) {
+    if (B < 0 || T < 0 || H <= 0 || N < 1 || dk != 128 || dv != 128 || segment_tokens <= 0 ||
+        segment_tokens % 16 != 0)
+        return 0;
+    return split_layout(static_cast<long long>(B) * T, H, N, segment_tokens).bytes;
+}
+
+int kda_split_segment_tokens(int B, int T, int H, int N, int varlen, int sm_count) {
+    if (B < 0 || T < 0 || H <= 0 || N < 1 || sm_count < 1) return 0;
+    const long long chains = static_cast<long long>(N) * H;
+    // P segments per sequence put N H (2P - 1) chains in one wave; packed
+    // sequences of unequal length may need up to N H (2P + 1).
+    const long long per = sm_count / chains;
+    const long long P = varlen ? (per - 1) / 2 : (per + 1) / 2;
+    if (P < 2) return 0;
+    const long long total = static_cast<long long>(B) * T;
+    const long long len = varlen ? (total + N - 1) / N : T;   // mean sequence length
+    const long long tau = ((len + P - 1) / P + 15) / 16 * 16;
+    if (tau <= 0 || tau >= len) return 0;
+    return static_cast<int>(tau);
+}
+
+kda_status kda_chunk_fwd_split(kda_dtype dt, int B, int T, int H, int dk, int dv,
+                               const void *q, const void *k, const void *v,
+                               const void *g_raw, const void *beta,
+                               const float *init_state,
+                               const int32_t *cu_seqlens, int N, int segment_tokens,
+                               void *out, float *final_state,
+                               void *workspace, unsigned long long workspace_bytes,
+                               const kda_params *p, kda_stream_t stream) {
+    if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_DTYPE;
+    if (B < 0 || T < 0 || H <= 0 || H > 65535 || N < 0) return KDA_ERR_ARG;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return KDA_ERR_SHAPE;
+    if (!kda::prefill_tc_supported(dt, dk, dv)) return KDA_ERR_SHAPE;   // bf16, dk = dv = 128 only
+    if (segment_tokens <= 0 || segment_tokens % 16 != 0) return KDA_ERR_ARG;
+    if (cu_seqlens) {
+        if (B != 1 || N < 1) return KDA_ERR_ARG;
+    } else if (N != B) {
+        return KDA_ERR_ARG;
+    }
+    const long long total = static_cast<long long>(B) * T;
+    if (total > INT32_MAX || N == 0) return kda_chunk_fwd(dt, B, T, H, dk, dv, q, k, v, g_raw, beta,
+                                                          init_state, cu_seqlens, N, out, final_state,
+                                                          p, stream);
+    const long long nv = split_nv_max(total, N, segment_tokens);
+    if (nv * H > INT32_MAX) return KDA_ERR_ARG;
+    if (total == 0)   // nothing to split: the plain call copies the initial states
+        return kda_chunk_fwd(dt, B, T, H, dk, dv, q, k, v, g_raw, beta, init_state, cu_seqlens, N,
+                             out, final_state, p, stream);
+    if (!q || !k || !v || !beta || !out || !workspace) return KDA_ERR_ARG;
+    const void *ptrs[] = {q, k, v, init_state, out, final_state};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return KDA_ERR_ALIGN;
+    if (!aligned_to(workspace, kSplitAlign)) return KDA_ERR_ALIGN;
+    if (!aligned_to(beta, 2) || !aligned_to(cu_seqlens, 4)) return KDA_ERR_ALIGN;
+    if (const kda_status gs = check_gate(p, dt, g_raw, true)) return gs;
+    const SplitLayout l = split_layout(total, H, N, segment_tokens);
+    if (workspace_bytes < l.bytes) return KDA_ERR_ARG;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    kda::SplitArgs sa;
+    sa.N = N;
+    sa.H = H;
+    sa.T_total = static_cast<int>(total);
+    sa.T_seq = T;
+    sa.seg_tokens = segment_tokens;
+    sa.nv_max = static_cast<int>(nv);
+    sa.cu_seqlens = cu_seqlens;
+    sa.vseg = reinterpret_cast<int4 *>(ws + l.vseg);
+    sa.seqtab = reinterpret_cast<int2 *>(ws + l.seqtab);
+    sa.states = reinterpret_cast<float *>(ws + l.states);
+    sa.s_in = reinterpret_cast<float *>(ws + l.s_in);
+    sa.out_trans = reinterpret_cast<float *>(ws + l.out_trans);
+    sa.out_zero = reinterpret_cast<float *>(ws + l.out_zero);
+    sa.out = out;
+    sa.final_state = final_state;
+
+    kda::PrefillArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g_raw; a.beta = beta;
+    a.init_state = init_state;
+    a.out = out;
+    a.final_state = sa.states;
+    resolve_params(p, a.g_min, a.A_log, a.scale, a.gate_mode, a.gate_scalar);
+    if (a.A_log && !aligned_to(a.A_log, 4)) return KDA_ERR_ALIGN;
+    a.N = sa.nv_max;
+    a.H = H;
+    a.T_total = sa.T_total;
+    a.T_seq = T;
+    a.vseg = sa.vseg;
+    a.out_trans = sa.out_trans;
+    a.out_zero = sa.out_zero;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (const kda_status st = from_cuda(kda::launch_split_plan(sa, s))) return st;
+    if (const kda_status st = from_cuda(kda::launch_prefill_tc(a, s))) return st;
+    if (const kda_status st = from_cuda(kda::launch_split_compose(sa, s))) return st;
+    return from_cuda(kda::launch_split_fixup(sa, s));
 }
 
 kda_status kda_decode_steps(kda_dtype dt, int N, int K, int H, int dk, int dv,

@@ -29,6 +29,24 @@ struct PrefillArgs {
     float *ckpt;
     long long ckpt_rows;
     int ckpt_every;
+    // Segment split (tensor-core prefill only; ckpt unused): when vseg is
+    // set, chain c runs the virtual sequence vseg[c / H] = {first token,
+    // end token, VSEG_* flags, init source} instead of sequence c / H, and
+    // final_state has one slot per virtual chain.  out_trans / out_zero
+    // ([T_total, H, 128] fp32) receive the output rows of the chains flagged
+    // VSEG_OUT_TRANS / VSEG_OUT_ZERO, unrounded.
+    const int4 *vseg;
+    float *out_trans, *out_zero;
+};
+
+// Flags of a virtual sequence (PrefillArgs::vseg[].z).
+enum : int {
+    VSEG_ZERO_INIT = 1,   // the state entering it is zero (init_state ignored)
+    VSEG_IDENT_INIT = 2,  // the state entering it is the identity (dk == dv)
+    VSEG_ZERO_V = 4,      // every value is zero (v is not read)
+    VSEG_OUT_TRANS = 8,   // its output rows go to out_trans (fp32)
+    VSEG_OUT_ZERO = 16,   // its output rows go to out_zero (fp32)
+    VSEG_EMPTY = 32       // no chain: the CTA exits at once
 };
 
 // Decode: q, k, g_raw [N, K, H, dk]; v, out [N, K, H, dv]; beta [N, K, H];
@@ -157,5 +175,25 @@ unsigned int take_tc_timeouts();
 unsigned int take_prep_timeouts();
 // Test hook: one kernel whose bounded wait on a never-arriving barrier gives up.
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s);
+
+// Segment split (kda_split.cu).  Workspace carved by the caller:
+//   vseg [nv_max] int4, seqtab [N] int2 {first virtual index, segments},
+//   states [nv_max, H, d, d] fp32 (the virtual chains' final states),
+//   s_in [nv_max, H, d, d] fp32 (the true state entering each segment),
+//   out_trans, out_zero [T_total, H, d] fp32 (the transition runs' and the
+//   zero-state runs' outputs of the tokens of segments 1..).
+struct SplitArgs {
+    int N, H, T_total, T_seq, seg_tokens, nv_max;
+    const int32_t *cu_seqlens;
+    int4 *vseg;
+    int2 *seqtab;
+    float *states, *s_in;
+    float *out_trans, *out_zero;
+    void *out;            // the call's output rows (segments 1.. written by the fixup)
+    float *final_state;   // [N, H, d, d] or nullptr
+};
+cudaError_t launch_split_plan(const SplitArgs &a, cudaStream_t s);
+cudaError_t launch_split_compose(const SplitArgs &a, cudaStream_t s);
+cudaError_t launch_split_fixup(const SplitArgs &a, cudaStream_t s);
 
 }  // namespace kda

@@ -152,8 +152,10 @@ __device__ __forceinline__ void note_timeout(volatile int *flag) {
 }
 
 // Unbounded: the launch's gate map is unbounded (the per-tile pair path is
-// compiled in); the bounded instance carries none of that code.
-template <bool Unbounded>
+// compiled in); the bounded instance carries none of that code.  Split: the
+// chains are the virtual sequences of a segment split (PrefillArgs::vseg);
+// the plain instance carries none of that code either.
+template <bool Unbounded, bool Split>
 __global__ void __launch_bounds__(NTHREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_v,
@@ -167,8 +169,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chain = blockIdx.x;
     const int n = chain / a.H, h = chain % a.H;
-    int bos, eos;
-    seq_span(a, n, bos, eos);
+    int bos, eos, vflags = 0, src = n;   // src: the sequence whose init_state enters
+    if constexpr (Split) {                // a virtual sequence of the segment split
+        const int4 e = a.vseg[n];
+        vflags = e.z;
+        if (vflags & VSEG_EMPTY) return;  // uniform: the CTA has not started anything
+        bos = min(max(e.x, 0), a.T_total);
+        eos = min(max(e.y, bos), a.T_total);
+        src = e.w;
+    } else {
+        seq_span(a, n, bos, eos);
+    }
+    const bool zero_v = (vflags & VSEG_ZERO_V) != 0;   // v = 0: the V tiles stay zero
     const int ntiles = (eos - bos + C - 1) / C;
     const size_t state_off = static_cast<size_t>(chain) * D * D;
     // gate source: a TMA tile of per-channel inputs (eq. (5)), one input per
@@ -191,12 +203,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         *abort_flag = 0;
         fence_mbar_init();
     }
+    if (zero_v) {   // no V is loaded: U = T Diag(beta) V reads these zeros
+        for (int i = tid; i < NS * 256; i += NTHREADS)
+            reinterpret_cast<uint4 *>(base + (i >> 8) * STAGE_BYTES + ST_V)[i & 255] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
     if (warp == 0) tmem_alloc(tmem_slot, TMEM_COLS);
     if (tid == 0) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         if (a.gate_mode != KDA_GATE_NONE && !a.gate_scalar) prefetch_tmap(&tm_z);
-        prefetch_tmap(&tm_v);
+        if (!zero_v) prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_o);
     }
     tc_fence_before();
@@ -577,12 +594,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const int ss = tt % NS;
             uint8_t *stg = base + ss * STAGE_BYTES;
             const int tok = bos + tt * C;
-            mbar_arrive_expect_tx(&bars[B_RAW + ss], z_tile ? TX_BYTES : TX_BYTES_NOZ);
+            mbar_arrive_expect_tx(&bars[B_RAW + ss],
+                                  (z_tile ? TX_BYTES : TX_BYTES_NOZ) - (zero_v ? C * D * 2 : 0));
             tma_load_3d(stg + ST_Q, &tm_q, &bars[B_RAW + ss], 0, h, tok);
             tma_load_3d(stg + ST_K, &tm_k, &bars[B_RAW + ss], 0, h, tok);
             if (z_tile) tma_load_3d(stg + ST_Z, &tm_z, &bars[B_RAW + ss], 0, h, tok);
-            tma_load_3d(stg + ST_V, &tm_v, &bars[B_RAW + ss], 0, h, tok);          // channels 0-63
-            tma_load_3d(stg + ST_V + 2048, &tm_v, &bars[B_RAW + ss], 64, h, tok);  // channels 64-127
+            if (!zero_v) {
+                tma_load_3d(stg + ST_V, &tm_v, &bars[B_RAW + ss], 0, h, tok);          // channels 0-63
+                tma_load_3d(stg + ST_V + 2048, &tm_v, &bars[B_RAW + ss], 64, h, tok);  // channels 64-127
+            }
         };
         constexpr int TMA_TID = 160, OST_TID = 192;  // lane 0 of chain warps 5 and 6
         int tma_next = 0;                            // (TMA thread) next tile to load
@@ -626,9 +646,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         };
 
         float S[HR];
+        if constexpr (Split) {
+            const size_t init_off = (static_cast<size_t>(src) * a.H + h) * D * D;
+            const bool init_given = a.init_state && !(vflags & (VSEG_ZERO_INIT | VSEG_IDENT_INIT));
 #pragma unroll
-        for (int cc = 0; cc < HR; ++cc)
-            S[cc] = a.init_state ? a.init_state[state_off + static_cast<size_t>(hf * HR + cc) * D + j] : 0.f;
+            for (int cc = 0; cc < HR; ++cc)
+                S[cc] = (vflags & VSEG_IDENT_INIT) ? (hf * HR + cc == j ? 1.f : 0.f)
+                        : init_given ? a.init_state[init_off + static_cast<size_t>(hf * HR + cc) * D + j] : 0.f;
+        } else {
+#pragma unroll
+            for (int cc = 0; cc < HR; ++cc)
+                S[cc] = a.init_state ? a.init_state[state_off + static_cast<size_t>(hf * HR + cc) * D + j] : 0.f;
+        }
         // fp16 S^T row j, K range [64 hf, 64 hf + 64) -> 32 TMEM columns
         auto write_sT = [&]() {
             uint32_t pk[HR / 2];
@@ -644,6 +673,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (tid == U_TID && ntiles > 0 && !issue_u(0)) note_timeout(abort_flag);
 
         __nv_bfloat16 *gout = static_cast<__nv_bfloat16 *>(a.out);
+        // fp32 rows of a segment-split run (no rounding, no staging)
+        float *fout = !Split ? nullptr
+                      : (vflags & VSEG_OUT_TRANS) ? a.out_trans : (vflags & VSEG_OUT_ZERO) ? a.out_zero : nullptr;
         uint8_t *ost = base + OFF_OST;
         // O of tile tt, rows [8 hf, 8 hf + 8): sum of the accumulators' columns
         // 16..31.  Full tiles go to the staging tile (stored by TMA), a
@@ -664,7 +696,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
             const int tt0 = bos + tt * C;
             const int nvv = min(C, eos - tt0);
-            if (nvv == C) {
+            if (fout) {
+                float *op = fout + static_cast<size_t>(tt0 + 8 * hf) * a.H * D + static_cast<size_t>(h) * D + j;
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+                    if (8 * hf + r < nvv) op[static_cast<size_t>(r) * a.H * D] = a.scale * o[r];
+            } else if (nvv == C) {
                 __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(ost + (tt & 1) * (C * D * 2));
                 const f32x2 sc = pack2(a.scale, a.scale);
 #pragma unroll
@@ -684,7 +721,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // after a chain barrier that follows read_out(tt): one thread stores the staged tile
         auto store_out = [&](int tt) {
             const int tt0 = bos + tt * C;
-            if (min(C, eos - tt0) == C) {
+            if (!fout && min(C, eos - tt0) == C) {
                 tma_store_3d(&tm_o, ost + (tt & 1) * (C * D * 2), 0, h, tt0);
                 bulk_commit();
             }
@@ -844,10 +881,12 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     const bool z_tile = a.gate_mode != KDA_GATE_NONE && !a.gate_scalar;
     if (!make_map(&tq, a.q, a.H, a.T_total, D, false) || !make_map(&tk, a.k, a.H, a.T_total, D, false) ||
         !make_map(&tz, z_tile ? a.g : a.q, a.H, a.T_total, D, false) ||
-        !make_map(&tv, a.v, a.H, a.T_total, D / 2, true) || !make_map(&to, a.out, a.H, a.T_total, D, false))
+        !make_map(&tv, a.v ? a.v : a.q, a.H, a.T_total, D / 2, true) ||
+        !make_map(&to, a.out, a.H, a.T_total, D, false))
         return cudaErrorInvalidValue;
     const bool unbounded = a.gate_mode == KDA_GATE_LOG_DECAY || a.gate_mode == KDA_GATE_NEG_SOFTPLUS;
-    auto kern = unbounded ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
+    auto kern = a.vseg ? (unbounded ? prefill_tc_kernel<true, true> : prefill_tc_kernel<false, true>)
+                       : (unbounded ? prefill_tc_kernel<true, false> : prefill_tc_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(a.N) * static_cast<unsigned>(a.H));

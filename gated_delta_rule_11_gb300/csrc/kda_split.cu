@@ -1,0 +1,317 @@
+// Segment split of the prefill: every sequence is cut into segments of
+// seg_tokens tokens that run at the same time, and the exact result is
+// assembled afterwards.
+//
+// Method: the recurrence of eq. (1) ("Kimi K3：从三条信息流到完整系统",
+// §KDA 是带逐通道遗忘的 delta rule) is affine in the state it starts from.
+// Over a segment starting from S_in,
+//     S_t = Phi_t S_in + S0_t,      o_t = o0_t + S_in^T (Phi_t^T q_t),
+// where (S0, o0) is the segment run from a zero state and Phi_t (dk x dk) is
+// the segment run with v = 0 from S = I: its state is Phi_t and its output
+// Phi_t^T q_t.  The pages compose segments exactly this way across devices
+// (§FlashKDA 与 KCP, eq. (17): a segment is the pair (M, E) = (Phi, S0) and
+// consecutive pairs compose as (M2 M1, M2 E1 + E2)) and across the
+// multiprocessors of one chip ("Kimi K3: Two point eight trillion
+// parameters, open weights, and forty-seven pages of how", §The machine
+// underneath).  Here one launch of the tensor-core prefill runs, for every
+// sequence, segment 0 from its given initial state, segments 1.. from zero,
+// and the transition run of each segment 1..; then
+//   split_compose_kernel: S_in,1 = final state of segment 0 and
+//       S_in,p+1 = Phi_p S_in,p + S0_p (fp32), the last one the final state;
+//   split_fixup_kernel:   o_t = o0_t + S_in,p^T R_t for t in segment p >= 1,
+//       R the transition run's output rows; o0 and R arrive unrounded
+//       (fp32), the product runs on fp16 copies with fp32 sums, and o_t is
+//       rounded to bf16 once.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kda_internal.cuh"
+#include "kda_tc_util.cuh"
+
+namespace kda {
+namespace {
+using namespace tcu;
+
+constexpr int D = 128;
+
+// Sequence n's token span, clamped like the prefill's.
+__device__ __forceinline__ void span_of(const SplitArgs &a, int n, int &b, int &e) {
+    if (a.cu_seqlens) {
+        b = min(max(a.cu_seqlens[n], 0), a.T_total);
+        e = min(max(a.cu_seqlens[n + 1], b), a.T_total);
+    } else {
+        b = n * a.T_seq;
+        e = b + a.T_seq;
+    }
+}
+__device__ __forceinline__ int segments_of(const SplitArgs &a, int n) {
+    int b, e;
+    span_of(a, n, b, e);
+    return max(1, (e - b + a.seg_tokens - 1) / a.seg_tokens);
+}
+
+// One CTA of 1024 threads.  Sequence n with P segments owns the 2P - 1
+// virtual sequences from base_n = sum over m < n of (2 P_m - 1): base_n + p
+// runs segment p (p = 0: the given initial state; p >= 1: zero), and
+// base_n + P + p - 1 the transition run of segment p >= 1, whose .w holds
+// base_n + p, the slot of the state entering that segment.  Entries past
+// the total are empty.
+__global__ void __launch_bounds__(1024) split_plan_kernel(SplitArgs a) {
+    __shared__ int warp_sums[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (a.N + 1023) / 1024;
+    const int n0 = min(tid * per, a.N), n1 = min(n0 + per, a.N);
+    int mine = 0;
+    for (int n = n0; n < n1; ++n) mine += 2 * segments_of(a, n) - 1;
+    // exclusive scan of `mine` over the block
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sums[lane], wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += y;
+        }
+        warp_sums[lane] = wi - w;   // exclusive prefix of the warps
+    }
+    __syncthreads();
+    int base = warp_sums[warp] + incl - mine;
+    for (int n = n0; n < n1; ++n) {
+        int b, e;
+        span_of(a, n, b, e);
+        const int P = max(1, (e - b + a.seg_tokens - 1) / a.seg_tokens);
+        a.seqtab[n] = make_int2(base, P);
+        for (int p = 0; p < P; ++p) {
+            const int sb = min(b + p * a.seg_tokens, e), se = min(sb + a.seg_tokens, e);
+            if (base + p < a.nv_max)
+                a.vseg[base + p] = make_int4(sb, se, p == 0 ? 0 : VSEG_ZERO_INIT | VSEG_OUT_ZERO, n);
+            if (p > 0 && base + P + p - 1 < a.nv_max)
+                a.vseg[base + P + p - 1] =
+                    make_int4(sb, se, VSEG_ZERO_V | VSEG_IDENT_INIT | VSEG_OUT_TRANS, base + p);
+        }
+        base += 2 * P - 1;
+    }
+    // the block's total: the last thread's inclusive end
+    __shared__ int total;
+    if (tid == 1023) total = base;
+    __syncthreads();
+    for (int i = total + tid; i < a.nv_max; i += 1024) a.vseg[i] = make_int4(0, 0, VSEG_EMPTY, 0);
+}
+
+// One CTA per (sequence, head), 256 threads, each an 8 x 8 block of the
+// 128 x 128 product.  Shared memory: Phi^T (row stride 132) and S_in.
+constexpr int CPAD = 132;
+constexpr int COMPOSE_SMEM = (D * CPAD + D * D) * 4;
+
+__global__ void __launch_bounds__(256) split_compose_kernel(SplitArgs a) {
+    extern __shared__ float csm[];
+    float *phiT = csm;              // phiT[c][r] = Phi[r][c]
+    float *sin_ = csm + D * CPAD;   // S_in[c][j]
+    const int n = blockIdx.x / a.H, h = blockIdx.x % a.H;
+    const int tid = threadIdx.x;
+    const int2 st = a.seqtab[n];
+    const int base = st.x, P = st.y;
+    const size_t hs = static_cast<size_t>(D) * D;
+    auto slot = [&](float *buf, int v) { return buf + (static_cast<size_t>(v) * a.H + h) * hs; };
+    const int r0 = (tid >> 4) * 8, j0 = (tid & 15) * 8;
+    // S_in of segment 1 = final state of segment 0
+    const float *cur = slot(a.states, base);
+    for (int i = tid; i < D * D / 4; i += 256)
+        reinterpret_cast<float4 *>(sin_)[i] = reinterpret_cast<const float4 *>(cur)[i];
+    __syncthreads();
+    for (int p = 1; p < P; ++p) {
+        // keep the entering state of segment p for the output fixup
+        float *keep = slot(a.s_in, base + p);
+        for (int i = tid; i < D * D / 4; i += 256)
+            reinterpret_cast<float4 *>(keep)[i] = reinterpret_cast<const float4 *>(sin_)[i];
+        const float *phi = slot(a.states, base + P + p - 1);
+        for (int i = tid; i < D * D; i += 256) {
+            const int r = i >> 7, c = i & 127;
+            phiT[c * CPAD + r] = phi[i];
+        }
+        __syncthreads();
+        float acc[8][8];
+        const float *s0 = slot(a.states, base + p);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 lo = *reinterpret_cast<const float4 *>(s0 + (r0 + i) * D + j0);
+            const float4 hi = *reinterpret_cast<const float4 *>(s0 + (r0 + i) * D + j0 + 4);
+            acc[i][0] = lo.x; acc[i][1] = lo.y; acc[i][2] = lo.z; acc[i][3] = lo.w;
+            acc[i][4] = hi.x; acc[i][5] = hi.y; acc[i][6] = hi.z; acc[i][7] = hi.w;
+        }
+#pragma unroll 2
+        for (int c = 0; c < D; ++c) {
+            const float4 pa = *reinterpret_cast<const float4 *>(phiT + c * CPAD + r0);
+            const float4 pb = *reinterpret_cast<const float4 *>(phiT + c * CPAD + r0 + 4);
+            const float4 sa = *reinterpret_cast<const float4 *>(sin_ + c * D + j0);
+            const float4 sb = *reinterpret_cast<const float4 *>(sin_ + c * D + j0 + 4);
+            const float pr[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+            const float sr[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) acc[i][jj] = fmaf(pr[i], sr[jj], acc[i][jj]);
+        }
+        __syncthreads();   // every thread has read S_in and Phi^T
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            *reinterpret_cast<float4 *>(sin_ + (r0 + i) * D + j0) =
+                make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+            *reinterpret_cast<float4 *>(sin_ + (r0 + i) * D + j0 + 4) =
+                make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+        }
+        __syncthreads();
+    }
+    if (a.final_state) {
+        float *fs = a.final_state + (static_cast<size_t>(n) * a.H + h) * hs;
+        for (int i = tid; i < D * D / 4; i += 256)
+            reinterpret_cast<float4 *>(fs)[i] = reinterpret_cast<const float4 *>(sin_)[i];
+    }
+}
+
+// o_t = o0_t + S_in^T R_t over the rows of one segment: CTA (virtual index,
+// chunk, head) takes FIX_TOKENS tokens of a transition run's segment, 64 at
+// a time.  S_in (fp32) is held as fp16 B fragments in shared memory, laid out
+// [j][c] (row stride 136 halves, conflict-free); R (fp32) is staged as fp16
+// [t][c] (same stride), the next 64 rows loaded into registers while the
+// current ones are multiplied.  Warp w computes rows 16 (w & 3) .. +16 and
+// columns 64 (w >> 2) .. +64 of the 64 x 128 update with m16n8k16 fp16
+// products.
+constexpr int FIX_TOKENS = 1024;
+constexpr int HSTR = 136;
+constexpr int FIX_SMEM = (D * HSTR + 64 * HSTR) * 2;
+
+__global__ void __launch_bounds__(256) split_fixup_kernel(SplitArgs a) {
+    extern __shared__ __align__(16) __half fsm[];
+    __half *sT = fsm;              // sT[j][c] = S_in[c][j]
+    __half *rs = fsm + D * HSTR;   // rs[t][c] = R[t][c]
+    const int vi = blockIdx.x, h = blockIdx.z;
+    const int4 e = a.vseg[vi];
+    if (!(e.z & VSEG_OUT_TRANS)) return;   // one CTA row per transition run
+    const int t_first = e.x + blockIdx.y * FIX_TOKENS;
+    const int t_end = min(e.y, t_first + FIX_TOKENS);
+    if (t_first >= t_end) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const float *R = a.out_trans, *O0 = a.out_zero;
+    __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(a.out);
+    // rows t0 .. t0 + 63 of R: thread tid holds float4 chunks i = tid + 256 k
+    // (row i >> 5, channels 4 (i & 31) ..), zero past the segment
+    float4 nxt[8];
+    auto load_r = [&](int t0) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = tid + 256 * k, t = t0 + (i >> 5);
+            nxt[k] = t < t_end ? *reinterpret_cast<const float4 *>(R + (static_cast<size_t>(t) * a.H + h) * D +
+                                                                    (i & 31) * 4)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    load_r(t_first);
+    {   // S_in^T as fp16: thread tid converts float4 chunks (row c, columns 4 m ..)
+        const float *sin_ = a.s_in + (static_cast<size_t>(e.w) * a.H + h) * D * D;
+        float4 x[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) x[k] = reinterpret_cast<const float4 *>(sin_)[tid + 256 * k];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int i = tid + 256 * k, c = i >> 5, j0 = (i & 31) * 4;
+            sT[(j0 + 0) * HSTR + c] = __float2half_rn(x[k].x);
+            sT[(j0 + 1) * HSTR + c] = __float2half_rn(x[k].y);
+            sT[(j0 + 2) * HSTR + c] = __float2half_rn(x[k].z);
+            sT[(j0 + 3) * HSTR + c] = __float2half_rn(x[k].w);
+        }
+    }
+    const int g = lane >> 2, tq = lane & 3;
+    const int m0 = 16 * (warp & 3), n0 = 64 * (warp >> 2);
+    for (int t0 = t_first; t0 < t_end; t0 += 64) {
+        __syncthreads();   // sT written / previous rows consumed
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = tid + 256 * k;
+            *reinterpret_cast<uint2 *>(rs + (i >> 5) * HSTR + (i & 31) * 4) =
+                make_uint2(pack_h2(nxt[k].x, nxt[k].y), pack_h2(nxt[k].z, nxt[k].w));
+        }
+        __syncthreads();
+        if (t0 + 64 < t_end) load_r(t0 + 64);   // in flight during the products
+        // this thread's o0 entries, loaded ahead of the products
+        float2 o0[2][8];
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            const int t = min(t0 + m0 + g + 8 * hr, t_end - 1);
+            const size_t row = (static_cast<size_t>(t) * a.H + h) * D;
+#pragma unroll
+            for (int nb = 0; nb < 8; ++nb)
+                o0[hr][nb] = *reinterpret_cast<const float2 *>(O0 + row + n0 + 8 * nb + 2 * tq);
+        }
+        float acc[8][4];
+#pragma unroll
+        for (int nb = 0; nb < 8; ++nb)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[nb][q] = 0.f;
+#pragma unroll
+        for (int k0 = 0; k0 < D; k0 += 16) {
+            const uint32_t a0 = *reinterpret_cast<const uint32_t *>(rs + (m0 + g) * HSTR + k0 + 2 * tq);
+            const uint32_t a1 = *reinterpret_cast<const uint32_t *>(rs + (m0 + g + 8) * HSTR + k0 + 2 * tq);
+            const uint32_t a2 = *reinterpret_cast<const uint32_t *>(rs + (m0 + g) * HSTR + k0 + 2 * tq + 8);
+            const uint32_t a3 = *reinterpret_cast<const uint32_t *>(rs + (m0 + g + 8) * HSTR + k0 + 2 * tq + 8);
+#pragma unroll
+            for (int nb = 0; nb < 8; ++nb) {
+                const int j = n0 + 8 * nb + g;
+                const uint32_t b0 = *reinterpret_cast<const uint32_t *>(sT + j * HSTR + k0 + 2 * tq);
+                const uint32_t b1 = *reinterpret_cast<const uint32_t *>(sT + j * HSTR + k0 + 2 * tq + 8);
+                mma_16816_f16(acc[nb], a0, a1, a2, a3, b0, b1);
+            }
+        }
+        // rows m0 + g (acc[.][0..1]) and m0 + g + 8 (acc[.][2..3]), columns n0 + 8 nb + 2 tq + {0, 1}
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            const int t = t0 + m0 + g + 8 * hr;
+            if (t >= t_end) continue;
+            __nv_bfloat16 *orow = O + (static_cast<size_t>(t) * a.H + h) * D;
+#pragma unroll
+            for (int nb = 0; nb < 8; ++nb)
+                *reinterpret_cast<__nv_bfloat162 *>(orow + n0 + 8 * nb + 2 * tq) =
+                    __floats2bfloat162_rn(o0[hr][nb].x + acc[nb][2 * hr], o0[hr][nb].y + acc[nb][2 * hr + 1]);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_split_plan(const SplitArgs &a, cudaStream_t s) {
+    split_plan_kernel<<<1, 1024, 0, s>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
+
+cudaError_t launch_split_compose(const SplitArgs &a, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(split_compose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         COMPOSE_SMEM);
+    if (e != cudaSuccess) return e;
+    split_compose_kernel<<<static_cast<unsigned>(a.N) * static_cast<unsigned>(a.H), 256, COMPOSE_SMEM, s>>>(a);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
+
+cudaError_t launch_split_fixup(const SplitArgs &a, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(split_fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         FIX_SMEM);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(static_cast<unsigned>(a.nv_max), static_cast<unsigned>((a.seg_tokens + FIX_TOKENS - 1) / FIX_TOKENS),
+                    static_cast<unsigned>(a.H));
+    split_fixup_kernel<<<grid, 256, FIX_SMEM, s>>>(a);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
+
+}  // namespace kda

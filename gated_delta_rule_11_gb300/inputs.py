@@ -72,6 +72,11 @@ WORKLOADS = {
     "varlen_bf16_H96_237568": Workload("varlen_bf16_H96_237568", "prefill", H=96, dk=128, dv=128,
                                        dtype="bf16", z_std=2.0, s0_std=0.0, seed=3,
                                        seqlens=(131072, 65536, 32768, 8192)),
+    # The layer's 96 heads sharded 8 ways by head (12 per GPU), one
+    # 131,072-token sequence: fewer chains than multiprocessors, the shape
+    # the segment split is for.
+    "tp8_bf16_H12_T131072": Workload("tp8_bf16_H12_T131072", "prefill", H=12, dk=128, dv=128,
+                                     dtype="bf16", z_std=2.0, s0_std=0.0, seed=6, B=1, T=131072),
     "decode_bf16_N256_H96": Workload("decode_bf16_N256_H96", "decode", H=96, dk=128, dv=128,
                                      dtype="bf16", z_std=2.0, s0_std=0.1, seed=4, N=256, steps=100),
     # Speculative replay: 8 tokens verified per sequence (the last committed

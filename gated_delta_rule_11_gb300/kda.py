@@ -27,7 +27,8 @@ _lock = threading.Lock()
 EXPORTED = ("kda_chunk_fwd", "kda_decode_step", "kda_status_str", "kda_last_cuda_error",
             "kda_version", "kda_launch_count", "kda_check_device_status", "kda_chunk_fwd_kernel",
             "kda_decode_steps", "kda_chunk_fwd_checkpointed", "kda_checkpoint_rows",
-            "kda_qkv_prep", "kda_output_gate", "kda_selftest_bounded_wait")
+            "kda_qkv_prep", "kda_output_gate", "kda_selftest_bounded_wait",
+            "kda_chunk_fwd_split", "kda_chunk_fwd_split_workspace", "kda_split_segment_tokens")
 
 
 class KdaError(RuntimeError):
@@ -75,6 +76,14 @@ def load_library(build_if_missing: bool = False):
         lib.kda_chunk_fwd_checkpointed.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, i,
                                                    vp, vp, i, vp, ctypes.c_longlong,
                                                    ctypes.POINTER(KdaParams), vp]
+        lib.kda_chunk_fwd_split.restype = i
+        lib.kda_chunk_fwd_split.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, i, i,
+                                            vp, vp, vp, ctypes.c_ulonglong,
+                                            ctypes.POINTER(KdaParams), vp]
+        lib.kda_chunk_fwd_split_workspace.restype = ctypes.c_ulonglong
+        lib.kda_chunk_fwd_split_workspace.argtypes = [i, i, i, i, i, i, i]
+        lib.kda_split_segment_tokens.restype = i
+        lib.kda_split_segment_tokens.argtypes = [i, i, i, i, i, i]
         lib.kda_checkpoint_rows.restype = ctypes.c_longlong
         lib.kda_checkpoint_rows.argtypes = [i, i, vp, i, i]
         lib.kda_qkv_prep.restype = i
@@ -251,9 +260,65 @@ def kda_chunk_fwd_checkpointed(q, k, v, g_raw, beta, init_state=None, cu_seqlens
     return out, final_state, checkpoints, first
 
 
+def split_segment_tokens(B: int, T: int, H: int, N: int, varlen: bool, sm_count: int) -> int:
+    """Segment length for kda_chunk_fwd_split that puts every chain in one
+    wave on ``sm_count`` multiprocessors, or 0 when splitting cannot."""
+    return int(load_library().kda_split_segment_tokens(int(B), int(T), int(H), int(N),
+                                                        int(bool(varlen)), int(sm_count)))
+
+
+def split_workspace_bytes(B: int, T: int, H: int, dk: int, dv: int, N: int,
+                          segment_tokens: int) -> int:
+    """Bytes of device workspace kda_chunk_fwd_split needs (0: rejected sizes)."""
+    return int(load_library().kda_chunk_fwd_split_workspace(int(B), int(T), int(H), int(dk),
+                                                             int(dv), int(N),
+                                                             int(segment_tokens)))
+
+
+def kda_chunk_fwd_split(q, k, v, g_raw, beta, init_state=None, cu_seqlens=None, *,
+                        segment_tokens: int | None = None, workspace=None, out=None,
+                        final_state=None, output_final_state: bool = True,
+                        g_min: float = -5.0, A_log=None, scale: float = 1.0,
+                        gate_mode: str = "bounded", gate_per_head: bool = False, stream=None):
+    """kda_chunk_fwd with every sequence cut into segments of
+    ``segment_tokens`` tokens that run concurrently (bf16, dk = dv = 128).
+
+    segment_tokens None: split_segment_tokens for this device's SM count;
+    when that is 0 (enough chains already), the plain kda_chunk_fwd runs.
+    workspace: a uint8 CUDA tensor of at least split_workspace_bytes(...)
+    bytes (allocated here when None).  Returns (out, final_state).
+    """
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("kda_chunk_fwd_split runs on CUDA tensors only")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if segment_tokens is None:
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        segment_tokens = split_segment_tokens(B, T, H, N, cu_seqlens is not None, sms)
+        if segment_tokens == 0:
+            return kda_chunk_fwd(q, k, v, g_raw, beta, init_state, cu_seqlens, out=out,
+                                 final_state=final_state, output_final_state=output_final_state,
+                                 g_min=g_min, A_log=A_log, scale=scale, gate_mode=gate_mode,
+                                 gate_per_head=gate_per_head, stream=stream)
+    need = split_workspace_bytes(B, T, H, dk, dv, max(N, 1), segment_tokens)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    elif (workspace.device != dev or workspace.dtype != torch.uint8 or
+          not workspace.is_contiguous() or workspace.numel() < need):
+        raise ValueError(f"workspace must be a contiguous uint8 tensor of >= {need} bytes on {dev}")
+    out, final_state, _ = _chunk_fwd(q, k, v, g_raw, beta, init_state, cu_seqlens, out,
+                                     final_state, output_final_state, g_min, A_log, scale,
+                                     stream, 0, None, 0, "kda_chunk_fwd_split", gate_mode,
+                                     gate_per_head, split=(int(segment_tokens), workspace))
+    return out, final_state
+
+
 def _chunk_fwd(q, k, v, g_raw, beta, init_state, cu_seqlens, out, final_state,
                output_final_state, g_min, A_log, scale, stream, every, ckpt, ckpt_rows, name,
-               gate_mode="bounded", gate_per_head=False):
+               gate_mode="bounded", gate_per_head=False, split=None):
     lib = load_library()
     dev = q.device
     if dev.type != "cuda":
@@ -288,7 +353,12 @@ def _chunk_fwd(q, k, v, g_raw, beta, init_state, cu_seqlens, out, final_state,
     prm = _params(g_min, A_log, scale, gate_mode, gate_per_head)
     common = (_dtype_code(q), B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw),
               _ptr(beta), _ptr(init_state), _ptr(cu_seqlens), N, _ptr(out), _ptr(final_state))
-    if ckpt is None:
+    if split is not None:
+        tau, ws = split
+        head = common[:14]
+        st = lib.kda_chunk_fwd_split(*head, tau, _ptr(out), _ptr(final_state), _ptr(ws),
+                                     ws.numel(), ctypes.byref(prm), _stream_handle(dev, stream))
+    elif ckpt is None:
         st = lib.kda_chunk_fwd(*common, ctypes.byref(prm), _stream_handle(dev, stream))
     else:
         st = lib.kda_chunk_fwd_checkpointed(*common, int(every), _ptr(ckpt), int(ckpt_rows),

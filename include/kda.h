@@ -170,6 +170,67 @@ kda_status kda_chunk_fwd_checkpointed(kda_dtype dt, int B, int T, int H, int dk,
                                       const kda_params *p, kda_stream_t stream);
 
 /*
+ * kda_chunk_fwd_split -- kda_chunk_fwd for launches with fewer (sequence,
+ * head) chains than the GPU has multiprocessors.  Each sequence is cut into
+ * consecutive segments of segment_tokens tokens (the last one shorter) that
+ * run at the same time, and the exact result is assembled afterwards
+ * ("Kimi K3: Two point eight trillion parameters, open weights, and
+ * forty-seven pages of how", §The machine underneath: the sequence split
+ * across the chip's multiprocessors and merged; the merge is the segment
+ * composition of "Kimi K3：从三条信息流到完整系统", §FlashKDA 与 KCP, eq. (17)).
+ * Because eq. (1) is affine in the state it starts from, a segment started
+ * from S_in gives S_t = Phi_t S_in + S0_t and o_t = o0_t + S_in^T Phi_t^T q_t,
+ * with (S0, o0) the segment run from a zero state and Phi_t the run with
+ * v = 0 from the identity (its state is Phi_t, its output Phi_t^T q_t).  A
+ * sequence of P segments therefore costs 2P - 1 concurrent chains of at most
+ * segment_tokens tokens, plus a serial fp32 composition of P - 1 128 x 128
+ * products per (sequence, head) and a per-token correction of the outputs
+ * of segments 1 .. P - 1; it pays when N * H * (2P - 1) chains fit the GPU
+ * at once (see kda_split_segment_tokens).
+ *
+ * Arguments as kda_chunk_fwd, plus:
+ *   segment_tokens: a positive multiple of 16 (KDA_ERR_ARG otherwise).
+ *   workspace: DEVICE scratch of at least kda_chunk_fwd_split_workspace(...)
+ *          bytes, 256-byte aligned, caller-owned; its contents on entry are
+ *          ignored and on return unspecified.  It must not overlap any other
+ *          argument, and no other call may use it until this one completes
+ *          on the stream.
+ * Supported for dt = KDA_BF16 with dk = dv = 128 (the tensor-core prefill);
+ * KDA_ERR_SHAPE otherwise.  Not combinable with checkpoints.
+ * Numerics: the segments run the same kernel as kda_chunk_fwd; the
+ * composition is fp32; for the tokens of segments 1 .. the zero-state and
+ * transition runs write their outputs unrounded (fp32, in the workspace),
+ * the correction S_in^T (Phi^T q) multiplies fp16 copies of S_in and of the
+ * transition outputs with fp32 accumulation, and o is rounded to bf16 once.
+ */
+kda_status kda_chunk_fwd_split(kda_dtype dt, int B, int T, int H, int dk, int dv,
+                               const void *q, const void *k, const void *v,
+                               const void *g_raw, const void *beta,
+                               const float *init_state,
+                               const int32_t *cu_seqlens, int N, int segment_tokens,
+                               void *out, float *final_state,
+                               void *workspace, unsigned long long workspace_bytes,
+                               const kda_params *p, kda_stream_t stream);
+
+/*
+ * kda_chunk_fwd_split_workspace -- bytes of workspace kda_chunk_fwd_split
+ * needs for these sizes (B * T tokens in all, N sequences), or 0 for
+ * arguments it would reject.  No GPU work.
+ */
+unsigned long long kda_chunk_fwd_split_workspace(int B, int T, int H, int dk, int dv, int N,
+                                                 int segment_tokens);
+
+/*
+ * kda_split_segment_tokens -- host helper: a segment length (multiple of
+ * 16) that puts every chain of the split in one wave on sm_count
+ * multiprocessors (one chain per multiprocessor), or 0 when splitting
+ * cannot (fewer than two segments per sequence fit).  varlen != 0: the
+ * B * T tokens are N packed sequences of unknown lengths (the bound then
+ * allows two chains more per sequence).  No GPU work.
+ */
+int kda_split_segment_tokens(int B, int T, int H, int N, int varlen, int sm_count);
+
+/*
  * kda_checkpoint_rows -- host helper: rows of the checkpoint buffer for
  * these sequences (cu_seqlens_host: HOST [N+1] or NULL for B rows of T).
  * Returns -1 for arguments kda_chunk_fwd would reject (E not a positive

@@ -168,3 +168,47 @@ def test_selftest_wait_limit_is_validated(lib):
     # out-of-range limits are refused on the host, before any launch
     assert lib.kda_selftest_bounded_wait(0, None) == 1
     assert lib.kda_selftest_bounded_wait(100001, None) == 1
+
+
+def _split(lib, dt=1, B=1, T=1024, H=2, dk=128, dv=128, ptr=4096, N=1, tau=256, ws=4096,
+           ws_bytes=1 << 40, cu=None):
+    p = ctypes.c_void_p(ptr)
+    return lib.kda_chunk_fwd_split(dt, B, T, H, dk, dv, p, p, p, p, p, None, cu, N, tau, p, None,
+                                   ctypes.c_void_p(ws) if ws else None, ws_bytes, None, None)
+
+
+def test_split_validation_rejects_before_launch(lib):
+    # Every case fails validation, so no pointer is dereferenced and no CUDA call is made.
+    assert _split(lib, dt=0) == 3                 # fp32: the split runs on the bf16 tensor-core path
+    assert _split(lib, dk=64, dv=64) == 3
+    assert _split(lib, dt=7) == 2
+    assert _split(lib, tau=0) == 1 and _split(lib, tau=40) == 1 and _split(lib, tau=-16) == 1
+    assert _split(lib, B=2, N=1) == 1             # N must equal B without cu_seqlens
+    assert _split(lib, ws=0) == 1                 # workspace required
+    assert _split(lib, ws=4096 + 16) == 4         # workspace 256-byte aligned
+    need = lib.kda_chunk_fwd_split_workspace(1, 1024, 2, 128, 128, 1, 256)
+    assert need > 0
+    assert _split(lib, ws_bytes=need - 1) == 1    # too small
+    assert _split(lib, ptr=4096 + 2) == 4         # misaligned tensors
+
+
+def test_split_workspace_and_segment_helpers(lib):
+    ws = lib.kda_chunk_fwd_split_workspace
+    # rejected sizes give 0
+    assert ws(1, 1024, 2, 64, 64, 1, 256) == 0 and ws(1, 1024, 2, 128, 128, 1, 24) == 0
+    assert ws(1, 1024, 2, 128, 128, 0, 256) == 0
+    # grows with the tokens (second output) and the virtual chains (states)
+    a, b = ws(1, 1024, 2, 128, 128, 1, 256), ws(1, 2048, 2, 128, 128, 1, 256)
+    c = ws(1, 1024, 2, 128, 128, 1, 128)
+    assert 0 < a < b and a < c
+    assert a >= 1024 * 2 * 128 * 2 + 2 * 2 * 128 * 128 * 4   # out2 plus two state sets
+    seg = lib.kda_split_segment_tokens
+    # 12 chains on 152 SMs: 6 segments (11 chains each) for equal lengths, 5 for packed
+    assert seg(1, 131072, 12, 1, 0, 152) == 131072 // 6 // 16 * 16 + 16 * (131072 // 6 % 16 != 0)
+    t5 = seg(1, 131072, 12, 1, 1, 152)
+    assert t5 % 16 == 0 and -(-131072 // t5) == 5
+    # 96 chains (the layer shape): no split fits one wave
+    assert seg(1, 8192, 96, 1, 0, 152) == 0
+    assert seg(1, 8192, 0, 1, 0, 152) == 0 and seg(1, 8192, 12, 1, 0, 0) == 0
+    for tau, n in ((seg(1, 8192, 12, 1, 0, 152), 6), (seg(1, 100000, 4, 1, 0, 152), 19)):
+        assert tau % 16 == 0 and -(-(8192 if n == 6 else 100000) // tau) <= n
