@@ -72,6 +72,7 @@ const char *kda_status_str(kda_status s) {
         case KDA_ERR_ALIGN: return "pointer not 16-byte aligned";
         case KDA_ERR_LAUNCH: return "CUDA launch failed";
         case KDA_ERR_TIMEOUT: return "a bounded device wait timed out";
+        case KDA_ERR_SCRATCH: return "the call needs more scratch than the library's static buffer (KDA_SPLIT_SCRATCH_BYTES) holds";
     }
     return "unknown status";
 }

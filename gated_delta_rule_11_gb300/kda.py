@@ -19,7 +19,7 @@ from . import build as _build
 
 KDA_F32, KDA_BF16 = 0, 1
 _STATUS = {0: "KDA_OK", 1: "KDA_ERR_ARG", 2: "KDA_ERR_DTYPE", 3: "KDA_ERR_SHAPE",
-           4: "KDA_ERR_ALIGN", 5: "KDA_ERR_LAUNCH", 6: "KDA_ERR_TIMEOUT"}
+           4: "KDA_ERR_ALIGN", 5: "KDA_ERR_LAUNCH", 6: "KDA_ERR_TIMEOUT", 7: "KDA_ERR_SCRATCH"}
 
 _lib = None
 _lock = threading.Lock()
@@ -28,7 +28,8 @@ EXPORTED = ("kda_chunk_fwd", "kda_decode_step", "kda_status_str", "kda_last_cuda
             "kda_version", "kda_launch_count", "kda_check_device_status", "kda_chunk_fwd_kernel",
             "kda_decode_steps", "kda_chunk_fwd_checkpointed", "kda_checkpoint_rows",
             "kda_qkv_prep", "kda_output_gate", "kda_selftest_bounded_wait",
-            "kda_chunk_fwd_split", "kda_chunk_fwd_split_workspace", "kda_split_segment_tokens")
+            "kda_chunk_fwd_split", "kda_chunk_fwd_split_workspace", "kda_split_segment_tokens",
+            "kda_chunk_fwd_split_noalloc")
 
 
 class KdaError(RuntimeError):
@@ -80,6 +81,9 @@ def load_library(build_if_missing: bool = False):
         lib.kda_chunk_fwd_split.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, i, i,
                                             vp, vp, vp, ctypes.c_ulonglong,
                                             ctypes.POINTER(KdaParams), vp]
+        lib.kda_chunk_fwd_split_noalloc.restype = i
+        lib.kda_chunk_fwd_split_noalloc.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, i,
+                                                    i, vp, vp, ctypes.POINTER(KdaParams), vp]
         lib.kda_chunk_fwd_split_workspace.restype = ctypes.c_ulonglong
         lib.kda_chunk_fwd_split_workspace.argtypes = [i, i, i, i, i, i, i]
         lib.kda_split_segment_tokens.restype = i
@@ -313,6 +317,52 @@ def kda_chunk_fwd_split(q, k, v, g_raw, beta, init_state=None, cu_seqlens=None, 
                                      final_state, output_final_state, g_min, A_log, scale,
                                      stream, 0, None, 0, "kda_chunk_fwd_split", gate_mode,
                                      gate_per_head, split=(int(segment_tokens), workspace))
+    return out, final_state
+
+
+# Size of the library's own scratch buffer used by kda_chunk_fwd_split_noalloc.
+SPLIT_SCRATCH_BYTES = 64 << 20
+
+
+def kda_chunk_fwd_split_noalloc(q, k, v, g_raw, beta, init_state=None, cu_seqlens=None, *,
+                                segment_tokens: int, out, final_state=None, g_min: float = -5.0,
+                                A_log=None, scale: float = 1.0, gate_mode: str = "bounded",
+                                gate_per_head: bool = False, stream=None):
+    """kda_chunk_fwd_split with the scratch inside the library (no device
+    allocation: neither here nor in the library).  For callers that cannot
+    allocate device memory, e.g. a process whose memory belongs to its own
+    caching pool.  ``out`` (and ``final_state``, if wanted) must be given;
+    sizes needing more than SPLIT_SCRATCH_BYTES of scratch raise KdaError
+    KDA_ERR_SCRATCH.  Calls on one device share the buffer: keep them ordered
+    on one stream.  Returns (out, final_state)."""
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("kda_chunk_fwd_split_noalloc runs on CUDA tensors only")
+    dt = q.dtype
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    for nm, t, shp in (("q", q, (B, T, H, dk)), ("k", k, (B, T, H, dk)),
+                       ("v", v, (B, T, H, dv)), ("beta", beta, (B, T, H)), ("out", out, (B, T, H, dv))):
+        _check(t, nm, shp, dt, dev)
+    _check_gate(g_raw, (B, T, H), dk, dt, dev, gate_mode, gate_per_head)
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if cu_seqlens is not None and (cu_seqlens.dtype != torch.int32 or cu_seqlens.device != dev):
+        raise ValueError("cu_seqlens must be an int32 tensor on the inputs' device")
+    if init_state is not None:
+        _check(init_state, "init_state", (N, H, dk, dv), torch.float32, dev)
+    if final_state is not None:
+        _check(final_state, "final_state", (N, H, dk, dv), torch.float32, dev)
+    if A_log is not None:
+        _check(A_log, "A_log", (H,), torch.float32, dev)
+    prm = _params(g_min, A_log, scale, gate_mode, gate_per_head)
+    st = lib.kda_chunk_fwd_split_noalloc(_dtype_code(q), B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v),
+                                         _ptr(g_raw), _ptr(beta), _ptr(init_state),
+                                         _ptr(cu_seqlens), N, int(segment_tokens), _ptr(out),
+                                         _ptr(final_state), ctypes.byref(prm),
+                                         _stream_handle(dev, stream))
+    if st != 0:
+        _raise(lib, "kda_chunk_fwd_split_noalloc", st)
     return out, final_state
 
 

@@ -51,7 +51,9 @@ typedef enum {
     KDA_ERR_SHAPE = 3,   /* unsupported dk/dv                                */
     KDA_ERR_ALIGN = 4,   /* pointer not 16-byte aligned                      */
     KDA_ERR_LAUNCH = 5,  /* CUDA rejected the launch (see kda_last_cuda_error) */
-    KDA_ERR_TIMEOUT = 6  /* reserved: a bounded device wait gave up          */
+    KDA_ERR_TIMEOUT = 6, /* reserved: a bounded device wait gave up          */
+    KDA_ERR_SCRATCH = 7  /* kda_chunk_fwd_split_noalloc: the call needs more
+                            than KDA_SPLIT_SCRATCH_BYTES of scratch          */
 } kda_status;
 
 typedef enum {
@@ -211,6 +213,41 @@ kda_status kda_chunk_fwd_split(kda_dtype dt, int B, int T, int H, int dk, int dv
                                void *out, float *final_state,
                                void *workspace, unsigned long long workspace_bytes,
                                const kda_params *p, kda_stream_t stream);
+
+/*
+ * kda_chunk_fwd_split_noalloc -- kda_chunk_fwd_split for callers that must
+ * not allocate device memory: a process whose device memory is all handed
+ * to its own caching pool, so that a cudaMalloc behind the pool's back can
+ * fail or fragment it, or a plain C caller that has no device allocator of
+ * its own.  The pages have no counterpart of this call: it is a packaging
+ * of the segment split, not part of the method.
+ *
+ * Arguments, results and errors as kda_chunk_fwd_split without workspace:
+ * the scratch is a buffer inside the library, KDA_SPLIT_SCRATCH_BYTES
+ * (64 MiB) of device memory that every GPU which loads the library holds
+ * until the process exits.  Sizes whose kda_chunk_fwd_split_workspace(...)
+ * exceeds it return KDA_ERR_SCRATCH and enqueue nothing (for example 2
+ * heads x 8192 tokens with 512-token segments need about 25 MiB; 96 heads x
+ * 8192 tokens do not fit).  The caller still provides q, k, v, g_raw, beta,
+ * init_state, out and final_state; nothing is allocated (no cudaMalloc,
+ * cudaFree or allocating library call).
+ *
+ * The first call on a device looks up the buffer's device address (once
+ * per device, with that device current); make that first call before any
+ * stream capture.  Every call on a device shares the one buffer and leaves
+ * its contents behind; each call writes every part of it that it reads, so
+ * nothing has to start at zero.  Two calls whose work overlaps on the GPU
+ * (different streams without ordering, or different host threads) race on
+ * the buffer and produce wrong results: order them on one stream.
+ */
+#define KDA_SPLIT_SCRATCH_BYTES (64ull << 20)
+kda_status kda_chunk_fwd_split_noalloc(kda_dtype dt, int B, int T, int H, int dk, int dv,
+                                       const void *q, const void *k, const void *v,
+                                       const void *g_raw, const void *beta,
+                                       const float *init_state,
+                                       const int32_t *cu_seqlens, int N, int segment_tokens,
+                                       void *out, float *final_state,
+                                       const kda_params *p, kda_stream_t stream);
 
 /*
  * kda_chunk_fwd_split_workspace -- bytes of workspace kda_chunk_fwd_split
