@@ -88,7 +88,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "spec", "prep", "post"],
+    ap.add_argument("--only", choices=["all", "prefill", "split", "decode", "spec", "prep", "post"],
                     default="all",
                     help="run one leg only (for profiling captures; the JSON line needs 'all')")
     ap.add_argument("--prefill-workload", default="varlen_bf16_H96_237568",
@@ -295,6 +295,17 @@ def run_single_leg(args, kda, dev):
         a = [inp[n] for n in ("q", "k", "v", "g_raw", "beta")]
         out, fin = kda.kda_chunk_fwd(*a, inp["init_state"], inp["cu_seqlens"])
         fn = lambda i: kda.kda_chunk_fwd(*a, inp["init_state"], inp["cu_seqlens"], out=out, final_state=fin)
+    elif args.only == "split":
+        w = kin.WORKLOADS["tp8_bf16_H12_T131072"]
+        inp = kin.make_prefill_inputs(w, device=dev)
+        a = [inp[n] for n in ("q", "k", "v", "g_raw", "beta")]
+        tau = kda.split_segment_tokens(w.B, w.T, w.H, w.B, False,
+                                       torch.cuda.get_device_properties(dev).multi_processor_count)
+        ws = torch.empty(kda.split_workspace_bytes(w.B, w.T, w.H, w.dk, w.dv, w.B, tau),
+                         dtype=torch.uint8, device=dev)
+        out, fin = kda.kda_chunk_fwd_split(*a, None, None, segment_tokens=tau, workspace=ws)
+        fn = lambda i: kda.kda_chunk_fwd_split(*a, None, None, segment_tokens=tau, workspace=ws,
+                                               out=out, final_state=fin)
     elif args.only == "decode":
         w = DECODE
         S = kin.make_decode_state(w, device=dev)
