@@ -26,7 +26,8 @@
 // dv columns, combining the two reductions over c across warps through
 // shared memory; decode_kernel, the multi-token replay, over one dv/CS-column
 // slab per CTA with one cross-warp reduction per token.  The replay's
-// per-token channel vectors (alpha k, alpha q) and (alpha, k), v, beta and
+// per-token channel vectors (alpha k, alpha q) and (alpha, k) (8-byte pairs,
+// one load per row, widened to the packed two-lane form in registers), v, beta and
 // k.q are computed for a block of up to 8 tokens at once into shared memory,
 // with their loads in flight beside the state's (bf16 drafts are first
 // staged into shared memory by cp.async).
@@ -158,8 +159,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode1_kernel(DecodeArgs a
 
 template <int DK, int DVS>
 struct DecodeSmem {
-    ulonglong2 akq[kTokBlock][DK];     // pairs (alpha k, alpha k), (alpha q, alpha q) per token and channel
-    ulonglong2 alk[kTokBlock][DK];     // pairs (alpha, alpha), (k, k)
+    float2 akq[kTokBlock][DK];         // (alpha k, alpha q) per token and channel
+    float2 alk[kTokBlock][DK];         // (alpha, k)
     float red[2][kDecodeThreads / (DVS / 4)][DVS];    // [a|b][row group][slab column]
     float4 u[DVS / 4];
     float v[kTokBlock][DVS];
@@ -271,8 +272,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2 * CS) decode_kernel(DecodeAr
                 zc = a.gate_mode == KDA_GATE_NONE ? 0.f : ld_in(gz + og);
             }
             const float alpha = expf(gate_log_decay(a.gate_mode, zc, escale, a.g_min));
-            sm.akq[i][c] = make_ulonglong2(pack2(alpha * kc, alpha * kc), pack2(alpha * qc, alpha * qc));
-            sm.alk[i][c] = make_ulonglong2(pack2(alpha, alpha), pack2(kc, kc));
+            sm.akq[i][c] = make_float2(alpha * kc, alpha * qc);
+            sm.alk[i][c] = make_float2(alpha, kc);
             float kq = kc * qc;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
@@ -317,10 +318,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 2 * CS) decode_kernel(DecodeAr
             // partial a_j = sum_c alpha_c k_c S_cj and b_j = sum_c alpha_c q_c S_cj over this thread's rows
             f32x2 pa0 = 0ull, pa1 = 0ull, pb0 = 0ull, pb1 = 0ull;     // +0.0f in both lanes
 #pragma unroll
-            for (int m = 0; m < RPL; ++m) {
-                const ulonglong2 ch = sm.akq[i][rg + m * RPP];
-                pa0 = ffma2(ch.x, st[m][0], pa0); pa1 = ffma2(ch.x, st[m][1], pa1);
-                pb0 = ffma2(ch.y, st[m][0], pb0); pb1 = ffma2(ch.y, st[m][1], pb1);
+            for (int m = 0; m < RPL; ++m) {   // one 8-byte load per row; the pairs are built in registers
+                const float2 ch = sm.akq[i][rg + m * RPP];
+                const f32x2 ak = pack2(ch.x, ch.x), aq = pack2(ch.y, ch.y);
+                pa0 = ffma2(ak, st[m][0], pa0); pa1 = ffma2(ak, st[m][1], pa1);
+                pb0 = ffma2(aq, st[m][0], pb0); pb1 = ffma2(aq, st[m][1], pb1);
             }
             {
                 const float2 a0 = unpack2(pa0), a1 = unpack2(pa1), b0 = unpack2(pb0), b1 = unpack2(pb1);
@@ -350,9 +352,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2 * CS) decode_kernel(DecodeAr
             const f32x2 u0 = pack2(u.x, u.y), u1 = pack2(u.z, u.w);
 #pragma unroll
             for (int m = 0; m < RPL; ++m) {
-                const ulonglong2 ch = sm.alk[i][rg + m * RPP];
-                st[m][0] = ffma2(ch.x, st[m][0], fmul2(ch.y, u0));
-                st[m][1] = ffma2(ch.x, st[m][1], fmul2(ch.y, u1));
+                const float2 ch = sm.alk[i][rg + m * RPP];
+                const f32x2 al = pack2(ch.x, ch.x), kk = pack2(ch.y, ch.y);
+                st[m][0] = ffma2(al, st[m][0], fmul2(kk, u0));
+                st[m][1] = ffma2(al, st[m][1], fmul2(kk, u1));
             }
         }
     }
