@@ -442,8 +442,9 @@ def run_ours(args, rank, world, local):
     # burst cuBLAS figure is its denominator, not the seconds-long sustained one
     tc_peak = float(peaks["bf16_tflops"])
     kernel_name = kda.chunk_fwd_kernel(torch.bfloat16, pw.dk, pw.dv)
-    prefill_src = source_hash("kda_prefill_tc.cu" if kernel_name == "prefill_tc_kernel"
-                              else "kda_prefill_simt.cu", "kda_internal.cuh", "kda_sm100.cuh")
+    prefill_src = (source_hash("kda_prefill_tc.cu", "kda_internal.cuh", "kda_sm100.cuh", "kda_tc_util.cuh")
+                   if kernel_name == "prefill_tc_kernel"
+                   else source_hash("kda_prefill_simt.cu", "kda_internal.cuh", "kda_sm100.cuh"))
     decode_src = source_hash("kda_decode.cu", "kda_internal.cuh")
     p_traffic = recorded_traffic("prefill", prefill_src)
     d_traffic = recorded_traffic("decode", decode_src)
