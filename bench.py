@@ -91,6 +91,8 @@ def parse():
     ap.add_argument("--only", choices=["all", "prefill", "split", "decode", "spec", "prep", "post"],
                     default="all",
                     help="run one leg only (for profiling captures; the JSON line needs 'all')")
+    ap.add_argument("--prep-tokens", type=int, default=0,
+                    help="--only prep/post: the first N tokens of the workload (profiling captures); 0 = all")
     ap.add_argument("--prefill-workload", default="varlen_bf16_H96_237568",
                     choices=[k for k, w in kin.WORKLOADS.items() if w.kind == "prefill" and w.dtype == "bf16"],
                     help="prefill workload (profiling captures use the smaller layer-shaped one)")
@@ -313,8 +315,10 @@ def run_single_leg(args, kda, dev):
         fn = lambda i: kda.kda_decode_step(t["q"], t["k"], t["v"], t["g_raw"], t["beta"], S)
     elif args.only == "prep":
         w = PREFILL
-        pi = kin.make_prep_inputs(w.total_tokens, w.H, w.dk, "bf16", device=dev)
-        cu = torch.tensor([0] + list(itertools.accumulate(w.seqlens)), dtype=torch.int32, device=dev)
+        ntok = min(args.prep_tokens or w.total_tokens, w.total_tokens)
+        pi = kin.make_prep_inputs(ntok, w.H, w.dk, "bf16", device=dev)
+        bounds = [min(b, ntok) for b in itertools.accumulate(w.seqlens)]
+        cu = torch.tensor([0] + bounds, dtype=torch.int32, device=dev)
         fn = lambda i: kda.kda_qkv_prep(pi["x_qkv"], pi["conv_w"], pi["beta_logit"], cu)
     elif args.only == "post":
         w = PREFILL
