@@ -131,21 +131,37 @@ __global__ void __launch_bounds__(256) split_compose_kernel(SplitArgs a) {
         float *keep = slot(a.s_in, base + p);
         for (int i = tid; i < D * D / 4; i += 256)
             reinterpret_cast<float4 *>(keep)[i] = reinterpret_cast<const float4 *>(sin_)[i];
-        const float *phi = slot(a.states, base + P + p - 1);
-        for (int i = tid; i < D * D; i += 256) {
-            const int r = i >> 7, c = i & 127;
-            phiT[c * CPAD + r] = phi[i];
+        // Phi as 16 float4 per thread, all requested before the first is used:
+        // chunk i = tid + 256 k is row i & 127, columns 4 (i >> 7) .., so a
+        // warp's lanes hold 32 consecutive rows and its transposed stores
+        // below fall in 32 distinct banks
+        const float4 *phi = reinterpret_cast<const float4 *>(slot(a.states, base + P + p - 1));
+        const float *s0 = slot(a.states, base + p);
+        float acc[8][8];
+        {
+            float4 x[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int i = tid + 256 * k;
+                x[k] = phi[(i & 127) * (D / 4) + (i >> 7)];
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 lo = *reinterpret_cast<const float4 *>(s0 + (r0 + i) * D + j0);
+                const float4 hi = *reinterpret_cast<const float4 *>(s0 + (r0 + i) * D + j0 + 4);
+                acc[i][0] = lo.x; acc[i][1] = lo.y; acc[i][2] = lo.z; acc[i][3] = lo.w;
+                acc[i][4] = hi.x; acc[i][5] = hi.y; acc[i][6] = hi.z; acc[i][7] = hi.w;
+            }
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int i = tid + 256 * k, r = i & 127, c = (i >> 7) * 4;
+                phiT[(c + 0) * CPAD + r] = x[k].x;
+                phiT[(c + 1) * CPAD + r] = x[k].y;
+                phiT[(c + 2) * CPAD + r] = x[k].z;
+                phiT[(c + 3) * CPAD + r] = x[k].w;
+            }
         }
         __syncthreads();
-        float acc[8][8];
-        const float *s0 = slot(a.states, base + p);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 lo = *reinterpret_cast<const float4 *>(s0 + (r0 + i) * D + j0);
-            const float4 hi = *reinterpret_cast<const float4 *>(s0 + (r0 + i) * D + j0 + 4);
-            acc[i][0] = lo.x; acc[i][1] = lo.y; acc[i][2] = lo.z; acc[i][3] = lo.w;
-            acc[i][4] = hi.x; acc[i][5] = hi.y; acc[i][6] = hi.z; acc[i][7] = hi.w;
-        }
 #pragma unroll 2
         for (int c = 0; c < D; ++c) {
             const float4 pa = *reinterpret_cast<const float4 *>(phiT + c * CPAD + r0);
