@@ -17,7 +17,8 @@
  * Conventions for every entry point:
  *   - All tensor arguments are DEVICE pointers owned by the caller; the
  *     library allocates no device or host memory and keeps no pointer after
- *     the call returns.
+ *     the call returns (kda_chunk_fwd_split takes a caller workspace;
+ *     kda_chunk_fwd_split_noalloc uses a fixed buffer inside the library).
  *   - Every call is asynchronous on the given stream (0 = legacy default
  *     stream).  A KDA_OK return means the work was validated and enqueued.
  *   - Tensors are dense and row-major ("contiguous") in the stated shape.
