@@ -312,6 +312,101 @@ kda_status kda_chunk_fwd_split(kda_dtype dt, int B, int T, int H, int dk, int dv
     return from_cuda(kda::launch_split_fixup(sa, s));
 }
 
+// ---------------------------------------------------------------- sequence split across ranks
+namespace {
+struct KcpLayout {
+    size_t vseg, s_in, out_trans, out_zero, bytes;
+};
+KcpLayout kcp_layout(int B, int T, int H) {
+    const size_t rows = static_cast<size_t>(B) * T * H * 128 * sizeof(float);
+    KcpLayout l;
+    l.vseg = 0;
+    l.s_in = round_up(static_cast<size_t>(2) * B * 16);
+    l.out_trans = round_up(l.s_in + static_cast<size_t>(B) * H * 128 * 128 * sizeof(float));
+    l.out_zero = round_up(l.out_trans + rows);
+    l.bytes = round_up(l.out_zero + rows);
+    return l;
+}
+bool kcp_sizes_ok(int B, int T, int H, int dk, int dv) {
+    return B >= 1 && T >= 1 && H >= 1 && H <= 65535 && dk == 128 && dv == 128 &&
+           static_cast<long long>(B) * T <= INT32_MAX && 2LL * B * H <= INT32_MAX;
+}
+kda::KcpArgs kcp_args(int B, int T, int H, void *workspace) {
+    const KcpLayout l = kcp_layout(B, T, H);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    kda::KcpArgs k{};
+    k.B = B;
+    k.T = T;
+    k.H = H;
+    k.vseg = reinterpret_cast<int4 *>(ws + l.vseg);
+    k.s_in = reinterpret_cast<float *>(ws + l.s_in);
+    k.out_trans = reinterpret_cast<float *>(ws + l.out_trans);
+    k.out_zero = reinterpret_cast<float *>(ws + l.out_zero);
+    return k;
+}
+}  // namespace
+
+unsigned long long kda_chunk_fwd_kcp_workspace(int B, int T, int H, int dk, int dv) {
+    return kcp_sizes_ok(B, T, H, dk, dv) ? kcp_layout(B, T, H).bytes : 0;
+}
+
+kda_status kda_chunk_fwd_kcp_part(kda_dtype dt, int B, int T, int H, int dk, int dv,
+                                  const void *q, const void *k, const void *v,
+                                  const void *g_raw, const void *beta,
+                                  float *pair_out, void *workspace, unsigned long long workspace_bytes,
+                                  const kda_params *p, kda_stream_t stream) {
+    if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_DTYPE;
+    if (B < 0 || T < 0 || H <= 0) return KDA_ERR_ARG;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv) || !kda::prefill_tc_supported(dt, dk, dv)) return KDA_ERR_SHAPE;
+    if (!kcp_sizes_ok(B, T, H, dk, dv)) return KDA_ERR_ARG;
+    const long long total = static_cast<long long>(B) * T;
+    if (!pair_out || !workspace || !q || !k || !v || !beta) return KDA_ERR_ARG;
+    const void *ptrs[] = {q, k, v, pair_out};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return KDA_ERR_ALIGN;
+    if (!aligned_to(workspace, kSplitAlign) || !aligned_to(beta, 2)) return KDA_ERR_ALIGN;
+    if (const kda_status gs = check_gate(p, dt, g_raw, true)) return gs;
+    if (workspace_bytes < kcp_layout(B, T, H).bytes) return KDA_ERR_ARG;
+    kda::KcpArgs ka = kcp_args(B, T, H, workspace);
+    kda::PrefillArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g_raw; a.beta = beta;
+    // every virtual sequence writes fp32 rows (out_zero / out_trans), so the
+    // bf16 output map is never stored through; it describes a valid region
+    a.out = ka.out_zero;
+    a.final_state = pair_out;    // slot 2n + w of [B, 2, H, d, d]: w = 0 zero-state run, 1 transition
+    resolve_params(p, a.g_min, a.A_log, a.scale, a.gate_mode, a.gate_scalar);
+    if (a.A_log && !aligned_to(a.A_log, 4)) return KDA_ERR_ALIGN;
+    a.N = 2 * B;
+    a.H = H;
+    a.T_total = static_cast<int>(total);
+    a.T_seq = T;
+    a.vseg = ka.vseg;
+    a.out_trans = ka.out_trans;
+    a.out_zero = ka.out_zero;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (const kda_status st = from_cuda(kda::launch_kcp_plan(ka, s))) return st;
+    return from_cuda(kda::launch_prefill_tc(a, s));
+}
+
+kda_status kda_chunk_fwd_kcp_finish(int B, int T, int H, int dk, int dv, int rank,
+                                    const float *pairs, void *out, float *final_state,
+                                    void *workspace, unsigned long long workspace_bytes,
+                                    kda_stream_t stream) {
+    if (!kcp_sizes_ok(B, T, H, dk, dv) || rank < 1) return dk == 128 && dv == 128 ? KDA_ERR_ARG : KDA_ERR_SHAPE;
+    if (!pairs || !workspace || !out) return KDA_ERR_ARG;
+    const void *ptrs[] = {pairs, out, final_state};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return KDA_ERR_ALIGN;
+    if (!aligned_to(workspace, kSplitAlign)) return KDA_ERR_ALIGN;
+    if (workspace_bytes < kcp_layout(B, T, H).bytes) return KDA_ERR_ARG;
+    kda::KcpArgs ka = kcp_args(B, T, H, workspace);
+    ka.rank = rank;
+    ka.pairs = pairs;
+    ka.out = out;
+    ka.final_state = final_state;
+    return from_cuda(kda::launch_kcp_finish(ka, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kda_status kda_decode_steps(kda_dtype dt, int N, int K, int H, int dk, int dv,
                             const void *q, const void *k, const void *v,
                             const void *g_raw, const void *beta, const int32_t *accepted,

@@ -193,6 +193,20 @@ struct SplitArgs {
     float *final_state;   // [N, H, d, d] or nullptr
 };
 cudaError_t launch_split_plan(const SplitArgs &a, cudaStream_t s);
+
+// Sequence split across ranks (kda_chunk_fwd_kcp_part / _finish): B
+// sequences of T tokens on this rank; workspace: vseg [2B] int4, s_in
+// [B, H, d, d] fp32, out_trans, out_zero [B T, H, d] fp32.
+struct KcpArgs {
+    int B, T, H, rank;
+    int4 *vseg;
+    float *s_in, *out_trans, *out_zero;
+    const float *pairs;   // [rank + 1, B, 2, H, d, d]
+    void *out;            // [B T, H, d] bf16
+    float *final_state;   // [B, H, d, d] or nullptr
+};
+cudaError_t launch_kcp_plan(const KcpArgs &a, cudaStream_t s);
+cudaError_t launch_kcp_finish(const KcpArgs &a, cudaStream_t s);
 cudaError_t launch_split_compose(const SplitArgs &a, cudaStream_t s);
 cudaError_t launch_split_fixup(const SplitArgs &a, cudaStream_t s);
 

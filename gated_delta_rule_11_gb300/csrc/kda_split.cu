@@ -105,38 +105,34 @@ __global__ void __launch_bounds__(1024) split_plan_kernel(SplitArgs a) {
     for (int i = total + tid; i < a.nv_max; i += 1024) a.vseg[i] = make_int4(0, 0, VSEG_EMPTY, 0);
 }
 
-// One CTA per (sequence, head), 256 threads, each an 8 x 8 block of the
-// 128 x 128 product.  Shared memory: Phi^T (row stride 132) and S_in.
+// State composition over one (sequence, head): S = s_first, then for
+// p = 1 .. P - 1: keep_of(p) <- S (the state entering segment p, when the
+// pointer is set), S <- phi_of(p) S + s0_of(p); final <- S (when set).  One
+// CTA of 256 threads, each an 8 x 8 block of the 128 x 128 product; shared
+// memory: Phi^T (row stride 132) and S.
 constexpr int CPAD = 132;
 constexpr int COMPOSE_SMEM = (D * CPAD + D * D) * 4;
 
-__global__ void __launch_bounds__(256) split_compose_kernel(SplitArgs a) {
-    extern __shared__ float csm[];
+template <typename PhiOf, typename S0Of, typename KeepOf>
+__device__ __forceinline__ void compose_chain(float *csm, int P, const float *s_first, PhiOf phi_of, S0Of s0_of,
+                                              KeepOf keep_of, float *final_out) {
     float *phiT = csm;              // phiT[c][r] = Phi[r][c]
-    float *sin_ = csm + D * CPAD;   // S_in[c][j]
-    const int n = blockIdx.x / a.H, h = blockIdx.x % a.H;
+    float *sin_ = csm + D * CPAD;   // S[c][j]
     const int tid = threadIdx.x;
-    const int2 st = a.seqtab[n];
-    const int base = st.x, P = st.y;
-    const size_t hs = static_cast<size_t>(D) * D;
-    auto slot = [&](float *buf, int v) { return buf + (static_cast<size_t>(v) * a.H + h) * hs; };
     const int r0 = (tid >> 4) * 8, j0 = (tid & 15) * 8;
-    // S_in of segment 1 = final state of segment 0
-    const float *cur = slot(a.states, base);
     for (int i = tid; i < D * D / 4; i += 256)
-        reinterpret_cast<float4 *>(sin_)[i] = reinterpret_cast<const float4 *>(cur)[i];
+        reinterpret_cast<float4 *>(sin_)[i] = reinterpret_cast<const float4 *>(s_first)[i];
     __syncthreads();
     for (int p = 1; p < P; ++p) {
-        // keep the entering state of segment p for the output fixup
-        float *keep = slot(a.s_in, base + p);
-        for (int i = tid; i < D * D / 4; i += 256)
-            reinterpret_cast<float4 *>(keep)[i] = reinterpret_cast<const float4 *>(sin_)[i];
+        if (float *keep = keep_of(p))
+            for (int i = tid; i < D * D / 4; i += 256)
+                reinterpret_cast<float4 *>(keep)[i] = reinterpret_cast<const float4 *>(sin_)[i];
         // Phi as 16 float4 per thread, all requested before the first is used:
         // chunk i = tid + 256 k is row i & 127, columns 4 (i >> 7) .., so a
         // warp's lanes hold 32 consecutive rows and its transposed stores
         // below fall in 32 distinct banks
-        const float4 *phi = reinterpret_cast<const float4 *>(slot(a.states, base + P + p - 1));
-        const float *s0 = slot(a.states, base + p);
+        const float4 *phi = reinterpret_cast<const float4 *>(phi_of(p));
+        const float *s0 = s0_of(p);
         float acc[8][8];
         {
             float4 x[16];
@@ -175,7 +171,7 @@ __global__ void __launch_bounds__(256) split_compose_kernel(SplitArgs a) {
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) acc[i][jj] = fmaf(pr[i], sr[jj], acc[i][jj]);
         }
-        __syncthreads();   // every thread has read S_in and Phi^T
+        __syncthreads();   // every thread has read S and Phi^T
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             *reinterpret_cast<float4 *>(sin_ + (r0 + i) * D + j0) =
@@ -185,53 +181,56 @@ __global__ void __launch_bounds__(256) split_compose_kernel(SplitArgs a) {
         }
         __syncthreads();
     }
-    if (a.final_state) {
-        float *fs = a.final_state + (static_cast<size_t>(n) * a.H + h) * hs;
+    if (final_out)
         for (int i = tid; i < D * D / 4; i += 256)
-            reinterpret_cast<float4 *>(fs)[i] = reinterpret_cast<const float4 *>(sin_)[i];
-    }
+            reinterpret_cast<float4 *>(final_out)[i] = reinterpret_cast<const float4 *>(sin_)[i];
 }
 
-// o_t = o0_t + S_in^T R_t over the rows of one segment: CTA (virtual index,
-// chunk, head) takes FIX_TOKENS tokens of a transition run's segment, 64 at
+__global__ void __launch_bounds__(256) split_compose_kernel(SplitArgs a) {
+    extern __shared__ float csm[];
+    const int n = blockIdx.x / a.H, h = blockIdx.x % a.H;
+    const int2 st = a.seqtab[n];
+    const int base = st.x, P = st.y;
+    const size_t hs = static_cast<size_t>(D) * D;
+    auto slot = [&](float *buf, int v) { return buf + (static_cast<size_t>(v) * a.H + h) * hs; };
+    // segment p's run from zero is virtual sequence base + p, its transition
+    // run base + P + p - 1; segment 0's run (from the given state) ends in
+    // the state entering segment 1
+    compose_chain(csm, P, slot(a.states, base), [&](int p) { return slot(a.states, base + P + p - 1); },
+                  [&](int p) { return slot(a.states, base + p); }, [&](int p) { return slot(a.s_in, base + p); },
+                  a.final_state ? a.final_state + (static_cast<size_t>(n) * a.H + h) * hs : nullptr);
+}
+
+// o_t = o0_t + S_in^T R_t over tokens [t_first, t_end) of head h: 64 rows at
 // a time.  S_in (fp32) is held as fp16 B fragments in shared memory, laid out
 // [j][c] (row stride 136 halves, conflict-free); R (fp32) is staged as fp16
 // [t][c] (same stride), the next 64 rows loaded into registers while the
 // current ones are multiplied.  Warp w computes rows 16 (w & 3) .. +16 and
 // columns 64 (w >> 2) .. +64 of the 64 x 128 update with m16n8k16 fp16
-// products.
+// products.  Rows are [token][H][128] in R, O0 and O.
 constexpr int FIX_TOKENS = 1024;
 constexpr int HSTR = 136;
 constexpr int FIX_SMEM = (D * HSTR + 64 * HSTR) * 2;
 
-__global__ void __launch_bounds__(256) split_fixup_kernel(SplitArgs a) {
-    extern __shared__ __align__(16) __half fsm[];
+__device__ __forceinline__ void fixup_span(__half *fsm, int t_first, int t_end, int h, int H, const float *sin_,
+                                           const float *R, const float *O0, __nv_bfloat16 *O) {
     __half *sT = fsm;              // sT[j][c] = S_in[c][j]
     __half *rs = fsm + D * HSTR;   // rs[t][c] = R[t][c]
-    const int vi = blockIdx.x, h = blockIdx.z;
-    const int4 e = a.vseg[vi];
-    if (!(e.z & VSEG_OUT_TRANS)) return;   // one CTA row per transition run
-    const int t_first = e.x + blockIdx.y * FIX_TOKENS;
-    const int t_end = min(e.y, t_first + FIX_TOKENS);
-    if (t_first >= t_end) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const float *R = a.out_trans, *O0 = a.out_zero;
-    __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(a.out);
     // rows t0 .. t0 + 63 of R: thread tid holds float4 chunks i = tid + 256 k
-    // (row i >> 5, channels 4 (i & 31) ..), zero past the segment
+    // (row i >> 5, channels 4 (i & 31) ..), zero past the span
     float4 nxt[8];
     auto load_r = [&](int t0) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int i = tid + 256 * k, t = t0 + (i >> 5);
-            nxt[k] = t < t_end ? *reinterpret_cast<const float4 *>(R + (static_cast<size_t>(t) * a.H + h) * D +
+            nxt[k] = t < t_end ? *reinterpret_cast<const float4 *>(R + (static_cast<size_t>(t) * H + h) * D +
                                                                     (i & 31) * 4)
                                : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     };
     load_r(t_first);
     {   // S_in^T as fp16: thread tid converts float4 chunks (row c, columns 4 m ..)
-        const float *sin_ = a.s_in + (static_cast<size_t>(e.w) * a.H + h) * D * D;
         float4 x[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) x[k] = reinterpret_cast<const float4 *>(sin_)[tid + 256 * k];
@@ -261,7 +260,7 @@ __global__ void __launch_bounds__(256) split_fixup_kernel(SplitArgs a) {
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
             const int t = min(t0 + m0 + g + 8 * hr, t_end - 1);
-            const size_t row = (static_cast<size_t>(t) * a.H + h) * D;
+            const size_t row = (static_cast<size_t>(t) * H + h) * D;
 #pragma unroll
             for (int nb = 0; nb < 8; ++nb)
                 o0[hr][nb] = *reinterpret_cast<const float2 *>(O0 + row + n0 + 8 * nb + 2 * tq);
@@ -290,7 +289,7 @@ __global__ void __launch_bounds__(256) split_fixup_kernel(SplitArgs a) {
         for (int hr = 0; hr < 2; ++hr) {
             const int t = t0 + m0 + g + 8 * hr;
             if (t >= t_end) continue;
-            __nv_bfloat16 *orow = O + (static_cast<size_t>(t) * a.H + h) * D;
+            __nv_bfloat16 *orow = O + (static_cast<size_t>(t) * H + h) * D;
 #pragma unroll
             for (int nb = 0; nb < 8; ++nb)
                 *reinterpret_cast<__nv_bfloat162 *>(orow + n0 + 8 * nb + 2 * tq) =
@@ -299,7 +298,83 @@ __global__ void __launch_bounds__(256) split_fixup_kernel(SplitArgs a) {
     }
 }
 
+// CTA (virtual index, chunk, head): FIX_TOKENS tokens of a transition run's segment.
+__global__ void __launch_bounds__(256) split_fixup_kernel(SplitArgs a) {
+    extern __shared__ __align__(16) __half fsm[];
+    const int vi = blockIdx.x, h = blockIdx.z;
+    const int4 e = a.vseg[vi];
+    if (!(e.z & VSEG_OUT_TRANS)) return;   // one CTA row per transition run
+    const int t_first = e.x + blockIdx.y * FIX_TOKENS;
+    const int t_end = min(e.y, t_first + FIX_TOKENS);
+    if (t_first >= t_end) return;
+    fixup_span(fsm, t_first, t_end, h, a.H, a.s_in + (static_cast<size_t>(e.w) * a.H + h) * D * D, a.out_trans,
+               a.out_zero, static_cast<__nv_bfloat16 *>(a.out));
+}
+
+// Sequence split across ranks (KCP): rank r >= 1 holds tokens of B
+// sequences of T tokens each; for each it runs the zero-state run (virtual
+// 2n) and the transition run (2n + 1) over its tokens.
+__global__ void __launch_bounds__(256) kcp_plan_kernel(KcpArgs a) {
+    for (int n = threadIdx.x; n < a.B; n += 256) {
+        a.vseg[2 * n] = make_int4(n * a.T, (n + 1) * a.T, VSEG_ZERO_INIT | VSEG_OUT_ZERO, n);
+        a.vseg[2 * n + 1] = make_int4(n * a.T, (n + 1) * a.T, VSEG_ZERO_V | VSEG_IDENT_INIT | VSEG_OUT_TRANS, n);
+    }
+}
+
+// One CTA per (sequence, head): the state entering rank r from the gathered
+// pairs of ranks 0 .. r ([r + 1, B, 2, H, d, d]: [.][.][0] the zero-state
+// run's final state (rank 0: its true final state), [.][.][1] the
+// transition), then this rank's final state.
+__global__ void __launch_bounds__(256) kcp_compose_kernel(KcpArgs a) {
+    extern __shared__ float csm[];
+    const int n = blockIdx.x / a.H, h = blockIdx.x % a.H;
+    const size_t hs = static_cast<size_t>(D) * D;
+    auto pair = [&](int rank, int which) {
+        return a.pairs + ((((static_cast<size_t>(rank) * a.B + n) * 2 + which) * a.H) + h) * hs;
+    };
+    float *keep = a.s_in + (static_cast<size_t>(n) * a.H + h) * hs;
+    compose_chain(csm, a.rank + 1, pair(0, 0), [&](int p) { return pair(p, 1); }, [&](int p) { return pair(p, 0); },
+                  [&](int p) { return p == a.rank ? keep : static_cast<float *>(nullptr); },
+                  a.final_state ? a.final_state + (static_cast<size_t>(n) * a.H + h) * hs : nullptr);
+}
+
+// CTA (sequence, chunk, head): FIX_TOKENS tokens of this rank's part of a sequence.
+__global__ void __launch_bounds__(256) kcp_fixup_kernel(KcpArgs a) {
+    extern __shared__ __align__(16) __half fsm[];
+    const int n = blockIdx.x, h = blockIdx.z;
+    const int t_first = n * a.T + blockIdx.y * FIX_TOKENS;
+    const int t_end = min((n + 1) * a.T, t_first + FIX_TOKENS);
+    if (t_first >= t_end) return;
+    fixup_span(fsm, t_first, t_end, h, a.H, a.s_in + (static_cast<size_t>(n) * a.H + h) * D * D, a.out_trans,
+               a.out_zero, static_cast<__nv_bfloat16 *>(a.out));
+}
+
 }  // namespace
+
+cudaError_t launch_kcp_plan(const KcpArgs &a, cudaStream_t s) {
+    kcp_plan_kernel<<<1, 256, 0, s>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
+
+cudaError_t launch_kcp_finish(const KcpArgs &a, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(kcp_compose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         COMPOSE_SMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kcp_fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FIX_SMEM);
+    if (e != cudaSuccess) return e;
+    kcp_compose_kernel<<<static_cast<unsigned>(a.B) * static_cast<unsigned>(a.H), 256, COMPOSE_SMEM, s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    count_launches(1);
+    const dim3 grid(static_cast<unsigned>(a.B), static_cast<unsigned>((a.T + FIX_TOKENS - 1) / FIX_TOKENS),
+                    static_cast<unsigned>(a.H));
+    kcp_fixup_kernel<<<grid, 256, FIX_SMEM, s>>>(a);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
 
 cudaError_t launch_split_plan(const SplitArgs &a, cudaStream_t s) {
     split_plan_kernel<<<1, 1024, 0, s>>>(a);

@@ -29,7 +29,8 @@ EXPORTED = ("kda_chunk_fwd", "kda_decode_step", "kda_status_str", "kda_last_cuda
             "kda_decode_steps", "kda_chunk_fwd_checkpointed", "kda_checkpoint_rows",
             "kda_qkv_prep", "kda_output_gate", "kda_selftest_bounded_wait",
             "kda_chunk_fwd_split", "kda_chunk_fwd_split_workspace", "kda_split_segment_tokens",
-            "kda_chunk_fwd_split_noalloc")
+            "kda_chunk_fwd_split_noalloc", "kda_chunk_fwd_kcp_workspace", "kda_chunk_fwd_kcp_part",
+            "kda_chunk_fwd_kcp_finish")
 
 
 class KdaError(RuntimeError):
@@ -81,6 +82,13 @@ def load_library(build_if_missing: bool = False):
         lib.kda_chunk_fwd_split.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, i, i,
                                             vp, vp, vp, ctypes.c_ulonglong,
                                             ctypes.POINTER(KdaParams), vp]
+        lib.kda_chunk_fwd_kcp_workspace.restype = ctypes.c_ulonglong
+        lib.kda_chunk_fwd_kcp_workspace.argtypes = [i, i, i, i, i]
+        lib.kda_chunk_fwd_kcp_part.restype = i
+        lib.kda_chunk_fwd_kcp_part.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp,
+                                               ctypes.c_ulonglong, ctypes.POINTER(KdaParams), vp]
+        lib.kda_chunk_fwd_kcp_finish.restype = i
+        lib.kda_chunk_fwd_kcp_finish.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, ctypes.c_ulonglong, vp]
         lib.kda_chunk_fwd_split_noalloc.restype = i
         lib.kda_chunk_fwd_split_noalloc.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, i,
                                                     i, vp, vp, ctypes.POINTER(KdaParams), vp]
@@ -317,6 +325,65 @@ def kda_chunk_fwd_split(q, k, v, g_raw, beta, init_state=None, cu_seqlens=None, 
                                      final_state, output_final_state, g_min, A_log, scale,
                                      stream, 0, None, 0, "kda_chunk_fwd_split", gate_mode,
                                      gate_per_head, split=(int(segment_tokens), workspace))
+    return out, final_state
+
+
+def kcp_workspace_bytes(B: int, T: int, H: int, dk: int, dv: int) -> int:
+    """Device workspace one rank needs for kda_chunk_fwd_kcp_part / _finish (0: rejected sizes)."""
+    return int(load_library().kda_chunk_fwd_kcp_workspace(int(B), int(T), int(H), int(dk), int(dv)))
+
+
+def kda_chunk_fwd_kcp_part(q, k, v, g_raw, beta, workspace, *, g_min: float = -5.0, A_log=None,
+                           scale: float = 1.0, gate_mode: str = "bounded", gate_per_head: bool = False,
+                           stream=None):
+    """A rank r >= 1's part of a sequence split across ranks: its tokens
+    (q, k, g_raw [B, T, H, 128], v [B, T, H, 128], beta [B, T, H], bf16) run
+    from a zero state and as the transition.  Returns the pair tensor
+    [B, 2, H, 128, 128] float32 ([:, 0] the zero-state final state, [:, 1]
+    the transition) to exchange with the other ranks; the workspace (uint8,
+    kcp_workspace_bytes) keeps the rows kda_chunk_fwd_kcp_finish needs."""
+    lib = load_library()
+    dev, dt = q.device, q.dtype
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    for nm, t, shp in (("q", q, (B, T, H, dk)), ("k", k, (B, T, H, dk)), ("v", v, (B, T, H, dv)),
+                       ("beta", beta, (B, T, H))):
+        _check(t, nm, shp, dt, dev)
+    _check_gate(g_raw, (B, T, H), dk, dt, dev, gate_mode, gate_per_head)
+    if A_log is not None:
+        _check(A_log, "A_log", (H,), torch.float32, dev)
+    need = kcp_workspace_bytes(B, T, H, dk, dv)
+    if workspace.device != dev or workspace.dtype != torch.uint8 or workspace.numel() < need:
+        raise ValueError(f"workspace must be a uint8 tensor of >= {need} bytes on {dev}")
+    pair = torch.empty((B, 2, H, dk, dk), dtype=torch.float32, device=dev)
+    prm = _params(g_min, A_log, scale, gate_mode, gate_per_head)
+    st = lib.kda_chunk_fwd_kcp_part(_dtype_code(q), B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw),
+                                    _ptr(beta), _ptr(pair), _ptr(workspace), workspace.numel(),
+                                    ctypes.byref(prm), _stream_handle(dev, stream))
+    if st != 0:
+        _raise(lib, "kda_chunk_fwd_kcp_part", st)
+    return pair
+
+
+def kda_chunk_fwd_kcp_finish(pairs, rank: int, workspace, B: int, T: int, H: int, *, dk: int = 128,
+                             dv: int = 128, out=None, final_state=None, stream=None):
+    """A rank r >= 1's outputs after the exchange: pairs [rank + 1, B, 2, H,
+    dk, dk] float32 on the device (entry [0][:, 0] is rank 0's final state).
+    Returns (out [B, T, H, dv] bf16, final_state [B, H, dk, dv] float32, the
+    state after this rank's tokens)."""
+    lib = load_library()
+    dev = workspace.device
+    _check(pairs, "pairs", (rank + 1, B, 2, H, dk, dk), torch.float32, dev)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device=dev)
+    _check(out, "out", (B, T, H, dv), torch.bfloat16, dev)
+    if final_state is None:
+        final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    _check(final_state, "final_state", (B, H, dk, dv), torch.float32, dev)
+    st = lib.kda_chunk_fwd_kcp_finish(B, T, H, dk, dv, int(rank), _ptr(pairs), _ptr(out), _ptr(final_state),
+                                      _ptr(workspace), workspace.numel(), _stream_handle(dev, stream))
+    if st != 0:
+        _raise(lib, "kda_chunk_fwd_kcp_finish", st)
     return out, final_state
 
 

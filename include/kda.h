@@ -251,6 +251,47 @@ kda_status kda_chunk_fwd_split_noalloc(kda_dtype dt, int B, int T, int H, int dk
                                        const kda_params *p, kda_stream_t stream);
 
 /*
+ * Sequence split across ranks (KCP: "Kimi K3：从三条信息流到完整系统",
+ * §FlashKDA 与 KCP, eq. (17)): each of R ranks holds the next T tokens of the
+ * same B sequences (rank 0 the first T).  Rank 0 runs kda_chunk_fwd from the
+ * sequences' initial states; its final states are its pair.  Every rank
+ * r >= 1 runs kda_chunk_fwd_kcp_part on its tokens, which yields its pair
+ * (S0, Phi): the final state of its tokens run from a zero state, and the
+ * transition Phi (its tokens run with v = 0 from the identity), so that the
+ * state after its tokens is Phi S_in + S0 for the state S_in entering them.
+ * The ranks exchange the pairs (an all-gather of B * 2 * H * dk * dk fp32
+ * values per rank; the caller does it, e.g. with torch.distributed), then
+ * every rank r >= 1 calls kda_chunk_fwd_kcp_finish with the pairs of ranks
+ * 0 .. r: it composes S_in of its tokens by eq. (17) (fp32) and writes its
+ * outputs o = o0 + S_in^T (Phi^T q) (rounded to bf16 once) and the state
+ * after its tokens (the last rank's is the sequences' final state).
+ * bf16 with dk = dv = 128 only (KDA_ERR_SHAPE otherwise); T >= 1.
+ *
+ * kda_chunk_fwd_kcp_workspace -- bytes of device workspace a rank needs
+ *   (the same buffer, untouched in between, for its _part and _finish
+ *   calls), or 0 for sizes the calls reject.  No GPU work.
+ * kda_chunk_fwd_kcp_part -- q, k, g_raw [B, T, H, dk], v [B, T, H, dv],
+ *   beta [B, T, H] (this rank's tokens, bf16); pair_out DEVICE fp32
+ *   [B, 2, H, dk, dk], 16-byte aligned: [n][0] = S0, [n][1] = Phi.  Gate
+ *   parameters as kda_chunk_fwd.  workspace 256-byte aligned.
+ * kda_chunk_fwd_kcp_finish -- rank >= 1; pairs DEVICE fp32
+ *   [rank + 1, B, 2, H, dk, dk] (entry [0][n][0] is rank 0's final state,
+ *   [0][n][1] is not read); out [B, T, H, dv] bf16; final_state
+ *   [B, H, dk, dv] fp32 or NULL.  Must follow the same rank's _part call on
+ *   the same workspace (stream order).
+ */
+unsigned long long kda_chunk_fwd_kcp_workspace(int B, int T, int H, int dk, int dv);
+kda_status kda_chunk_fwd_kcp_part(kda_dtype dt, int B, int T, int H, int dk, int dv,
+                                  const void *q, const void *k, const void *v,
+                                  const void *g_raw, const void *beta,
+                                  float *pair_out, void *workspace, unsigned long long workspace_bytes,
+                                  const kda_params *p, kda_stream_t stream);
+kda_status kda_chunk_fwd_kcp_finish(int B, int T, int H, int dk, int dv, int rank,
+                                    const float *pairs, void *out, float *final_state,
+                                    void *workspace, unsigned long long workspace_bytes,
+                                    kda_stream_t stream);
+
+/*
  * kda_chunk_fwd_split_workspace -- bytes of workspace kda_chunk_fwd_split
  * needs for these sizes (B * T tokens in all, N sequences), or 0 for
  * arguments it would reject.  No GPU work.
