@@ -32,9 +32,10 @@ struct PrefillArgs {
     // Segment split (tensor-core prefill only; ckpt unused): when vseg is
     // set, chain c runs the virtual sequence vseg[c / H] = {first token,
     // end token, VSEG_* flags, init source} instead of sequence c / H, and
-    // final_state has one slot per virtual chain.  out_trans / out_zero
-    // ([T_total, H, 128] fp32) receive the output rows of the chains flagged
-    // VSEG_OUT_TRANS / VSEG_OUT_ZERO, unrounded.
+    // final_state has one slot per virtual chain.  Every virtual chain
+    // writes its output rows unrounded, as fp32: to out_trans when flagged
+    // VSEG_OUT_TRANS, else to out_zero ([T_total, H, 128] each); out is not
+    // written.
     const int4 *vseg;
     float *out_trans, *out_zero;
 };
@@ -46,7 +47,9 @@ enum : int {
     VSEG_ZERO_V = 4,      // every value is zero (v is not read)
     VSEG_OUT_TRANS = 8,   // its output rows go to out_trans (fp32)
     VSEG_OUT_ZERO = 16,   // its output rows go to out_zero (fp32)
-    VSEG_EMPTY = 32       // no chain: the CTA exits at once
+    VSEG_EMPTY = 32,      // no chain: the CTA exits at once
+    VSEG_OUT_FINAL = 64   // its out_zero rows are the outputs themselves (a sequence's first
+                          // segment): the fixup only rounds them
 };
 
 // Decode: q, k, g_raw [N, K, H, dk]; v, out [N, K, H, dv]; beta [N, K, H];

@@ -159,7 +159,8 @@ template <bool Unbounded, bool Split>
 __global__ void __launch_bounds__(NTHREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_o, PrefillArgs a) {
+                  const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_ft,
+                  const __grid_constant__ CUtensorMap tm_fz, PrefillArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + OFF_BAR);
@@ -180,7 +181,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     } else {
         seq_span(a, n, bos, eos);
     }
-    const bool zero_v = (vflags & VSEG_ZERO_V) != 0;   // v = 0: the V tiles stay zero
+    // v = 0 (a transition run): the V loads address heads past H, so the
+    // whole box lies outside the tensor and TMA writes its zero fill (the
+    // transaction still counts the full box); no branch in the tile loop.
+    const int v_head = (vflags & VSEG_ZERO_V) ? h + a.H : h;
     const int ntiles = (eos - bos + C - 1) / C;
     const size_t state_off = static_cast<size_t>(chain) * D * D;
     // gate source: a TMA tile of per-channel inputs (eq. (5)), one input per
@@ -203,17 +207,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (zero_v) {   // no V is loaded: U = T Diag(beta) V reads these zeros
-        for (int i = tid; i < NS * 256; i += NTHREADS)
-            reinterpret_cast<uint4 *>(base + (i >> 8) * STAGE_BYTES + ST_V)[i & 255] = make_uint4(0, 0, 0, 0);
-        fence_proxy_async_smem();
-    }
     if (warp == 0) tmem_alloc(tmem_slot, TMEM_COLS);
     if (tid == 0) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         if (a.gate_mode != KDA_GATE_NONE && !a.gate_scalar) prefetch_tmap(&tm_z);
-        if (!zero_v) prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_o);
     }
     tc_fence_before();
@@ -594,15 +593,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const int ss = tt % NS;
             uint8_t *stg = base + ss * STAGE_BYTES;
             const int tok = bos + tt * C;
-            mbar_arrive_expect_tx(&bars[B_RAW + ss],
-                                  (z_tile ? TX_BYTES : TX_BYTES_NOZ) - (zero_v ? C * D * 2 : 0));
+            mbar_arrive_expect_tx(&bars[B_RAW + ss], z_tile ? TX_BYTES : TX_BYTES_NOZ);
             tma_load_3d(stg + ST_Q, &tm_q, &bars[B_RAW + ss], 0, h, tok);
             tma_load_3d(stg + ST_K, &tm_k, &bars[B_RAW + ss], 0, h, tok);
             if (z_tile) tma_load_3d(stg + ST_Z, &tm_z, &bars[B_RAW + ss], 0, h, tok);
-            if (!zero_v) {
-                tma_load_3d(stg + ST_V, &tm_v, &bars[B_RAW + ss], 0, h, tok);          // channels 0-63
-                tma_load_3d(stg + ST_V + 2048, &tm_v, &bars[B_RAW + ss], 64, h, tok);  // channels 64-127
-            }
+            tma_load_3d(stg + ST_V, &tm_v, &bars[B_RAW + ss], 0, v_head, tok);          // channels 0-63
+            tma_load_3d(stg + ST_V + 2048, &tm_v, &bars[B_RAW + ss], 64, v_head, tok);  // channels 64-127
         };
         constexpr int TMA_TID = 160, OST_TID = 192;  // lane 0 of chain warps 5 and 6
         int tma_next = 0;                            // (TMA thread) next tile to load
@@ -673,13 +669,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (tid == U_TID && ntiles > 0 && !issue_u(0)) note_timeout(abort_flag);
 
         __nv_bfloat16 *gout = static_cast<__nv_bfloat16 *>(a.out);
-        // fp32 rows of a segment-split run (no rounding, no staging)
-        float *fout = !Split ? nullptr
-                      : (vflags & VSEG_OUT_TRANS) ? a.out_trans : (vflags & VSEG_OUT_ZERO) ? a.out_zero : nullptr;
+        // every run of a segment split writes fp32 rows, unrounded, to
+        // out_trans or out_zero (by its flags; the same code for every run)
+        const bool f_trans = (vflags & VSEG_OUT_TRANS) != 0;
         uint8_t *ost = base + OFF_OST;
         // O of tile tt, rows [8 hf, 8 hf + 8): sum of the accumulators' columns
-        // 16..31.  Full tiles go to the staging tile (stored by TMA), a
-        // sequence's partial last tile straight to global memory.
+        // 16..31.  Full tiles go to a staging tile stored by TMA (bf16: two
+        // tiles, alternating; fp32: one tile, the whole staging area, free
+        // again before the next chain barrier), a sequence's partial last tile
+        // straight to global memory.
         auto read_out = [&](int tt) {
             const uint32_t eb = tmem + TM_E + E_BUF * static_cast<uint32_t>(tt & 1) + lane_base + 16 + 8 * hf;
             float o[8], x[NACC - 1][8];
@@ -696,8 +694,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
             const int tt0 = bos + tt * C;
             const int nvv = min(C, eos - tt0);
-            if (fout) {
-                float *op = fout + static_cast<size_t>(tt0 + 8 * hf) * a.H * D + static_cast<size_t>(h) * D + j;
+            if (Split && nvv == C) {
+                float *stg = reinterpret_cast<float *>(ost);
+#pragma unroll
+                for (int r = 0; r < 8; ++r) stg[(8 * hf + r) * D + j] = a.scale * o[r];
+                fence_proxy_async_smem();
+            } else if constexpr (Split) {
+                float *op = (f_trans ? a.out_trans : a.out_zero) + static_cast<size_t>(tt0 + 8 * hf) * a.H * D + static_cast<size_t>(h) * D + j;
 #pragma unroll
                 for (int r = 0; r < 8; ++r)
                     if (8 * hf + r < nvv) op[static_cast<size_t>(r) * a.H * D] = a.scale * o[r];
@@ -721,11 +724,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // after a chain barrier that follows read_out(tt): one thread stores the staged tile
         auto store_out = [&](int tt) {
             const int tt0 = bos + tt * C;
-            if (!fout && min(C, eos - tt0) == C) {
-                tma_store_3d(&tm_o, ost + (tt & 1) * (C * D * 2), 0, h, tt0);
+            if (min(C, eos - tt0) == C) {
+                if constexpr (Split) tma_store_3d(f_trans ? &tm_ft : &tm_fz, ost, 0, h, tt0);
+                else tma_store_3d(&tm_o, ost + (tt & 1) * (C * D * 2), 0, h, tt0);
                 bulk_commit();
             }
-            bulk_wait_read<1>();   // the other staging tile is free again
+            if constexpr (!Split) bulk_wait_read<1>();   // the other staging tile is free again
         };
         for (int t = 0; t < ntiles; ++t) {
             const int s = t % NS;
@@ -756,6 +760,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tmem_st_wait();
             }
             tc_fence_before();
+            // fp32 staging: the previous tile's store has read it before the
+            // chain passes this barrier (read_out writes it next)
+            if constexpr (Split) if (tid == OST_TID) bulk_wait_read<0>();
             if (named_bar_or(2, NCHAIN, *abort_flag != 0)) break;   // uniform across the chain
             if (lane == 0 && warp < 2) {
                 tc_fence_after();
@@ -806,6 +813,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
         }
         // uniform decision: every chain thread takes the same branch
+        if constexpr (Split) if (tid == OST_TID) bulk_wait_read<0>();
         const bool aborted = named_bar_or(2, NCHAIN, *abort_flag != 0);
         if (ntiles > 0 && !aborted) {
             read_out(ntiles - 1);
@@ -841,16 +849,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-// [T_total, H, 128] bf16 viewed as a 3-D tensor (d, head, token).
-bool make_map(CUtensorMap *m, const void *ptr, int H, int T_total, int box_d, bool swizzle128) {
+// [T_total, H, 128] bf16 (or fp32) viewed as a 3-D tensor (d, head, token).
+bool make_map(CUtensorMap *m, const void *ptr, int H, int T_total, int box_d, bool swizzle128,
+              bool fp32 = false) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
+    const cuuint64_t esz = fp32 ? 4 : 2;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
                                 static_cast<cuuint64_t>(T_total)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * esz, static_cast<cuuint64_t>(H) * D * esz};
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_d), 1, static_cast<cuuint32_t>(C)};
     const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+    const CUresult r = enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                           const_cast<void *>(ptr), dims, strides, box,
                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -875,7 +886,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
-    CUtensorMap tq, tk, tz, tv, to;
+    CUtensorMap tq, tk, tz, tv, to, tft, tfz;
     // the gate tile map exists only for per-channel gates (a per-head g_raw is
     // [T, H]; with no gate it may be NULL) -- the same test as the kernel's
     const bool z_tile = a.gate_mode != KDA_GATE_NONE && !a.gate_scalar;
@@ -884,13 +895,19 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
         !make_map(&tv, a.v ? a.v : a.q, a.H, a.T_total, D / 2, true) ||
         !make_map(&to, a.out, a.H, a.T_total, D, false))
         return cudaErrorInvalidValue;
+    // a segment split's fp32 row buffers (the plain kernel never reads these)
+    if (a.vseg ? !make_map(&tft, a.out_trans, a.H, a.T_total, D, false, true) ||
+                     !make_map(&tfz, a.out_zero, a.H, a.T_total, D, false, true)
+               : false)
+        return cudaErrorInvalidValue;
+    if (!a.vseg) tft = tfz = to;
     const bool unbounded = a.gate_mode == KDA_GATE_LOG_DECAY || a.gate_mode == KDA_GATE_NEG_SOFTPLUS;
     auto kern = a.vseg ? (unbounded ? prefill_tc_kernel<true, true> : prefill_tc_kernel<false, true>)
                        : (unbounded ? prefill_tc_kernel<true, false> : prefill_tc_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(a.N) * static_cast<unsigned>(a.H));
-    kern<<<grid, NTHREADS, SMEM_BYTES, s>>>(tq, tk, tz, tv, to, a);
+    kern<<<grid, NTHREADS, SMEM_BYTES, s>>>(tq, tk, tz, tv, to, tft, tfz, a);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;

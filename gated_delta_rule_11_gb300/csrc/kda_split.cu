@@ -15,13 +15,14 @@
 // parameters, open weights, and forty-seven pages of how", §The machine
 // underneath).  Here one launch of the tensor-core prefill runs, for every
 // sequence, segment 0 from its given initial state, segments 1.. from zero,
-// and the transition run of each segment 1..; then
+// and the transition run of each segment 1.., every run writing its output
+// rows unrounded (fp32; one output path, so the runs' tile loop carries no
+// per-run branch); then
 //   split_compose_kernel: S_in,1 = final state of segment 0 and
 //       S_in,p+1 = Phi_p S_in,p + S0_p (fp32), the last one the final state;
 //   split_fixup_kernel:   o_t = o0_t + S_in,p^T R_t for t in segment p >= 1,
-//       R the transition run's output rows; o0 and R arrive unrounded
-//       (fp32), the product runs on fp16 copies with fp32 sums, and o_t is
-//       rounded to bf16 once.
+//       R the transition run's output rows, the product on fp16 copies with
+//       fp32 sums, and o_t = o0_t in segment 0; o_t is rounded to bf16 once.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -91,7 +92,8 @@ __global__ void __launch_bounds__(1024) split_plan_kernel(SplitArgs a) {
         for (int p = 0; p < P; ++p) {
             const int sb = min(b + p * a.seg_tokens, e), se = min(sb + a.seg_tokens, e);
             if (base + p < a.nv_max)
-                a.vseg[base + p] = make_int4(sb, se, p == 0 ? 0 : VSEG_ZERO_INIT | VSEG_OUT_ZERO, n);
+                a.vseg[base + p] = make_int4(sb, se, p == 0 ? VSEG_OUT_ZERO | VSEG_OUT_FINAL
+                                                            : VSEG_ZERO_INIT | VSEG_OUT_ZERO, n);
             if (p > 0 && base + P + p - 1 < a.nv_max)
                 a.vseg[base + P + p - 1] =
                     make_int4(sb, se, VSEG_ZERO_V | VSEG_IDENT_INIT | VSEG_OUT_TRANS, base + p);
@@ -298,15 +300,50 @@ __device__ __forceinline__ void fixup_span(__half *fsm, int t_first, int t_end, 
     }
 }
 
-// CTA (virtual index, chunk, head): FIX_TOKENS tokens of a transition run's segment.
+// o_t = bf16(O0_t) for the tokens [t_first, t_end) of head h (a first
+// segment, whose run started from the sequence's own initial state): float4
+// chunks (row i / 32, channels 4 (i % 32) ..), four loads in flight a thread.
+__device__ __forceinline__ void round_span(int t_first, int t_end, int h, int H, const float *O0,
+                                           __nv_bfloat16 *O) {
+    const int n4 = (t_end - t_first) * (D / 4);
+    for (int i0 = threadIdx.x; i0 < n4; i0 += 4 * 256) {
+        float4 x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + 256 * u;
+            if (i < n4)
+                x[u] = *reinterpret_cast<const float4 *>(
+                    O0 + (static_cast<size_t>(t_first + i / (D / 4)) * H + h) * D + 4 * (i % (D / 4)));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + 256 * u;
+            if (i < n4) {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(x[u].x, x[u].y), hi = __floats2bfloat162_rn(x[u].z, x[u].w);
+                uint2 w;
+                w.x = *reinterpret_cast<uint32_t *>(&lo);
+                w.y = *reinterpret_cast<uint32_t *>(&hi);
+                *reinterpret_cast<uint2 *>(O + (static_cast<size_t>(t_first + i / (D / 4)) * H + h) * D +
+                                           4 * (i % (D / 4))) = w;
+            }
+        }
+    }
+}
+
+// CTA (virtual index, chunk, head): FIX_TOKENS tokens of a transition run's
+// segment (corrected), or of a first segment (rounded).
 __global__ void __launch_bounds__(256) split_fixup_kernel(SplitArgs a) {
     extern __shared__ __align__(16) __half fsm[];
     const int vi = blockIdx.x, h = blockIdx.z;
     const int4 e = a.vseg[vi];
-    if (!(e.z & VSEG_OUT_TRANS)) return;   // one CTA row per transition run
+    if (!(e.z & (VSEG_OUT_TRANS | VSEG_OUT_FINAL))) return;   // one CTA row per transition run or first segment
     const int t_first = e.x + blockIdx.y * FIX_TOKENS;
     const int t_end = min(e.y, t_first + FIX_TOKENS);
     if (t_first >= t_end) return;
+    if (e.z & VSEG_OUT_FINAL) {
+        round_span(t_first, t_end, h, a.H, a.out_zero, static_cast<__nv_bfloat16 *>(a.out));
+        return;
+    }
     fixup_span(fsm, t_first, t_end, h, a.H, a.s_in + (static_cast<size_t>(e.w) * a.H + h) * D * D, a.out_trans,
                a.out_zero, static_cast<__nv_bfloat16 *>(a.out));
 }
