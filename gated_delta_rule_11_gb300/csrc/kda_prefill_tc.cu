@@ -154,8 +154,10 @@ __device__ __forceinline__ void note_timeout(volatile int *flag) {
 // Unbounded: the launch's gate map is unbounded (the per-tile pair path is
 // compiled in); the bounded instance carries none of that code.  Split: the
 // chains are the virtual sequences of a segment split (PrefillArgs::vseg);
-// the plain instance carries none of that code either.
-template <bool Unbounded, bool Split>
+// the plain instance carries none of that code either.  Ckpt: state
+// checkpoints are written (PrefillArgs::ckpt set); without it the tile loop
+// has no checkpoint test.
+template <bool Unbounded, bool Split, bool Ckpt>
 __global__ void __launch_bounds__(NTHREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_v,
@@ -582,7 +584,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int j = tid & 127;           // value channel = TMEM lane
         const int hf = tid >> 7;           // which half of the key rows / tile columns
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const long long ck_row0 = a.ckpt ? ckpt_first_row(a, n) : 0;
+        const long long ck_row0 = Ckpt ? ckpt_first_row(a, n) : 0;
         constexpr int HR = D / 2;          // state rows per thread
         constexpr uint32_t id_e = idesc_f16kind(kTypeF16, 128, 32, 0, 0);
         constexpr uint32_t id_g = idesc_f16kind(kTypeF16, 128, 16, 0, 0);
@@ -807,9 +809,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (tid == TMA_TID && t + NS < ntiles) issue_tma(tma_next++);
             if (tid == OST_TID && t > 0) store_out(t - 1);
             // state checkpoint after this tile (off the chain's critical path)
-            if (float *cp = ckpt_slot(a, ck_row0, min((t + 1) * C, eos - bos), h, D * D)) {
+            if constexpr (Ckpt) {
+                if (float *cp = ckpt_slot(a, ck_row0, min((t + 1) * C, eos - bos), h, D * D)) {
 #pragma unroll
-                for (int cc = 0; cc < HR; ++cc) __stcs(cp + static_cast<size_t>(hf * HR + cc) * D + j, S[cc]);
+                    for (int cc = 0; cc < HR; ++cc) __stcs(cp + static_cast<size_t>(hf * HR + cc) * D + j, S[cc]);
+                }
             }
         }
         // uniform decision: every chain thread takes the same branch
@@ -902,8 +906,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
         return cudaErrorInvalidValue;
     if (!a.vseg) tft = tfz = to;
     const bool unbounded = a.gate_mode == KDA_GATE_LOG_DECAY || a.gate_mode == KDA_GATE_NEG_SOFTPLUS;
-    auto kern = a.vseg ? (unbounded ? prefill_tc_kernel<true, true> : prefill_tc_kernel<false, true>)
-                       : (unbounded ? prefill_tc_kernel<true, false> : prefill_tc_kernel<false, false>);
+    auto kern = a.vseg   ? (unbounded ? prefill_tc_kernel<true, true, false> : prefill_tc_kernel<false, true, false>)
+                : a.ckpt ? (unbounded ? prefill_tc_kernel<true, false, true> : prefill_tc_kernel<false, false, true>)
+                         : (unbounded ? prefill_tc_kernel<true, false, false> : prefill_tc_kernel<false, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(a.N) * static_cast<unsigned>(a.H));
