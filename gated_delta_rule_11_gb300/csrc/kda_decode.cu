@@ -187,7 +187,10 @@ __device__ __forceinline__ float4 ld_state(const float4 *p) {
 // partials of one column each, form u_j and o_j; barrier; every thread
 // applies u to its rows.  The second barrier also orders the partials'
 // reads before the next token's writes, so one buffer serves all tokens.
-template <typename Tin, int DK, int DV, int CS>
+// GenericGate = false compiles the default gate (eq. (5), one input per key
+// channel) with the gate-mode tests and the staging loop's chunk count
+// constant; true takes any kda_gate_mode.
+template <typename Tin, int DK, int DV, int CS, bool GenericGate>
 __global__ void __launch_bounds__(kDecodeThreads, 2 * CS) decode_kernel(DecodeArgs a) {
     constexpr int DVS = DV / CS;                     // slab columns
     constexpr int V4 = DVS / 4;                      // float4 per slab row
@@ -233,7 +236,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2 * CS) decode_kernel(DecodeAr
     auto stage = [&](int i0, int nb) {
         constexpr int CH = DK * static_cast<int>(sizeof(Tin)) / 16;    // 16-byte chunks per channel row
         constexpr int CV = DVS * static_cast<int>(sizeof(Tin)) / 16;   // per value-slab row
-        const int nz = (a.gate_mode != KDA_GATE_NONE && !a.gate_scalar) ? 1 : 0;
+        const int nz = !GenericGate || (a.gate_mode != KDA_GATE_NONE && !a.gate_scalar) ? 1 : 0;
         const int per_tok = CH * (2 + nz) + CV;
         for (int idx = tid; idx < nb * per_tok; idx += kDecodeThreads) {
             const int i = idx / per_tok, w = idx % per_tok;
@@ -261,17 +264,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 2 * CS) decode_kernel(DecodeAr
             if constexpr (kStage) {
                 kc = __bfloat162float(kin[i * DK + c]);
                 qc = __bfloat162float(qin[i * DK + c]);
-                zc = a.gate_mode == KDA_GATE_NONE ? 0.f
+                zc = !GenericGate ? __bfloat162float(zin[i * DK + c])
+                     : a.gate_mode == KDA_GATE_NONE ? 0.f
                      : a.gate_scalar ? ld_in(gz + (static_cast<size_t>(n) * a.K + i0 + i) * a.H + h)
                                      : __bfloat162float(zin[i * DK + c]);
             } else {
                 const size_t o = (static_cast<size_t>(n) * a.K + i0 + i) * tok_k + static_cast<size_t>(h) * DK + c;
                 kc = ld_in(gk + o);
                 qc = ld_in(gq + o);
-                const size_t og = a.gate_scalar ? (static_cast<size_t>(n) * a.K + i0 + i) * a.H + h : o;
-                zc = a.gate_mode == KDA_GATE_NONE ? 0.f : ld_in(gz + og);
+                const size_t og = GenericGate && a.gate_scalar ? (static_cast<size_t>(n) * a.K + i0 + i) * a.H + h : o;
+                zc = GenericGate && a.gate_mode == KDA_GATE_NONE ? 0.f : ld_in(gz + og);
             }
-            const float alpha = expf(gate_log_decay(a.gate_mode, zc, escale, a.g_min));
+            const float alpha = expf(GenericGate ? gate_log_decay(a.gate_mode, zc, escale, a.g_min)
+                                                 : log_decay(zc, escale, a.g_min));
             sm.akq[i][c] = make_float2(alpha * kc, alpha * qc);
             sm.alk[i][c] = make_float2(alpha, kc);
             float kq = kc * qc;
@@ -377,9 +382,13 @@ cudaError_t launch_t(int dk, int dv, const DecodeArgs &a, cudaStream_t s) {
         if (single && default_gate)                                       \
             decode1_kernel<Tin, DK_, DV_, false><<<grid, block, 0, s>>>(a); \
         else if (single) decode1_kernel<Tin, DK_, DV_, true><<<grid, block, 0, s>>>(a); \
-        else if constexpr (DV_ >= 64)                                     \
-            decode_kernel<Tin, DK_, DV_, 2><<<dim3(grid.x * 2), block, 0, s>>>(a); \
-        else decode_kernel<Tin, DK_, DV_, 1><<<grid, block, 0, s>>>(a);   \
+        else if constexpr (DK_ == 128 && DV_ == 128) {                   \
+            if (default_gate)                                             \
+                decode_kernel<Tin, DK_, DV_, 2, false><<<dim3(grid.x * 2), block, 0, s>>>(a); \
+            else decode_kernel<Tin, DK_, DV_, 2, true><<<dim3(grid.x * 2), block, 0, s>>>(a); \
+        } else if constexpr (DV_ >= 64)                                   \
+            decode_kernel<Tin, DK_, DV_, 2, true><<<dim3(grid.x * 2), block, 0, s>>>(a); \
+        else decode_kernel<Tin, DK_, DV_, 1, true><<<grid, block, 0, s>>>(a); \
         const cudaError_t e = cudaGetLastError();                         \
         if (e == cudaSuccess) count_launches(1);                          \
         return e;                                                         \
