@@ -156,8 +156,9 @@ __device__ __forceinline__ void note_timeout(volatile int *flag) {
 // chains are the virtual sequences of a segment split (PrefillArgs::vseg);
 // the plain instance carries none of that code either.  Ckpt: state
 // checkpoints are written (PrefillArgs::ckpt set); without it the tile loop
-// has no checkpoint test.
-template <bool Unbounded, bool Split, bool Ckpt>
+// has no checkpoint test.  ChannelGate: the default gate (eq. (5), one input
+// per key channel) with the gate-shape tests constant.
+template <bool Unbounded, bool Split, bool Ckpt, bool ChannelGate>
 __global__ void __launch_bounds__(NTHREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_v,
@@ -191,8 +192,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const size_t state_off = static_cast<size_t>(chain) * D * D;
     // gate source: a TMA tile of per-channel inputs (eq. (5)), one input per
     // (token, head) shared by the channels, or none (alpha = 1)
-    const bool gate_none = a.gate_mode == KDA_GATE_NONE;
-    const bool z_tile = !gate_none && !a.gate_scalar;
+    const bool gate_none = !ChannelGate && a.gate_mode == KDA_GATE_NONE;
+    const bool z_tile = ChannelGate || (!gate_none && !a.gate_scalar);
     // unbounded maps (the gate as the log-decay, Kimi Linear's -softplus):
     // a tile whose cumulative decay leaves fp32's range for e^{-b} takes the
     // position-pair path for L and A
@@ -906,9 +907,15 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
         return cudaErrorInvalidValue;
     if (!a.vseg) tft = tfz = to;
     const bool unbounded = a.gate_mode == KDA_GATE_LOG_DECAY || a.gate_mode == KDA_GATE_NEG_SOFTPLUS;
-    auto kern = a.vseg   ? (unbounded ? prefill_tc_kernel<true, true, false> : prefill_tc_kernel<false, true, false>)
-                : a.ckpt ? (unbounded ? prefill_tc_kernel<true, false, true> : prefill_tc_kernel<false, false, true>)
-                         : (unbounded ? prefill_tc_kernel<true, false, false> : prefill_tc_kernel<false, false, false>);
+    const bool channel_gate = !unbounded && a.gate_mode == KDA_GATE_BOUNDED && !a.gate_scalar;
+    auto kern = a.vseg   ? (unbounded      ? prefill_tc_kernel<true, true, false, false>
+                            : channel_gate ? prefill_tc_kernel<false, true, false, true>
+                                           : prefill_tc_kernel<false, true, false, false>)
+                : a.ckpt ? (unbounded ? prefill_tc_kernel<true, false, true, false>
+                                      : prefill_tc_kernel<false, false, true, false>)
+                         : (unbounded      ? prefill_tc_kernel<true, false, false, false>
+                            : channel_gate ? prefill_tc_kernel<false, false, false, true>
+                                           : prefill_tc_kernel<false, false, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(a.N) * static_cast<unsigned>(a.H));
