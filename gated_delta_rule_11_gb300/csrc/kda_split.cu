@@ -107,85 +107,82 @@ __global__ void __launch_bounds__(1024) split_plan_kernel(SplitArgs a) {
     for (int i = total + tid; i < a.nv_max; i += 1024) a.vseg[i] = make_int4(0, 0, VSEG_EMPTY, 0);
 }
 
-// State composition over one (sequence, head): S = s_first, then for
-// p = 1 .. P - 1: keep_of(p) <- S (the state entering segment p, when the
-// pointer is set), S <- phi_of(p) S + s0_of(p); final <- S (when set).  One
-// CTA of 256 threads, each an 8 x 8 block of the 128 x 128 product; shared
-// memory: Phi^T (row stride 132) and S.
+// State composition over one (sequence, head), CW of the state's columns
+// per CTA (blockIdx.y picks them): S = s_first, then for p = 1 .. P - 1:
+// keep_of(p) <- S (the state entering segment p, when the pointer is set),
+// S <- phi_of(p) S + s0_of(p); final <- S (when set).  The columns of S
+// never mix (each is advanced by the same Phi), so the column blocks of one
+// chain run on separate CTAs with no exchange.  256 threads, each 8 rows of
+// one column; shared memory: Phi^T (row stride CPAD) and the CTA's columns
+// of S.  Phi of the next step is loaded into registers while the current
+// product runs.
 constexpr int CPAD = 132;
-constexpr int COMPOSE_SMEM = (D * CPAD + D * D) * 4;
+constexpr int CW = 16;
+constexpr int COMPOSE_SMEM = (D * CPAD + D * CW) * 4;
 
 template <typename PhiOf, typename S0Of, typename KeepOf>
 __device__ __forceinline__ void compose_chain(float *csm, int P, const float *s_first, PhiOf phi_of, S0Of s0_of,
                                               KeepOf keep_of, float *final_out) {
     float *phiT = csm;              // phiT[c][r] = Phi[r][c]
-    float *sin_ = csm + D * CPAD;   // S[c][j]
-    const int tid = threadIdx.x;
-    const int r0 = (tid >> 4) * 8, j0 = (tid & 15) * 8;
-    for (int i = tid; i < D * D / 4; i += 256)
-        reinterpret_cast<float4 *>(sin_)[i] = reinterpret_cast<const float4 *>(s_first)[i];
+    float *sc = csm + D * CPAD;     // sc[c][jj] = S[c][jb + jj]
+    const int tid = threadIdx.x, jb = static_cast<int>(blockIdx.y) * CW;
+    const int r0 = (tid >> 4) * 8, jj = tid & (CW - 1);
+    static_assert(CW == 16 && D == 128, "thread layout: 16 row groups x 16 columns");
+    // this CTA's columns of a [D, D] state as float4 chunks i: row i / (CW / 4), columns 4 (i % (CW / 4)) ..
+    auto cols4 = [&](const float *m, int i) {
+        return reinterpret_cast<const float4 *>(m + (i / (CW / 4)) * D + jb) + (i % (CW / 4));
+    };
+    for (int i = tid; i < D * CW / 4; i += 256) reinterpret_cast<float4 *>(sc)[i] = *cols4(s_first, i);
+    // Phi as 16 float4 per thread: chunk i = tid + 256 k is row i & 127,
+    // columns 4 (i >> 7) .., so a warp's lanes hold 32 consecutive rows and
+    // its transposed stores fall in 32 distinct banks
+    float4 x[16];
+    auto load_phi = [&](int p) {
+        const float4 *phi = reinterpret_cast<const float4 *>(phi_of(p));
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int i = tid + 256 * k;
+            x[k] = phi[(i & 127) * (D / 4) + (i >> 7)];
+        }
+    };
+    if (P > 1) load_phi(1);
     __syncthreads();
     for (int p = 1; p < P; ++p) {
         if (float *keep = keep_of(p))
-            for (int i = tid; i < D * D / 4; i += 256)
-                reinterpret_cast<float4 *>(keep)[i] = reinterpret_cast<const float4 *>(sin_)[i];
-        // Phi as 16 float4 per thread, all requested before the first is used:
-        // chunk i = tid + 256 k is row i & 127, columns 4 (i >> 7) .., so a
-        // warp's lanes hold 32 consecutive rows and its transposed stores
-        // below fall in 32 distinct banks
-        const float4 *phi = reinterpret_cast<const float4 *>(phi_of(p));
+            for (int i = tid; i < D * CW / 4; i += 256)
+                *const_cast<float4 *>(cols4(keep, i)) = reinterpret_cast<const float4 *>(sc)[i];
         const float *s0 = s0_of(p);
-        float acc[8][8];
-        {
-            float4 x[16];
+        float acc[8];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const int i = tid + 256 * k;
-                x[k] = phi[(i & 127) * (D / 4) + (i >> 7)];
-            }
+        for (int i = 0; i < 8; ++i) acc[i] = s0[(r0 + i) * D + jb + jj];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 lo = *reinterpret_cast<const float4 *>(s0 + (r0 + i) * D + j0);
-                const float4 hi = *reinterpret_cast<const float4 *>(s0 + (r0 + i) * D + j0 + 4);
-                acc[i][0] = lo.x; acc[i][1] = lo.y; acc[i][2] = lo.z; acc[i][3] = lo.w;
-                acc[i][4] = hi.x; acc[i][5] = hi.y; acc[i][6] = hi.z; acc[i][7] = hi.w;
-            }
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const int i = tid + 256 * k, r = i & 127, c = (i >> 7) * 4;
-                phiT[(c + 0) * CPAD + r] = x[k].x;
-                phiT[(c + 1) * CPAD + r] = x[k].y;
-                phiT[(c + 2) * CPAD + r] = x[k].z;
-                phiT[(c + 3) * CPAD + r] = x[k].w;
-            }
+        for (int k = 0; k < 16; ++k) {
+            const int i = tid + 256 * k, r = i & 127, c = (i >> 7) * 4;
+            phiT[(c + 0) * CPAD + r] = x[k].x;
+            phiT[(c + 1) * CPAD + r] = x[k].y;
+            phiT[(c + 2) * CPAD + r] = x[k].z;
+            phiT[(c + 3) * CPAD + r] = x[k].w;
         }
         __syncthreads();
-#pragma unroll 2
+        if (p + 1 < P) load_phi(p + 1);   // in flight during the product
+#pragma unroll 4
         for (int c = 0; c < D; ++c) {
             const float4 pa = *reinterpret_cast<const float4 *>(phiT + c * CPAD + r0);
             const float4 pb = *reinterpret_cast<const float4 *>(phiT + c * CPAD + r0 + 4);
-            const float4 sa = *reinterpret_cast<const float4 *>(sin_ + c * D + j0);
-            const float4 sb = *reinterpret_cast<const float4 *>(sin_ + c * D + j0 + 4);
-            const float pr[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
-            const float sr[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) acc[i][jj] = fmaf(pr[i], sr[jj], acc[i][jj]);
+            const float sv = sc[c * CW + jj];
+            acc[0] = fmaf(pa.x, sv, acc[0]); acc[1] = fmaf(pa.y, sv, acc[1]);
+            acc[2] = fmaf(pa.z, sv, acc[2]); acc[3] = fmaf(pa.w, sv, acc[3]);
+            acc[4] = fmaf(pb.x, sv, acc[4]); acc[5] = fmaf(pb.y, sv, acc[5]);
+            acc[6] = fmaf(pb.z, sv, acc[6]); acc[7] = fmaf(pb.w, sv, acc[7]);
         }
         __syncthreads();   // every thread has read S and Phi^T
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            *reinterpret_cast<float4 *>(sin_ + (r0 + i) * D + j0) =
-                make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-            *reinterpret_cast<float4 *>(sin_ + (r0 + i) * D + j0 + 4) =
-                make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
-        }
+        for (int i = 0; i < 8; ++i) sc[(r0 + i) * CW + jj] = acc[i];
         __syncthreads();
     }
     if (final_out)
-        for (int i = tid; i < D * D / 4; i += 256)
-            reinterpret_cast<float4 *>(final_out)[i] = reinterpret_cast<const float4 *>(sin_)[i];
+        for (int i = tid; i < D * CW / 4; i += 256)
+            *const_cast<float4 *>(cols4(final_out, i)) = reinterpret_cast<const float4 *>(sc)[i];
 }
 
 __global__ void __launch_bounds__(256) split_compose_kernel(SplitArgs a) {
@@ -358,7 +355,7 @@ __global__ void __launch_bounds__(256) kcp_plan_kernel(KcpArgs a) {
     }
 }
 
-// One CTA per (sequence, head): the state entering rank r from the gathered
+// One CTA per (sequence, head, column block): the state entering rank r from the gathered
 // pairs of ranks 0 .. r ([r + 1, B, 2, H, d, d]: [.][.][0] the zero-state
 // run's final state (rank 0: its true final state), [.][.][1] the
 // transition), then this rank's final state.
@@ -401,7 +398,8 @@ cudaError_t launch_kcp_finish(const KcpArgs &a, cudaStream_t s) {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(kcp_fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FIX_SMEM);
     if (e != cudaSuccess) return e;
-    kcp_compose_kernel<<<static_cast<unsigned>(a.B) * static_cast<unsigned>(a.H), 256, COMPOSE_SMEM, s>>>(a);
+    kcp_compose_kernel<<<dim3(static_cast<unsigned>(a.B) * static_cast<unsigned>(a.H), D / CW), 256, COMPOSE_SMEM,
+                         s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     count_launches(1);
@@ -424,7 +422,8 @@ cudaError_t launch_split_compose(const SplitArgs &a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(split_compose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          COMPOSE_SMEM);
     if (e != cudaSuccess) return e;
-    split_compose_kernel<<<static_cast<unsigned>(a.N) * static_cast<unsigned>(a.H), 256, COMPOSE_SMEM, s>>>(a);
+    split_compose_kernel<<<dim3(static_cast<unsigned>(a.N) * static_cast<unsigned>(a.H), D / CW), 256, COMPOSE_SMEM,
+                           s>>>(a);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;
