@@ -266,6 +266,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const float zs = zs_next;
             zs_next = load_zs(t + NPROD);
             if (!mbar_wait(&bars[B_RAW + s], (t / NS) & 1, kWaitLimitNs)) note_timeout(abort_flag);
+            // the abort flag as seen after this tile's own wait; read here so
+            // its latency is off the barrier that publishes it
+            const bool abort_seen = *abort_flag != 0;
 
             // Gate and decays in log2 units, branch-free: the retention
             // a_r = 2^{g_r / ln 2}; prefix products give e^{b_r}, suffix
@@ -378,7 +381,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 *reinterpret_cast<float2 *>(kgm + row * PADF + c0) = make_float2(to_tf32(kg.x), to_tf32(kg.y));
                 *reinterpret_cast<float2 *>(kim + row * PADF + c0) = make_float2(to_tf32(ki.x), to_tf32(ki.y));
             }
-            if (named_bar_or(pbar, 128, *abort_flag != 0)) break;   // uniform across the warpgroup
+            if (named_bar_or(pbar, 128, abort_seen)) break;   // uniform across the warpgroup
             const bool pair_tile =
                 unbounded && named_bar_or(pbar, 128, gC[0] < kPairThreshold || gC[1] < kPairThreshold);
 
@@ -741,6 +744,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             bool ok = mbar_wait(&bars[B_VT], t & 1, kWaitLimitNs);
             ok = mbar_wait(&bars[B_FULL + s], (t / NS) & 1, kWaitLimitNs) && ok;   // U, e^{b_C} visible
             if (!ok) note_timeout(abort_flag);
+            const bool abort_seen = *abort_flag != 0;   // read early: off the barrier below
             tc_fence_after();
             {
                 // tile columns [8 hf, 8 hf + 8) of Vt^T = U^T - (W S)^T
@@ -766,7 +770,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             // fp32 staging: the previous tile's store has read it before the
             // chain passes this barrier (read_out writes it next)
             if constexpr (Split) if (tid == OST_TID) bulk_wait_read<0>();
-            if (named_bar_or(2, NCHAIN, *abort_flag != 0)) break;   // uniform across the chain
+            if (named_bar_or(2, NCHAIN, abort_seen)) break;   // uniform across the chain
             if (lane == 0 && warp < 2) {
                 tc_fence_after();
                 const uint32_t stb = sb + s * STAGE_BYTES;
