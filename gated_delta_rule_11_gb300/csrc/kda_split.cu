@@ -208,27 +208,50 @@ __global__ void __launch_bounds__(256) split_compose_kernel(SplitArgs a) {
 // columns 64 (w >> 2) .. +64 of the 64 x 128 update with m16n8k16 fp16
 // products.  Rows are [token][H][128] in R, O0 and O.
 constexpr int FIX_TOKENS = 1024;
-constexpr int HSTR = 136;
-constexpr int FIX_SMEM = (D * HSTR + 64 * HSTR) * 2;
+constexpr int HSTR = 136;                         // fp16 row stride of S_in^T (bank spread)
+constexpr int FT = 32;                            // tokens per stage
+constexpr int RPAD = 136;                         // fp32 row stride of the staged rows
+constexpr int FIX_STAGE = 2 * FT * RPAD * 4;      // R and o0 rows of one stage
+constexpr int FIX_SMEM = D * HSTR * 2 + 2 * FIX_STAGE;
 
-__device__ __forceinline__ void fixup_span(__half *fsm, int t_first, int t_end, int h, int H, const float *sin_,
-                                           const float *R, const float *O0, __nv_bfloat16 *O) {
-    __half *sT = fsm;              // sT[j][c] = S_in[c][j]
-    __half *rs = fsm + D * HSTR;   // rs[t][c] = R[t][c]
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                 ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// o_t = bf16(o0_t + S_in^T R_t) for the tokens [t_first, t_end) of head h.
+// R and o0 rows stream through two shared-memory stages of FT tokens by
+// 16-byte cp.async (no registers held while in flight; stage k + 1 loads
+// while stage k is used); S_in^T is converted to fp16 once.  Eight warps,
+// warp w the rows 16 (w & 1) .. and columns 32 (w >> 1) .. of a stage's
+// [FT, 128] output: m16n8k16 products, A (R rows) converted from fp32 in
+// registers, fp32 sums, one bf16 rounding.
+__device__ __forceinline__ void fixup_span(unsigned char *fsm, int t_first, int t_end, int h, int H,
+                                           const float *sin_, const float *R, const float *O0,
+                                           __nv_bfloat16 *O) {
+    __half *sT = reinterpret_cast<__half *>(fsm);                 // sT[j][c] = S_in[c][j]
+    float *stage0 = reinterpret_cast<float *>(fsm + D * HSTR * 2);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // rows t0 .. t0 + 63 of R: thread tid holds float4 chunks i = tid + 256 k
-    // (row i >> 5, channels 4 (i & 31) ..), zero past the span
-    float4 nxt[8];
-    auto load_r = [&](int t0) {
+    // stage buf: rows [t0, t0 + FT) of R then of o0, RPAD floats a row;
+    // 2 x FT x 32 chunks of 16 bytes, 8 a thread; rows past t_end are not
+    // loaded (their products are never stored); one commit group a stage
+    auto load_stage = [&](int t0, int buf) {
+        float *st = stage0 + buf * (2 * FT * RPAD);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int i = tid + 256 * k, t = t0 + (i >> 5);
-            nxt[k] = t < t_end ? *reinterpret_cast<const float4 *>(R + (static_cast<size_t>(t) * H + h) * D +
-                                                                    (i & 31) * 4)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < 2 * FT * 32 / 256; ++k) {
+            const int i = tid + 256 * k;
+            const int which = i / (FT * 32), row = (i / 32) % FT, ch = i % 32;
+            const int t = t0 + row;
+            if (t < t_end)
+                cp_async16(st + (which * FT + row) * RPAD + ch * 4,
+                           (which ? O0 : R) + (static_cast<size_t>(t) * H + h) * D + ch * 4);
         }
+        cp_async_commit();
     };
-    load_r(t_first);
+    load_stage(t_first, 0);
     {   // S_in^T as fp16: thread tid converts float4 chunks (row c, columns 4 m ..)
         float4 x[16];
 #pragma unroll
@@ -243,40 +266,30 @@ __device__ __forceinline__ void fixup_span(__half *fsm, int t_first, int t_end, 
         }
     }
     const int g = lane >> 2, tq = lane & 3;
-    const int m0 = 16 * (warp & 3), n0 = 64 * (warp >> 2);
-    for (int t0 = t_first; t0 < t_end; t0 += 64) {
-        __syncthreads();   // sT written / previous rows consumed
+    constexpr int NB = 4;                          // n8 blocks a warp
+    const int m0 = 16 * (warp & 1), n0 = 32 * (warp >> 1);
+    int buf = 0;
+    for (int t0 = t_first; t0 < t_end; t0 += FT, buf ^= 1) {
+        load_stage(t0 + FT, buf ^ 1);              // an empty group past t_end
+        cp_async_wait<1>();                        // this thread's copies of stage buf are done
+        __syncthreads();                           // everyone's; S_in^T written (first pass)
+        const float *rs = stage0 + buf * (2 * FT * RPAD);
+        const float *os = rs + FT * RPAD;
+        float acc[NB][4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int i = tid + 256 * k;
-            *reinterpret_cast<uint2 *>(rs + (i >> 5) * HSTR + (i & 31) * 4) =
-                make_uint2(pack_h2(nxt[k].x, nxt[k].y), pack_h2(nxt[k].z, nxt[k].w));
-        }
-        __syncthreads();
-        if (t0 + 64 < t_end) load_r(t0 + 64);   // in flight during the products
-        // this thread's o0 entries, loaded ahead of the products
-        float2 o0[2][8];
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-            const int t = min(t0 + m0 + g + 8 * hr, t_end - 1);
-            const size_t row = (static_cast<size_t>(t) * H + h) * D;
-#pragma unroll
-            for (int nb = 0; nb < 8; ++nb)
-                o0[hr][nb] = *reinterpret_cast<const float2 *>(O0 + row + n0 + 8 * nb + 2 * tq);
-        }
-        float acc[8][4];
-#pragma unroll
-        for (int nb = 0; nb < 8; ++nb)
+        for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
             for (int q = 0; q < 4; ++q) acc[nb][q] = 0.f;
 #pragma unroll
         for (int k0 = 0; k0 < D; k0 += 16) {
-            const uint32_t a0 = *reinterpret_cast<const uint32_t *>(rs + (m0 + g) * HSTR + k0 + 2 * tq);
-            const uint32_t a1 = *reinterpret_cast<const uint32_t *>(rs + (m0 + g + 8) * HSTR + k0 + 2 * tq);
-            const uint32_t a2 = *reinterpret_cast<const uint32_t *>(rs + (m0 + g) * HSTR + k0 + 2 * tq + 8);
-            const uint32_t a3 = *reinterpret_cast<const uint32_t *>(rs + (m0 + g + 8) * HSTR + k0 + 2 * tq + 8);
+            const float2 x0 = *reinterpret_cast<const float2 *>(rs + (m0 + g) * RPAD + k0 + 2 * tq);
+            const float2 x1 = *reinterpret_cast<const float2 *>(rs + (m0 + g + 8) * RPAD + k0 + 2 * tq);
+            const float2 x2 = *reinterpret_cast<const float2 *>(rs + (m0 + g) * RPAD + k0 + 2 * tq + 8);
+            const float2 x3 = *reinterpret_cast<const float2 *>(rs + (m0 + g + 8) * RPAD + k0 + 2 * tq + 8);
+            const uint32_t a0 = pack_h2(x0.x, x0.y), a1 = pack_h2(x1.x, x1.y);
+            const uint32_t a2 = pack_h2(x2.x, x2.y), a3 = pack_h2(x3.x, x3.y);
 #pragma unroll
-            for (int nb = 0; nb < 8; ++nb) {
+            for (int nb = 0; nb < NB; ++nb) {
                 const int j = n0 + 8 * nb + g;
                 const uint32_t b0 = *reinterpret_cast<const uint32_t *>(sT + j * HSTR + k0 + 2 * tq);
                 const uint32_t b1 = *reinterpret_cast<const uint32_t *>(sT + j * HSTR + k0 + 2 * tq + 8);
@@ -286,15 +299,20 @@ __device__ __forceinline__ void fixup_span(__half *fsm, int t_first, int t_end, 
         // rows m0 + g (acc[.][0..1]) and m0 + g + 8 (acc[.][2..3]), columns n0 + 8 nb + 2 tq + {0, 1}
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
-            const int t = t0 + m0 + g + 8 * hr;
+            const int r = m0 + g + 8 * hr, t = t0 + r;
             if (t >= t_end) continue;
             __nv_bfloat16 *orow = O + (static_cast<size_t>(t) * H + h) * D;
 #pragma unroll
-            for (int nb = 0; nb < 8; ++nb)
-                *reinterpret_cast<__nv_bfloat162 *>(orow + n0 + 8 * nb + 2 * tq) =
-                    __floats2bfloat162_rn(o0[hr][nb].x + acc[nb][2 * hr], o0[hr][nb].y + acc[nb][2 * hr + 1]);
+            for (int nb = 0; nb < NB; ++nb) {
+                const int col = n0 + 8 * nb + 2 * tq;
+                const float2 o0 = *reinterpret_cast<const float2 *>(os + r * RPAD + col);
+                *reinterpret_cast<__nv_bfloat162 *>(orow + col) =
+                    __floats2bfloat162_rn(o0.x + acc[nb][2 * hr], o0.y + acc[nb][2 * hr + 1]);
+            }
         }
+        __syncthreads();                           // stage buf consumed before it is refilled
     }
+    cp_async_wait<0>();
 }
 
 // o_t = bf16(O0_t) for the tokens [t_first, t_end) of head h (a first
@@ -330,7 +348,7 @@ __device__ __forceinline__ void round_span(int t_first, int t_end, int h, int H,
 // CTA (virtual index, chunk, head): FIX_TOKENS tokens of a transition run's
 // segment (corrected), or of a first segment (rounded).
 __global__ void __launch_bounds__(256) split_fixup_kernel(SplitArgs a) {
-    extern __shared__ __align__(16) __half fsm[];
+    extern __shared__ __align__(16) unsigned char fsm[];
     const int vi = blockIdx.x, h = blockIdx.z;
     const int4 e = a.vseg[vi];
     if (!(e.z & (VSEG_OUT_TRANS | VSEG_OUT_FINAL))) return;   // one CTA row per transition run or first segment
@@ -374,7 +392,7 @@ __global__ void __launch_bounds__(256) kcp_compose_kernel(KcpArgs a) {
 
 // CTA (sequence, chunk, head): FIX_TOKENS tokens of this rank's part of a sequence.
 __global__ void __launch_bounds__(256) kcp_fixup_kernel(KcpArgs a) {
-    extern __shared__ __align__(16) __half fsm[];
+    extern __shared__ __align__(16) unsigned char fsm[];
     const int n = blockIdx.x, h = blockIdx.z;
     const int t_first = n * a.T + blockIdx.y * FIX_TOKENS;
     const int t_end = min((n + 1) * a.T, t_first + FIX_TOKENS);
