@@ -70,6 +70,8 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
+#include <type_traits>
+
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
 #include "kda_tc_util.cuh"
@@ -283,20 +285,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 const f32x2 zc = pack2(-kLog2e * escale, -kLog2e * escale);
                 const f32x2 lc = pack2(kLog2e * a.g_min, kLog2e * a.g_min);
                 const f32x2 one = pack2(1.f, 1.f);
+                // full tiles (all but a sequence's last) without the row masks
+                auto gate_rows = [&](auto full) {
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int row = 8 * hh + r;
-                    const bool in = row < nv;
-                    const uint32_t zz = *reinterpret_cast<const uint32_t *>(st + ST_Z + row * 256 + c0 * 2);
-                    const uint32_t kk = in ? *reinterpret_cast<const uint32_t *>(st + ST_K + row * 256 + c0 * 2) : 0u;
-                    const uint32_t qq = in ? *reinterpret_cast<const uint32_t *>(st + ST_Q + row * 256 + c0 * 2) : 0u;
-                    kx[r] = pack2(bf16_half(kk, 0), bf16_half(kk, 1));
-                    qx[r] = pack2(bf16_half(qq, 0), bf16_half(qq, 1));
-                    const float2 e = unpack2(fmul2(zc, pack2(bf16_half(zz, 0), bf16_half(zz, 1))));
-                    const f32x2 den = fadd2(one, pack2(ex2_approx(e.x), ex2_approx(e.y)));
-                    const float2 lg = unpack2(fmul2(lc, pack2(rcp_approx(unpack2(den).x), rcp_approx(unpack2(den).y))));
-                    suf[r] = in ? pack2(ex2_approx(lg.x), ex2_approx(lg.y)) : one;   // a_r (1 past the end)
-                }
+                    for (int r = 0; r < 8; ++r) {
+                        const int row = 8 * hh + r;
+                        const bool in = decltype(full)::value || row < nv;
+                        const uint32_t zz = *reinterpret_cast<const uint32_t *>(st + ST_Z + row * 256 + c0 * 2);
+                        const uint32_t kk = in ? *reinterpret_cast<const uint32_t *>(st + ST_K + row * 256 + c0 * 2) : 0u;
+                        const uint32_t qq = in ? *reinterpret_cast<const uint32_t *>(st + ST_Q + row * 256 + c0 * 2) : 0u;
+                        kx[r] = pack2(bf16_half(kk, 0), bf16_half(kk, 1));
+                        qx[r] = pack2(bf16_half(qq, 0), bf16_half(qq, 1));
+                        const float2 e = unpack2(fmul2(zc, pack2(bf16_half(zz, 0), bf16_half(zz, 1))));
+                        const f32x2 den = fadd2(one, pack2(ex2_approx(e.x), ex2_approx(e.y)));
+                        const float2 lg = unpack2(fmul2(lc, pack2(rcp_approx(unpack2(den).x), rcp_approx(unpack2(den).y))));
+                        suf[r] = in ? pack2(ex2_approx(lg.x), ex2_approx(lg.y)) : one;   // a_r (1 past the end)
+                    }
+                };
+                if (nv == C) gate_rows(std::true_type{});
+                else gate_rows(std::false_type{});
             } else if (z_tile) {                        // unbounded map per key channel
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
