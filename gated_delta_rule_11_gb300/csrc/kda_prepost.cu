@@ -182,7 +182,9 @@ template <> struct Oct<float> {
 // channels per lane), so a warp works on 32 * 8 / D tokens at once; each
 // group walks its own consecutive tokens with the three previous inputs in
 // registers.  Six resident CTAs per SM keep twelve tiles in flight.
-template <typename Tin, int D>
+// PART 0 runs the q and k tensors (L2-normalised; beta with q), PART 1 the
+// v tensor: the norm test is a compile-time constant in each instance.
+template <typename Tin, int D, int PART>
 __global__ void __launch_bounds__(kPrepWarps * 32, 6) prep_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                                PrepArgs a) {
     using namespace sm100;
@@ -202,7 +204,8 @@ __global__ void __launch_bounds__(kPrepWarps * 32, 6) prep_kernel(const __grid_c
     const int H = a.H;
     // task counts fit in 32 bits (the launcher checks): a CTA owns the runs
     // 2 rp, 2 rp + 1 of one (tensor, head) mh, or one empty sequence's state
-    const int row_tasks = 3 * H;                                   // (tensor, head) pairs
+    constexpr int M0 = PART == 0 ? 0 : 2, NM = PART == 0 ? 2 : 1;  // this instance's tensors
+    const int row_tasks = NM * H;                                  // (tensor, head) pairs
     const int n_runs = (a.T_total + kRun - 1) / kRun;
     const int run_tasks = (n_runs + 1) / 2 * row_tasks;
     const int task = static_cast<int>(blockIdx.x);
@@ -216,7 +219,7 @@ __global__ void __launch_bounds__(kPrepWarps * 32, 6) prep_kernel(const __grid_c
         const int et = task - run_tasks;
         if (warp != 0 || et >= a.N * row_tasks || !sout) return;
         const int n = et / row_tasks;
-        const int mh = et % row_tasks;
+        const int mh = M0 * H + et % row_tasks;
         int bos, eos;
         span_of(a, n, bos, eos);
         if (eos > bos) return;
@@ -234,7 +237,7 @@ __global__ void __launch_bounds__(kPrepWarps * 32, 6) prep_kernel(const __grid_c
     }
 
     const int run0 = task / row_tasks * 2;
-    const int mh = task % row_tasks;                       // m * H + h
+    const int mh = M0 * H + task % row_tasks;              // m * H + h
     const int m = mh / H, h = mh % H;
     const int nr = min(2, n_runs - run0);                  // runs of this CTA
     if (tid == 0) {
@@ -353,7 +356,7 @@ __global__ void __launch_bounds__(kPrepWarps * 32, 6) prep_kernel(const __grid_c
                 win[1][q] = win[2][q];
                 win[2][q] = xt[q];
             }
-            if (m < 2) {                              // q, k: L2Norm over the head's d channels
+            if constexpr (PART == 0) {                // q, k: L2Norm over the head's d channels
                 const float2 s2 = unpack2(ss2);
                 float ss = s2.x + s2.y;
     #pragma unroll
@@ -388,7 +391,7 @@ __global__ void __launch_bounds__(kPrepWarps * 32, 6) prep_kernel(const __grid_c
             for (int u2 = 0; u2 < PER_SLOT; ++u2) token(s_begin + u2, s_begin + u2 < s_end, std::true_type{});
         }
         // beta = Sigmoid(logit) for this run's tokens and head h (the q-tensor CTAs)
-        if (m == 0 && a.beta_logit) {
+        if (PART == 0 && m == 0 && a.beta_logit) {
             const Tin *bl = static_cast<const Tin *>(a.beta_logit);
             Tin *bo = static_cast<Tin *>(a.beta);
             for (int t = t_begin + tid; t < t_end; t += kPrepWarps * 32)
@@ -465,11 +468,13 @@ __global__ void __launch_bounds__(kWarps * 32) output_gate_kernel(PostArgs a) {
 // x_qkv [T, 3, H, d] viewed as the 3-D tensor (channel, tensor-head, token).
 template <typename Tin, int D>
 cudaError_t launch_prep_d(const PrepArgs &a, cudaStream_t s) {
-    // a CTA per pair of runs of each (tensor, head), then one per empty-sequence state
-    const long long tasks = static_cast<long long>(((a.T_total + kRun - 1) / kRun + 1) / 2) * 3 * a.H +
-                            static_cast<long long>(a.N) * 3 * a.H;
-    if (tasks <= 0) return cudaSuccess;
-    if (tasks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    // per instance, a CTA per pair of runs of each of its (tensor, head)
+    // pairs, then one per empty-sequence state: q and k (2 H pairs), v (H)
+    const long long per_h = static_cast<long long>(((a.T_total + kRun - 1) / kRun + 1) / 2) +
+                            static_cast<long long>(a.N);
+    const long long tasks_qk = per_h * 2 * a.H, tasks_v = per_h * a.H;
+    if (tasks_v <= 0) return cudaSuccess;
+    if (tasks_qk > 0x7fffffffLL) return cudaErrorInvalidValue;
     auto enc = tensor_map_encoder();
     if (!enc) return cudaErrorInvalidValue;
     CUtensorMap tm;
@@ -486,11 +491,17 @@ cudaError_t launch_prep_d(const PrepArgs &a, cudaStream_t s) {
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     constexpr int smem = prep_smem_bytes<Tin, D>();
     if (smem > 48 * 1024) {
-        const cudaError_t ea = cudaFuncSetAttribute(prep_kernel<Tin, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t ea = cudaFuncSetAttribute(prep_kernel<Tin, D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (ea == cudaSuccess)
+            ea = cudaFuncSetAttribute(prep_kernel<Tin, D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (ea != cudaSuccess) return ea;
     }
-    prep_kernel<Tin, D><<<static_cast<unsigned>(tasks), kPrepWarps * 32, smem, s>>>(tm, a);
-    const cudaError_t e = cudaGetLastError();
+    prep_kernel<Tin, D, 0><<<static_cast<unsigned>(tasks_qk), kPrepWarps * 32, smem, s>>>(tm, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    count_launches(1);
+    prep_kernel<Tin, D, 1><<<static_cast<unsigned>(tasks_v), kPrepWarps * 32, smem, s>>>(tm, a);
+    e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;
 }
