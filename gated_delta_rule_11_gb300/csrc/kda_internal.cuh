@@ -44,7 +44,7 @@ struct PrefillArgs {
 enum : int {
     VSEG_ZERO_INIT = 1,   // the state entering it is zero (init_state ignored)
     VSEG_IDENT_INIT = 2,  // the state entering it is the identity (dk == dv)
-    VSEG_ZERO_V = 4,      // every value is zero (v is not read)
+    VSEG_ZERO_V = 4,      // every value is zero (V loaded past the last head: TMA zero fill)
     VSEG_OUT_TRANS = 8,   // its output rows go to out_trans (fp32)
     VSEG_OUT_ZERO = 16,   // its output rows go to out_zero (fp32)
     VSEG_EMPTY = 32,      // no chain: the CTA exits at once
