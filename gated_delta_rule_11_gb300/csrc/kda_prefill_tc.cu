@@ -139,10 +139,15 @@ static_assert(STAGE_BYTES % 1024 == 0 && ST_WQ % 1024 == 0 && ST_KD % 1024 == 0,
 constexpr uint32_t TX_BYTES = 4 * C * D * 2;        // q, k, g_raw, v tiles
 constexpr uint32_t TX_BYTES_NOZ = 3 * C * D * 2;    // q, k, v (gate per head or none)
 
+// The kernel's gate map (a compile-time instance parameter): the bounded
+// map of eq. (5), or an unbounded one (the gate is the log-decay itself, or
+// Kimi Linear's negative softplus).
+enum : int { MAP_BOUNDED = 0, MAP_LOG_DECAY = 1, MAP_NEG_SOFTPLUS = 2 };
 // log2 of the retention under an unbounded gate map: the gate itself, or
 // -softplus(e^A z) = -(max(x, 0) + log(1 + e^-|x|)), in log2 units.
-__device__ __forceinline__ float unbounded_lg(int mode, float z, float escale) {
-    if (mode == KDA_GATE_LOG_DECAY) return kLog2e * z;
+template <int Map>
+__device__ __forceinline__ float unbounded_lg(float z, float escale) {
+    if constexpr (Map == MAP_LOG_DECAY) return kLog2e * z;
     const float x = escale * z;
     return -(fmaxf(x, 0.f) * kLog2e + lg2_approx(1.f + ex2_approx(-fabsf(x) * kLog2e)));
 }
@@ -153,14 +158,14 @@ __device__ __forceinline__ void note_timeout(volatile int *flag) {
     atomicAdd(&g_tc_timeouts, 1u);
 }
 
-// Unbounded: the launch's gate map is unbounded (the per-tile pair path is
-// compiled in); the bounded instance carries none of that code.  Split: the
+// Map: the launch's gate map; an unbounded one compiles in the per-tile
+// pair path, which the bounded instance carries none of.  Split: the
 // chains are the virtual sequences of a segment split (PrefillArgs::vseg);
 // the plain instance carries none of that code either.  Ckpt: state
 // checkpoints are written (PrefillArgs::ckpt set); without it the tile loop
 // has no checkpoint test.  ChannelGate: the default gate (eq. (5), one input
 // per key channel) with the gate-shape tests constant.
-template <bool Unbounded, bool Split, bool Ckpt, bool ChannelGate>
+template <int Map, bool Split, bool Ckpt, bool ChannelGate>
 __global__ void __launch_bounds__(NTHREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_v,
@@ -199,7 +204,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // unbounded maps (the gate as the log-decay, Kimi Linear's -softplus):
     // a tile whose cumulative decay leaves fp32's range for e^{-b} takes the
     // position-pair path for L and A
-    constexpr bool unbounded = Unbounded;
+    constexpr bool unbounded = Map != MAP_BOUNDED;
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -305,19 +310,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (nv == C) gate_rows(std::true_type{});
                 else gate_rows(std::false_type{});
             } else if (z_tile) {                        // unbounded map per key channel
+                // full tiles without the row masks, as for the bounded map
+                auto gate_rows = [&](auto full) {
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int row = 8 * hh + r;
-                    const bool in = row < nv;
-                    const uint32_t zz = *reinterpret_cast<const uint32_t *>(st + ST_Z + row * 256 + c0 * 2);
-                    const uint32_t kk = in ? *reinterpret_cast<const uint32_t *>(st + ST_K + row * 256 + c0 * 2) : 0u;
-                    const uint32_t qq = in ? *reinterpret_cast<const uint32_t *>(st + ST_Q + row * 256 + c0 * 2) : 0u;
-                    kx[r] = pack2(bf16_half(kk, 0), bf16_half(kk, 1));
-                    qx[r] = pack2(bf16_half(qq, 0), bf16_half(qq, 1));
-                    suf[r] = in ? pack2(ex2_approx(unbounded_lg(a.gate_mode, bf16_half(zz, 0), escale)),
-                                        ex2_approx(unbounded_lg(a.gate_mode, bf16_half(zz, 1), escale)))
-                                : pack2(1.f, 1.f);
-                }
+                    for (int r = 0; r < 8; ++r) {
+                        const int row = 8 * hh + r;
+                        const bool in = decltype(full)::value || row < nv;
+                        const uint32_t zz = *reinterpret_cast<const uint32_t *>(st + ST_Z + row * 256 + c0 * 2);
+                        const uint32_t kk = in ? *reinterpret_cast<const uint32_t *>(st + ST_K + row * 256 + c0 * 2) : 0u;
+                        const uint32_t qq = in ? *reinterpret_cast<const uint32_t *>(st + ST_Q + row * 256 + c0 * 2) : 0u;
+                        kx[r] = pack2(bf16_half(kk, 0), bf16_half(kk, 1));
+                        qx[r] = pack2(bf16_half(qq, 0), bf16_half(qq, 1));
+                        suf[r] = in ? pack2(ex2_approx(unbounded_lg<Map>(bf16_half(zz, 0), escale)),
+                                            ex2_approx(unbounded_lg<Map>(bf16_half(zz, 1), escale)))
+                                    : pack2(1.f, 1.f);
+                    }
+                };
+                if (nv == C) gate_rows(std::true_type{});
+                else gate_rows(std::false_type{});
             } else {                                    // one gate per (token, head), or none
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
@@ -328,7 +338,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     const float z = __shfl_sync(0xffffffffu, zs, row);
                     float lg;
                     if (unbounded) {
-                        lg = unbounded_lg(a.gate_mode, z, escale);
+                        lg = unbounded_lg<Map>(z, escale);
                     } else {
                         const float sig = rcp_approx(1.f + ex2_approx(-kLog2e * escale * z));
                         lg = gate_none ? 0.f : (kLog2e * a.g_min) * sig;
@@ -392,7 +402,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const bool pair_tile =
                 unbounded && named_bar_or(pbar, 128, gC[0] < kPairThreshold || gC[1] < kPairThreshold);
 
-            if constexpr (Unbounded) if (pair_tile) {
+            if constexpr (unbounded) if (pair_tile) {
                 // L_ri = sum_c k_rc k_ic 2^{B_rc - B_ic}, A_ri = sum_c q_rc k_ic 2^{B_rc - B_ic}
                 // (i <= r, so every exponent is <= 0), B the in-tile cumulative
                 // log2-decay, stored in the K e^-b operand's place.
@@ -405,7 +415,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     const float zr = __shfl_sync(0xffffffffu, zs, row);
 #pragma unroll
                     for (int ch = 0; ch < 2; ++ch) {
-                        cum[ch] += m * unbounded_lg(a.gate_mode, z_tile ? bf16_half(zz, ch) : zr, escale);
+                        cum[ch] += m * unbounded_lg<Map>(z_tile ? bf16_half(zz, ch) : zr, escale);
                         bv[ch][r] = cum[ch];
                     }
                 }
@@ -919,14 +929,25 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     if (!a.vseg) tft = tfz = to;
     const bool unbounded = a.gate_mode == KDA_GATE_LOG_DECAY || a.gate_mode == KDA_GATE_NEG_SOFTPLUS;
     const bool channel_gate = !unbounded && a.gate_mode == KDA_GATE_BOUNDED && !a.gate_scalar;
-    auto kern = a.vseg   ? (unbounded      ? prefill_tc_kernel<true, true, false, false>
-                            : channel_gate ? prefill_tc_kernel<false, true, false, true>
-                                           : prefill_tc_kernel<false, true, false, false>)
-                : a.ckpt ? (unbounded ? prefill_tc_kernel<true, false, true, false>
-                                      : prefill_tc_kernel<false, false, true, false>)
-                         : (unbounded      ? prefill_tc_kernel<true, false, false, false>
-                            : channel_gate ? prefill_tc_kernel<false, false, false, true>
-                                           : prefill_tc_kernel<false, false, false, false>);
+    // instance <gate map, split, checkpoints, default gate>
+    using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
+                          CUtensorMap, PrefillArgs);
+    Kern kern;
+    if (unbounded) {
+        const bool ld = a.gate_mode == KDA_GATE_LOG_DECAY;
+        kern = a.vseg   ? (ld ? prefill_tc_kernel<MAP_LOG_DECAY, true, false, false>
+                              : prefill_tc_kernel<MAP_NEG_SOFTPLUS, true, false, false>)
+               : a.ckpt ? (ld ? prefill_tc_kernel<MAP_LOG_DECAY, false, true, false>
+                              : prefill_tc_kernel<MAP_NEG_SOFTPLUS, false, true, false>)
+                        : (ld ? prefill_tc_kernel<MAP_LOG_DECAY, false, false, false>
+                              : prefill_tc_kernel<MAP_NEG_SOFTPLUS, false, false, false>);
+    } else {
+        kern = a.vseg   ? (channel_gate ? prefill_tc_kernel<MAP_BOUNDED, true, false, true>
+                                        : prefill_tc_kernel<MAP_BOUNDED, true, false, false>)
+               : a.ckpt ? prefill_tc_kernel<MAP_BOUNDED, false, true, false>
+                        : (channel_gate ? prefill_tc_kernel<MAP_BOUNDED, false, false, true>
+                                        : prefill_tc_kernel<MAP_BOUNDED, false, false, false>);
+    }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(a.N) * static_cast<unsigned>(a.H));
