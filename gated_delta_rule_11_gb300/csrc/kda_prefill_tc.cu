@@ -143,6 +143,9 @@ constexpr uint32_t TX_BYTES_NOZ = 3 * C * D * 2;    // q, k, v (gate per head or
 // map of eq. (5), or an unbounded one (the gate is the log-decay itself, or
 // Kimi Linear's negative softplus).
 enum : int { MAP_BOUNDED = 0, MAP_LOG_DECAY = 1, MAP_NEG_SOFTPLUS = 2 };
+// The gate's shape (an instance parameter): decided at run time, or one
+// input per key channel, or one per (token, head).
+enum : int { SHAPE_ANY = 0, SHAPE_CHANNEL = 1, SHAPE_HEAD = 2 };
 // log2 of the retention under an unbounded gate map: the gate itself, or
 // -softplus(e^A z) = -(max(x, 0) + log(1 + e^-|x|)), in log2 units.
 template <int Map>
@@ -163,9 +166,10 @@ __device__ __forceinline__ void note_timeout(volatile int *flag) {
 // chains are the virtual sequences of a segment split (PrefillArgs::vseg);
 // the plain instance carries none of that code either.  Ckpt: state
 // checkpoints are written (PrefillArgs::ckpt set); without it the tile loop
-// has no checkpoint test.  ChannelGate: the default gate (eq. (5), one input
-// per key channel) with the gate-shape tests constant.
-template <int Map, bool Split, bool Ckpt, bool ChannelGate>
+// has no checkpoint test.  Shape: the gate's shape, runtime (SHAPE_ANY) or
+// compiled in: one input per key channel (the default gate, eq. (5)) or one
+// per (token, head), with the gate-shape tests constant.
+template <int Map, bool Split, bool Ckpt, int Shape>
 __global__ void __launch_bounds__(NTHREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_v,
@@ -199,8 +203,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const size_t state_off = static_cast<size_t>(chain) * D * D;
     // gate source: a TMA tile of per-channel inputs (eq. (5)), one input per
     // (token, head) shared by the channels, or none (alpha = 1)
-    const bool gate_none = !ChannelGate && a.gate_mode == KDA_GATE_NONE;
-    const bool z_tile = ChannelGate || (!gate_none && !a.gate_scalar);
+    const bool gate_none = Shape == SHAPE_ANY && a.gate_mode == KDA_GATE_NONE;
+    const bool z_tile = Shape == SHAPE_CHANNEL || (Shape == SHAPE_ANY && !gate_none && !a.gate_scalar);
     // unbounded maps (the gate as the log-decay, Kimi Linear's -softplus):
     // a tile whose cumulative decay leaves fp32's range for e^{-b} takes the
     // position-pair path for L and A
@@ -329,25 +333,30 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (nv == C) gate_rows(std::true_type{});
                 else gate_rows(std::false_type{});
             } else {                                    // one gate per (token, head), or none
+                auto gate_rows = [&](auto full) {
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int row = 8 * hh + r;
-                    const bool in = row < nv;
-                    const uint32_t kk = in ? *reinterpret_cast<const uint32_t *>(st + ST_K + row * 256 + c0 * 2) : 0u;
-                    const uint32_t qq = in ? *reinterpret_cast<const uint32_t *>(st + ST_Q + row * 256 + c0 * 2) : 0u;
-                    const float z = __shfl_sync(0xffffffffu, zs, row);
-                    float lg;
-                    if (unbounded) {
-                        lg = unbounded_lg<Map>(z, escale);
-                    } else {
-                        const float sig = rcp_approx(1.f + ex2_approx(-kLog2e * escale * z));
-                        lg = gate_none ? 0.f : (kLog2e * a.g_min) * sig;
+                    for (int r = 0; r < 8; ++r) {
+                        const int row = 8 * hh + r;
+                        const bool in = decltype(full)::value || row < nv;
+                        const uint32_t kk = in ? *reinterpret_cast<const uint32_t *>(st + ST_K + row * 256 + c0 * 2) : 0u;
+                        const uint32_t qq = in ? *reinterpret_cast<const uint32_t *>(st + ST_Q + row * 256 + c0 * 2) : 0u;
+                        const float z = __shfl_sync(0xffffffffu, zs, row);
+                        float lg;
+                        if (unbounded) {
+                            lg = unbounded_lg<Map>(z, escale);
+                        } else {
+                            const float sig = rcp_approx(1.f + ex2_approx(-kLog2e * escale * z));
+                            lg = gate_none ? 0.f : (kLog2e * a.g_min) * sig;
+                        }
+                        const float a_r = in ? ex2_approx(lg) : 1.f;
+                        kx[r] = pack2(bf16_half(kk, 0), bf16_half(kk, 1));
+                        qx[r] = pack2(bf16_half(qq, 0), bf16_half(qq, 1));
+                        suf[r] = pack2(a_r, a_r);
                     }
-                    const float a_r = in ? ex2_approx(lg) : 1.f;
-                    kx[r] = pack2(bf16_half(kk, 0), bf16_half(kk, 1));
-                    qx[r] = pack2(bf16_half(qq, 0), bf16_half(qq, 1));
-                    suf[r] = pack2(a_r, a_r);
-                }
+                };
+                // full tiles without the row masks only where the shape is compiled in
+                if (Shape == SHAPE_HEAD && nv == C) gate_rows(std::true_type{});
+                else gate_rows(std::false_type{});
             }
             float gC[2], inv_gC[2];
             {
@@ -929,24 +938,26 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
     if (!a.vseg) tft = tfz = to;
     const bool unbounded = a.gate_mode == KDA_GATE_LOG_DECAY || a.gate_mode == KDA_GATE_NEG_SOFTPLUS;
     const bool channel_gate = !unbounded && a.gate_mode == KDA_GATE_BOUNDED && !a.gate_scalar;
+    const bool head_gate = !unbounded && a.gate_mode == KDA_GATE_BOUNDED && a.gate_scalar;
     // instance <gate map, split, checkpoints, default gate>
     using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
                           CUtensorMap, PrefillArgs);
     Kern kern;
     if (unbounded) {
         const bool ld = a.gate_mode == KDA_GATE_LOG_DECAY;
-        kern = a.vseg   ? (ld ? prefill_tc_kernel<MAP_LOG_DECAY, true, false, false>
-                              : prefill_tc_kernel<MAP_NEG_SOFTPLUS, true, false, false>)
-               : a.ckpt ? (ld ? prefill_tc_kernel<MAP_LOG_DECAY, false, true, false>
-                              : prefill_tc_kernel<MAP_NEG_SOFTPLUS, false, true, false>)
-                        : (ld ? prefill_tc_kernel<MAP_LOG_DECAY, false, false, false>
-                              : prefill_tc_kernel<MAP_NEG_SOFTPLUS, false, false, false>);
+        kern = a.vseg   ? (ld ? prefill_tc_kernel<MAP_LOG_DECAY, true, false, SHAPE_ANY>
+                              : prefill_tc_kernel<MAP_NEG_SOFTPLUS, true, false, SHAPE_ANY>)
+               : a.ckpt ? (ld ? prefill_tc_kernel<MAP_LOG_DECAY, false, true, SHAPE_ANY>
+                              : prefill_tc_kernel<MAP_NEG_SOFTPLUS, false, true, SHAPE_ANY>)
+                        : (ld ? prefill_tc_kernel<MAP_LOG_DECAY, false, false, SHAPE_ANY>
+                              : prefill_tc_kernel<MAP_NEG_SOFTPLUS, false, false, SHAPE_ANY>);
     } else {
-        kern = a.vseg   ? (channel_gate ? prefill_tc_kernel<MAP_BOUNDED, true, false, true>
-                                        : prefill_tc_kernel<MAP_BOUNDED, true, false, false>)
-               : a.ckpt ? prefill_tc_kernel<MAP_BOUNDED, false, true, false>
-                        : (channel_gate ? prefill_tc_kernel<MAP_BOUNDED, false, false, true>
-                                        : prefill_tc_kernel<MAP_BOUNDED, false, false, false>);
+        kern = a.vseg   ? (channel_gate ? prefill_tc_kernel<MAP_BOUNDED, true, false, SHAPE_CHANNEL>
+                                        : prefill_tc_kernel<MAP_BOUNDED, true, false, SHAPE_ANY>)
+               : a.ckpt ? prefill_tc_kernel<MAP_BOUNDED, false, true, SHAPE_ANY>
+               : channel_gate ? prefill_tc_kernel<MAP_BOUNDED, false, false, SHAPE_CHANNEL>
+               : head_gate    ? prefill_tc_kernel<MAP_BOUNDED, false, false, SHAPE_HEAD>
+                              : prefill_tc_kernel<MAP_BOUNDED, false, false, SHAPE_ANY>;
     }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
