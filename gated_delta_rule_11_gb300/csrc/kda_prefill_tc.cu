@@ -403,9 +403,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 const float2 ki = unpack2(fmul2(kd2, igc));
                 *reinterpret_cast<uint32_t *>(st + ST_WQ + (wq0 ^ sw)) = pack_h2(qg.x, qg.y);
                 *reinterpret_cast<uint32_t *>(st + ST_KD + (kd0 ^ sw)) = pack_h2(kd.x, kd.y);
-                *reinterpret_cast<float2 *>(qgm + row * PADF + c0) = make_float2(to_tf32(qg.x), to_tf32(qg.y));
-                *reinterpret_cast<float2 *>(kgm + row * PADF + c0) = make_float2(to_tf32(kg.x), to_tf32(kg.y));
-                *reinterpret_cast<float2 *>(kim + row * PADF + c0) = make_float2(to_tf32(ki.x), to_tf32(ki.y));
+                *reinterpret_cast<float2 *>(qgm + row * PADF + c0) = make_float2(tf32_operand(qg.x), tf32_operand(qg.y));
+                *reinterpret_cast<float2 *>(kgm + row * PADF + c0) = make_float2(tf32_operand(kg.x), tf32_operand(kg.y));
+                *reinterpret_cast<float2 *>(kim + row * PADF + c0) = make_float2(tf32_operand(ki.x), tf32_operand(ki.y));
             }
             if (named_bar_or(pbar, 128, abort_seen)) break;   // uniform across the warpgroup
             const bool pair_tile =

@@ -50,6 +50,12 @@ __device__ __forceinline__ float to_tf32(float x) {
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(u) : "f"(x));
     return __uint_as_float(u);
 }
+// x rounded to tf32 for a tf32 mma.sync operand, which reads only the upper
+// 19 bits of each 32-bit element: adding half a tf32 ulp (bit 12) to the
+// pattern rounds those bits to nearest, ties away from zero -- the value
+// to_tf32 gives -- with one integer add; the low 13 bits are left as
+// garbage, so the result is for mma operands only.
+__device__ __forceinline__ float tf32_operand(float x) { return __uint_as_float(__float_as_uint(x) + 0x1000u); }
 // D (16x8 fp32) += A (16x8 tf32, row) * B (8x8 tf32, col)
 __device__ __forceinline__ void mma_1688_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                               uint32_t b0, uint32_t b1) {
