@@ -33,6 +33,7 @@
 // staged into shared memory by cp.async).
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
+#include "kda_tc_util.cuh"
 
 namespace kda {
 namespace {
@@ -275,8 +276,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 2 * CS) decode_kernel(DecodeAr
                 const size_t og = GenericGate && a.gate_scalar ? (static_cast<size_t>(n) * a.K + i0 + i) * a.H + h : o;
                 zc = GenericGate && a.gate_mode == KDA_GATE_NONE ? 0.f : ld_in(gz + og);
             }
-            const float alpha = expf(GenericGate ? gate_log_decay(a.gate_mode, zc, escale, a.g_min)
-                                                 : log_decay(zc, escale, a.g_min));
+            // the default gate on the MUFU path (as the tensor-core prefill):
+            // alpha = 2^(log2(e) g_min / (1 + 2^(-log2(e) e^A z)))
+            const float alpha =
+                GenericGate ? expf(gate_log_decay(a.gate_mode, zc, escale, a.g_min))
+                            : tcu::ex2_approx(tcu::kLog2e * a.g_min *
+                                              tcu::rcp_approx(1.f + tcu::ex2_approx(-tcu::kLog2e * escale * zc)));
             sm.akq[i][c] = make_float2(alpha * kc, alpha * qc);
             sm.alk[i][c] = make_float2(alpha, kc);
             float kq = kc * qc;
